@@ -1,0 +1,147 @@
+"""Python access to the float64 CPU oracle (oracle/oracle.c).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg import this package.  It shares no code with
+the CUDA library; both take their inputs from the seeded generator module.
+
+Every function takes the exact tensors the GPU sees (torch CPU tensors or
+numpy arrays, bf16 or fp32) and returns float64 numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+F32, BF16 = 0, 1
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        vp, i32p, i64p, dp = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+        cl, ci, cd = ctypes.c_long, ctypes.c_int, ctypes.c_double
+        L.oracle_decode.argtypes = [vp, ci, vp, vp, ci, cl, cl, cl, cl, cl, cd, i32p, i64p, cl, dp, dp, ci]
+        L.oracle_prefill_causal.argtypes = [vp, vp, vp, ci, cl, cl, cl, cl, cl, cd, i64p, cl, dp, dp, ci]
+        L.oracle_decode_partials.argtypes = [vp, ci, vp, vp, ci, cl, cl, cl, cl, cl, cd, i32p, cl, cl,
+                                             i64p, cl, dp, dp, dp]
+        L.oracle_combine.argtypes = [dp, dp, dp, cl, cl, cl, dp, dp]
+        for f in (L.oracle_decode, L.oracle_prefill_causal, L.oracle_decode_partials, L.oracle_combine):
+            f.restype = ci
+        _lib = L
+    return _lib
+
+
+def default_threads() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def _raw(t):
+    """(contiguous numpy array holding the exact element bits, dtype code)."""
+    try:
+        import torch
+        if isinstance(t, torch.Tensor):
+            t = t.detach().contiguous().cpu()
+            if t.dtype == torch.bfloat16:
+                return t.view(torch.int16).numpy().view(np.uint16), BF16
+            if t.dtype == torch.float32:
+                return t.numpy(), F32
+            raise TypeError(f"oracle takes bf16 or fp32 tensors, got {t.dtype}")
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(t)
+    if a.dtype == np.float32:
+        return a, F32
+    if a.dtype == np.uint16:  # raw bf16 bits
+        return a, BF16
+    raise TypeError(f"oracle takes float32 or raw-bf16 uint16 arrays, got {a.dtype}")
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with status {rc}")
+
+
+def decode(q, k, v, scale, seqlens=None, rows=None, threads=None):
+    """Decode attention. q [B,Hq,D], k/v [B,Hkv,S,D].  Returns (out [n,D], lse [n])
+    for the rows b*Hq+h listed in ``rows`` (all rows in order when None)."""
+    qa, qt = _raw(q)
+    ka, kt = _raw(k)
+    va, vt = _raw(v)
+    assert kt == vt
+    B, Hq, D = qa.shape
+    _, Hkv, S, Dk = ka.shape
+    assert Dk == D and va.shape == ka.shape and ka.shape[0] == B
+    sl = None if seqlens is None else np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
+    rw = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = B * Hq if rw is None else len(rw)
+    out = np.zeros((n, D))
+    lse = np.zeros(n)
+    rc = lib().oracle_decode(_ptr(qa), qt, _ptr(ka), _ptr(va), kt, B, Hq, Hkv, S, D, float(scale),
+                             _ptr(sl), _ptr(rw), n, _ptr(out), _ptr(lse), threads or default_threads())
+    _check(rc, "decode")
+    return out, lse
+
+
+def prefill_causal(q, k, v, scale, rows=None, threads=None):
+    """Causal prefill. q [B,H,S,D], k/v [B,Hkv,S,D].  Returns (out [n,D], lse [n]) for
+    the rows (b*H+h)*S+i listed in ``rows`` (all rows in order when None)."""
+    qa, qt = _raw(q)
+    ka, kt = _raw(k)
+    va, vt = _raw(v)
+    assert qt == kt == vt
+    B, H, S, D = qa.shape
+    _, Hkv, Sk, Dk = ka.shape
+    assert Sk == S and Dk == D and va.shape == ka.shape
+    rw = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = B * H * S if rw is None else len(rw)
+    out = np.zeros((n, D))
+    lse = np.zeros(n)
+    rc = lib().oracle_prefill_causal(_ptr(qa), _ptr(ka), _ptr(va), qt, B, H, Hkv, S, D, float(scale),
+                                     _ptr(rw), n, _ptr(out), _ptr(lse), threads or default_threads())
+    _check(rc, "prefill_causal")
+    return out, lse
+
+
+def decode_partials(q, k, v, scale, b, h, bounds, seqlens=None):
+    """Split-KV partials (m, l, o) of decode row (b, h); chunk c = [bounds[c], bounds[c+1])."""
+    qa, qt = _raw(q)
+    ka, kt = _raw(k)
+    va, vt = _raw(v)
+    B, Hq, D = qa.shape
+    _, Hkv, S, _ = ka.shape
+    bd = np.ascontiguousarray(np.asarray(bounds, dtype=np.int64))
+    N = len(bd) - 1
+    sl = None if seqlens is None else np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
+    m = np.zeros(N)
+    l = np.zeros(N)
+    o = np.zeros((N, D))
+    rc = lib().oracle_decode_partials(_ptr(qa), qt, _ptr(ka), _ptr(va), kt, B, Hq, Hkv, S, D,
+                                      float(scale), _ptr(sl), b, h, _ptr(bd), N, _ptr(m), _ptr(l), _ptr(o))
+    _check(rc, "decode_partials")
+    return m, l, o
+
+
+def combine(m, l, o):
+    """Log-sum-exp merge. m, l [R,N]; o [R,N,D] -> (out [R,D], lse [R])."""
+    m = np.ascontiguousarray(np.asarray(m, dtype=np.float64))
+    l = np.ascontiguousarray(np.asarray(l, dtype=np.float64))
+    o = np.ascontiguousarray(np.asarray(o, dtype=np.float64))
+    R, N = m.shape
+    D = o.shape[2]
+    out = np.zeros((R, D))
+    lse = np.zeros(R)
+    rc = lib().oracle_combine(_ptr(m), _ptr(l), _ptr(o), R, N, D, _ptr(out), _ptr(lse))
+    _check(rc, "combine")
+    return out, lse

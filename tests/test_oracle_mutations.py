@@ -1,0 +1,85 @@
+"""Every plausible mistake planted in a copy of the oracle is caught by a pin.
+
+Each case copies oracle/oracle.c to a temporary directory, applies one
+textual change (a dropped term, a wrong sign, a wrong index, a swapped
+operand), compiles the copy, points the oracle wrapper at it and runs all
+pins: at least one must fail.  The shipped oracle is never modified.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTATIONS = {
+    "dropped_scale": ("s[j - j0] = scale * dot;", "s[j - j0] = dot;"),
+    "exp_sign_flipped": ("sum += exp(s[j] - m);", "sum += exp(m - s[j]);"),
+    "max_not_subtracted_in_lse": ("double lse_v = m + log(sum);", "double lse_v = log(sum);"),
+    "log2_instead_of_ln": ("double lse_v = m + log(sum);", "double lse_v = m + log2(sum);"),
+    "weights_unnormalised": ("double w = exp(s[j] - lse_v);", "double w = exp(s[j] - m);"),
+    "scores_dims_reversed": ("widen(k, kv_dtype, kv_base + (size_t)j * D + d)", "widen(k, kv_dtype, kv_base + (size_t)j * D + (D - 1 - d))"),
+    "gqa_index_modulo": ("(size_t)(h / G)) * (size_t)S * D;", "(size_t)(h % job->Hkv)) * (size_t)S * D;"),
+    "seqlens_ignored": ("L = job->seqlens ? job->seqlens[b] : S;", "L = S;"),
+    "causal_excludes_diagonal": ("L = i + 1;", "L = i;"),
+    "causal_one_too_many": ("L = i + 1;", "L = (i + 2 < S) ? i + 2 : S;"),
+    "max_over_first_key_only": ("for (long j = 0; j < L; ++j)\n        if (s[j] > m)", "for (long j = 0; j < 1; ++j)\n        if (s[j] > m)"),
+    "partial_l_missing": ("lc += w;", "lc += 1.0;"),
+    "partial_o_unweighted": ("oc[d] += w * widen(v,", "oc[d] += widen(v,"),
+    "combine_l_unweighted": ("ls += lr[i] * w;", "ls += lr[i];"),
+    "combine_o_unweighted": ("out_r[d] += orow[(size_t)i * D + d] * w;", "out_r[d] += orow[(size_t)i * D + d];"),
+    "combine_all_empty_not_handled": ("if (ms == -INFINITY) {\n            lse[r] = -INFINITY;\n            continue;\n        }", ""),
+    "empty_lse_zero": ("*lse = -INFINITY;\n        return;", "*lse = 0.0;\n        return;"),
+    "bf16_low_bits_kept": ("<< 16;", "<< 15;"),
+}
+
+
+def _build_mutant(tmp_path, name, old, new):
+    text = open(SRC).read()
+    assert text.count(old) >= 1, f"mutation {name}: pattern not found"
+    src = tmp_path / f"{name}.c"
+    src.write_text(text.replace(old, new))
+    lib = tmp_path / f"{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-pthread",
+                    str(src), "-o", str(lib), "-lm"], check=True)
+    return str(lib)
+
+
+def _bf16_pin():
+    """bf16 inputs widen exactly: a bf16 tensor and its float32 copy give identical results."""
+    import numpy as np
+    import torch
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(1, 2, 8, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, 1, 9, 8, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 1, 9, 8, generator=g).to(torch.bfloat16)
+    a = oracle.decode(q, k, v, 0.5)
+    b = oracle.decode(q.float(), k.float(), v.float(), 0.5)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_bf16_widening_is_exact():
+    _bf16_pin()
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(tmp_path, monkeypatch, name):
+    old, new = MUTATIONS[name]
+    path = _build_mutant(tmp_path, name, old, new)
+    real = oracle.lib()
+    mutant = ctypes.CDLL(path)
+    for fn in ("oracle_decode", "oracle_prefill_causal", "oracle_decode_partials", "oracle_combine"):
+        getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
+        getattr(mutant, fn).restype = getattr(real, fn).restype
+    monkeypatch.setattr(oracle, "_lib", mutant)
+    caught = []
+    for pin in oracle_pins.ALL_PINS + [_bf16_pin]:
+        try:
+            pin()
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutation {name}"
