@@ -1,0 +1,406 @@
+#!/usr/bin/env python3
+"""Benchmark of the hot path on B300: split-KV decode at S = 131072 (and, when
+the build has it, the fused causal prefill at S = 16384).
+
+One step = one pass of the path over one batch of synthetic input:
+  1. the split phase: every (KV head, chunk) partial (ta_decode_partials),
+  2. the log-sum-exp merge of the partials (ta_combine),
+  3. the causal prefill of the prefill workload (ta_prefill_causal), if built.
+Each call is bracketed by CUDA events on the stream it is launched on.
+
+The JSON line's ``value`` is decode KV-cache throughput in GB/s (the K and V
+bytes a decode step must read, over the time of steps 1-2), summed over
+ranks; ``us_per_token`` is the decode time of one step; ``prefill_tflops`` the
+causal FLOPs over the prefill time.  Inputs are larger than L2 (512 MiB of
+K/V per decode step), so no flush is needed between steps.
+
+``--impl reference`` times the float64 CPU oracle on the host cores on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DECODE_WORKLOAD = "gqa_32x8_d128_s131072"
+PREFILL_WORKLOAD = "causal_prefill_32x8_d128_s16384"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_split_kernel_gqa_32x8_d128_s131072.md")
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", device_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        rows = [l for (t, l) in self.lines if t0 - 0.05 <= t <= t1 + 0.05] or [l for (_, l) in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if
+    the kernel source is unchanged since that capture; else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    kv = {}
+    for line in text.splitlines():
+        if ":" in line and line.startswith("- "):
+            key, _, val = line[2:].partition(":")
+            kv[key.strip()] = val.strip().strip("`")
+    src = os.path.join(ROOT, "long_context_decode_04_b300", "csrc", "decode.cu")
+    if kv.get("decode.cu sha256") != source_hash(src):
+        return None
+    try:
+        return int(kv["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def cpu_oracle_decode(x, rows, threads):
+    import oracle
+    t = time.perf_counter()
+    oracle.decode(x["q"], x["k"], x["v"], x["scale"], rows=rows, threads=threads)
+    return time.perf_counter() - t
+
+
+def run_reference(args, rank, world):
+    """The float64 CPU oracle on the host cores, a bounded sample per step."""
+    if rank != 0:
+        return
+    import oracle
+    from long_context_decode_04_b300 import accounting, synth
+    w = synth.WORKLOADS[DECODE_WORKLOAD]
+    x = synth.make_inputs(w)
+    rows = list(range(w.Hq))  # a whole decode step: every query head over every key
+    threads = min(oracle.default_threads(), len(rows))
+    sample_bytes = accounting.decode_kv_bytes(w.B, w.Hkv, w.D, w.S, 2)
+    for _ in range(args.warmup):
+        cpu_oracle_decode(x, rows, threads)
+    t = 0.0
+    for _ in range(args.steps):
+        t += cpu_oracle_decode(x, rows, threads)
+    gbs = sample_bytes * args.steps / t / 1e9
+    line = {"impl": "reference", "metric": "decode KV-cache GB/s at S=131072", "value": round(gbs, 4),
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{DECODE_WORKLOAD} (B=1, Hq=32, Hkv=8, D=128, S=131072, bf16 K/V)"},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": "per step: one full decode step, all 32 query heads over all "
+                                       "131072 keys (512 MiB of K/V); the oracle threads over query heads"},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-prefill", action="store_true", help="time the decode path only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from long_context_decode_04_b300 import accounting, synth, ta
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    # ---------------- decode workload (each rank runs an independent replica)
+    w = synth.WORKLOADS[DECODE_WORKLOAD]
+    x = synth.make_inputs(w)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    plan = ta.plan_decode(w.B, w.Hq, w.Hkv, w.S, w.D)
+    R, N = w.B * w.Hq, plan.n_split
+    ws = ta.decode_workspace(w.B, w.Hq, w.Hkv, w.S, w.D, device=dev)
+    pm = torch.empty((R, N), dtype=torch.float32, device=dev)
+    pl = torch.empty((R, N), dtype=torch.float32, device=dev)
+    po = torch.empty((R, N, w.D), dtype=torch.float32, device=dev)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    cws_bytes = ta.combine_workspace_bytes(R, N, w.D)
+    cws = torch.zeros(max(256, cws_bytes), dtype=torch.uint8, device=dev)
+    kv_bytes = accounting.decode_kv_bytes(w.B, w.Hkv, w.D, w.S, 2)
+    combine_levels = plan.levels
+
+    # ---------------- prefill workload
+    do_prefill = not args.no_prefill
+    pf = None
+    if do_prefill:
+        pw = synth.WORKLOADS[PREFILL_WORKLOAD]
+        y = synth.make_inputs(pw)
+        pq, pk, pv = (y[n].to(dev) for n in ("q", "k", "v"))
+        pout = torch.empty_like(pq)
+        plse = torch.empty((pw.B, pw.Hq, pw.S), dtype=torch.float32, device=dev)
+        try:
+            ta.prefill_causal(pq, pk, pv, scale=pw.scale, out=pout, lse=plse)
+            torch.cuda.synchronize()
+            pf = (pw, pq, pk, pv, pout, plse)
+        except ta.TAError as e:
+            if e.status != ta.TA_ERR_UNSUPPORTED:
+                raise
+            do_prefill = False
+    launches_per_step = 1 + combine_levels + (1 if do_prefill else 0)
+
+    def step(ev):
+        ev[0].record(stream)
+        ta.decode_partials(q, k, v, scale=w.scale, workspace=ws, m=pm, l=pl, o=po)
+        ev[1].record(stream)
+        ta.combine(pm, pl, po, workspace=cws, out=out, lse=lse)
+        ev[2].record(stream)
+        if do_prefill:
+            pw_, pq_, pk_, pv_, pout_, plse_ = pf
+            ta.prefill_causal(pq_, pk_, pv_, scale=pw_.scale, out=pout_, lse=plse_)
+        ev[3].record(stream)
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    warm = new_events()
+    for _ in range(args.warmup):
+        step(warm)
+    torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(dev)
+    dev_id = str(getattr(props, "uuid", "")) or str(local)
+    if dev_id and not dev_id.startswith("GPU-") and len(dev_id) == 36:
+        dev_id = "GPU-" + dev_id
+    sampler = ClockSampler(dev_id)
+    time.sleep(0.3)  # let the sampler start before the timed region
+
+    evs = [new_events() for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall1 = time.time()
+    clocks = sampler.stop(wall0, wall1)
+
+    total_ms = t_start.elapsed_time(t_end)
+    split_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    comb_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    pre_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    dec_total = sum(split_ms) + sum(comb_ms)
+    pre_total = sum(pre_ms)
+
+    def max_over_ranks(val):
+        if world == 1:
+            return val
+        t = torch.tensor([val], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    total_ms = max_over_ranks(total_ms)
+    dec_total = max_over_ranks(dec_total)
+    pre_total = max_over_ranks(pre_total)
+    split_avg = max_over_ranks(sum(split_ms) / len(split_ms))
+
+    # ---------------- end to end through the public single call, host buffers
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    hq = x["q"].pin_memory()
+    hk = x["k"].pin_memory()
+    hv = x["v"].pin_memory()
+    hout = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty((w.B, w.Hq), dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dws = ta.decode_workspace(w.B, w.Hq, w.Hkv, w.S, w.D, device=dev)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        ta.decode(dq, dk, dv, scale=w.scale, workspace=dws, out=out, lse=lse)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
+    d2h = hout.numel() * 2 + hlse.numel() * 4
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # ---------------- CPU baseline: the oracle, as it stands, on the host cores
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = min(oracle.default_threads(), w.Hq)  # the oracle threads over query heads
+        t_cpu = cpu_oracle_decode(x, list(range(w.Hq)), threads)
+        cpu = {"value": round(kv_bytes / t_cpu / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": "one full decode step: all 32 query heads over all 131072 keys (512 MiB of K/V)"}
+
+    dec_s = dec_total / 1e3
+    value = world * kv_bytes * args.steps / dec_s / 1e9
+    split_s = split_avg / 1e3
+    achieved = kv_bytes / split_s / 1e9
+    line = {
+        "metric": "decode KV-cache GB/s (% of B300 HBM peak) and us/token at S=131072; prefill TFLOP/s",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "accumulate": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{DECODE_WORKLOAD}: B=1, Hq=32, Hkv=8, D=128, S=131072, bf16 q/K/V N(0,1), "
+                        f"scale=1/sqrt(128)",
+            "split_kv": {"n_split": plan.n_split, "chunk": plan.chunk, "grid": plan.grid,
+                         "merge_levels": plan.levels},
+            "prefill_workload": (f"{PREFILL_WORKLOAD}: B=1, H=32, Hkv=8, D=128, S=16384, causal, bf16"
+                                 if do_prefill else "not in this build"),
+            "l2": "inputs larger than L2 (512 MiB of K/V per decode step); no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "us_per_token": round(1e3 * dec_total / args.steps, 3),
+        "decode_hbm_frac": round(value / world / peaks["hbm_gbs"], 4),
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": kv_bytes,
+                     "peak_source": peaks["source"], "avg_launch_us": round(1e3 * split_avg, 3)},
+        "combine_us": round(1e3 * sum(comb_ms) / len(comb_ms), 3),
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": round(world * kv_bytes * e2e_steps / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "call": "ta_decode_ex with pinned host buffers copied in and results copied out"},
+        "cpu_baseline": cpu,
+    }
+    if do_prefill:
+        pw = pf[0]
+        flops = accounting.prefill_causal_flops(pw.B, pw.Hq, pw.S, pw.D)
+        tflops = world * flops * args.steps / (pre_total / 1e3) / 1e12
+        line["prefill_tflops"] = round(tflops, 2)
+        line["roofline_prefill"] = {"bound": "tensor", "kernel": "prefill_causal_kernel",
+                                    "achieved": round(tflops / world, 2), "peak": peaks["bf16_tflops_sustained"],
+                                    "unit": "TFLOP/s",
+                                    "frac": round(tflops / world / peaks["bf16_tflops_sustained"], 4),
+                                    "traffic": None, "peak_source": peaks["source"] + " (sustained)",
+                                    "avg_launch_us": round(1e3 * pre_total / args.steps, 2)}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

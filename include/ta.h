@@ -1,0 +1,206 @@
+/*
+ * ta.h -- C ABI of the split-KV exact attention library for B300 (sm_103a).
+ *
+ * The library computes exact scaled-dot-product softmax attention for
+ * long-context inference on one GPU:
+ *
+ *   - decode: one query per (sequence, query head) against a long KV cache,
+ *     computed split-KV: each KV chunk yields a partial (running max m,
+ *     sum of exponentials l, unnormalised output o) and the partials are
+ *     merged by a log-sum-exp tree reduction;
+ *   - the merge itself, exposed for caller-supplied partials;
+ *   - causal prefill: fused QK^T * scale -> softmax -> V on the tensor cores.
+ *
+ * Definition (Attention glossary, jisaku.com/glossary/attention, section
+ * "basic concepts and operating principle"): the query's inner product with
+ * each key gives a score; softmax turns scores into weights; the output is
+ * the weighted mean of the value vectors.  With s_j = scale * <q, k_j> over
+ * the attended keys:
+ *
+ *   lse = ln sum_j exp(s_j)         (natural log, in scaled-logit units)
+ *   out = sum_j exp(s_j - lse) v_j
+ *
+ * The split into chunks and the merge are exact reformulations, not
+ * approximations (Tree Attention explainer, aibr.jp/archives/143699,
+ * sections 1-3: attention's log-sum-exp "energy" is reduced along the
+ * sequence axis as an associative tree; section 2: the method is exact).
+ *
+ * Conventions for every entry point
+ *   - All tensors are row-major and contiguous, in device memory unless
+ *     stated, owned by the caller.  The library never frees caller memory.
+ *   - Grouped-query attention: with G = Hq / Hkv, query head h reads KV
+ *     head floor(h / G).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; no entry point
+ *     synchronises the device on the compute path.
+ *   - Errors: every entry point returns a ta_status and never aborts the
+ *     process.  Arguments are validated before anything is launched; a
+ *     rejected call launches nothing.  A launch failure is reported as
+ *     TA_ERR_CUDA.  ta_last_error() gives a message for the calling thread's
+ *     last non-OK status.
+ */
+#ifndef TA_H
+#define TA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TA_OK = 0,
+    TA_ERR_INVALID_ARG = 1,  /* bad sizes, null or misaligned pointers   */
+    TA_ERR_UNSUPPORTED = 2,  /* valid, but a shape this build has no kernel for */
+    TA_ERR_WORKSPACE = 3,    /* caller workspace missing or too small     */
+    TA_ERR_CUDA = 4          /* a CUDA runtime call or launch failed      */
+} ta_status;
+
+typedef enum { TA_F32 = 0, TA_BF16 = 1 } ta_dtype;
+
+/* Device-side conditions recorded in the workspace status word (bit set). */
+enum {
+    TA_DEVERR_SEQLEN = 1,   /* some seqlens[b] < 0 or > S; clamped to [0, S]     */
+    TA_DEVERR_TIMEOUT = 2   /* a pipeline wait exceeded its time limit; output invalid */
+};
+
+/*
+ * Split-KV plan chosen by the KV-chunk scheduler.  Chunk c of a sequence
+ * covers keys [c * chunk, min((c + 1) * chunk, S)).  The merge runs in
+ * `levels` launches of fan-in <= `fanin` (0 levels: one chunk, the decode
+ * kernel writes the result itself).
+ */
+typedef struct {
+    int32_t n_split;        /* chunks per (sequence, KV head)                */
+    int32_t chunk;          /* keys per chunk                                */
+    int32_t levels;         /* merge launches after the decode kernel        */
+    int32_t fanin;          /* partials merged by one warp in one level      */
+    int32_t grid;           /* CTAs of the persistent decode kernel          */
+    int32_t sm_count;       /* SMs the plan was made for                     */
+    size_t workspace_bytes; /* device scratch the call needs                 */
+} ta_decode_plan;
+
+/*
+ * Full parameter set of a decode call.
+ *   q    [B, Hq, D]        in_dtype
+ *   k, v [B, Hkv, S, D]    in_dtype (rows at or past seqlens[b] are never read)
+ *   out  [B, Hq, D]        out_dtype
+ *   lse  [B, Hq]           fp32, may be NULL
+ *   seqlens [B] int32 on the device, may be NULL (= every sequence has S keys);
+ *     seqlens[b] = 0 gives out = 0 and lse = -inf.  Values outside [0, S]
+ *     are clamped on the device and TA_DEVERR_SEQLEN is recorded.
+ *   chunk / n_split: 0 = scheduler default; chunk > 0 forces keys per chunk
+ *     (takes precedence), else n_split > 0 forces the number of chunks.
+ *   workspace: device scratch of at least ta_decode_plan.workspace_bytes,
+ *     256-byte aligned, whose first 256 bytes (the status word) the caller
+ *     zeroes once when it sets the workspace up.  NULL = use the library's
+ *     own per-device workspace (grown on demand with cudaMalloc, which
+ *     synchronises; calls using it on different streams must not overlap).
+ * Supported: D in {64, 128}; in_dtype = out_dtype family F32 or BF16
+ * (out may be F32 for BF16 inputs); G in {1, 2, 4} for D = 128 and
+ * G in {1, 2, 4, 8} for D = 64.  Pointers q, k, v, out 16-byte aligned.
+ */
+typedef struct {
+    const void *q;
+    const void *k;
+    const void *v;
+    void *out;
+    float *lse;
+    int32_t B, Hq, Hkv, S, D;
+    float scale;
+    const int32_t *seqlens;
+    ta_dtype in_dtype;
+    ta_dtype out_dtype;
+    int32_t chunk;
+    int32_t n_split;
+    void *workspace;
+    size_t workspace_bytes;
+    void *stream;
+} ta_decode_params;
+
+/*
+ * Split-KV decode, bf16 q/K/V/out, default plan, library workspace.
+ * Exact attention of each of the B*Hq queries over keys [0, L_b) of its KV
+ * head, L_b = seqlens[b] or S.  Layouts and rules as in ta_decode_params.
+ */
+ta_status ta_decode(const void *q, const void *k, const void *v, void *out, float *lse,
+                    int B, int Hq, int Hkv, int S, int D, float scale,
+                    const int32_t *seqlens, void *stream);
+
+/* Split-KV decode with every option of ta_decode_params. */
+ta_status ta_decode_ex(const ta_decode_params *p);
+
+/*
+ * The split phase alone: every (sequence b, query head h, chunk c) partial
+ * of ta_decode_ex, written to caller buffers and not merged.
+ *   m, l [B*Hq, n_split] fp32, o [B*Hq, n_split, D] fp32, row r = b*Hq + h,
+ *   with n_split the plan's (ta_decode_plan_for with the same chunk /
+ *   n_split / seqlens choice).  m is in natural-log units; an empty chunk
+ *   gives m = -inf, l = 0, o = 0.  Merging them with ta_combine gives the
+ *   decode result.  p->out and p->lse are ignored; p->workspace may be NULL
+ *   or any zeroed 256-byte-aligned buffer of >= 256 bytes (only its status
+ *   word is used).  o 16-byte aligned; m, l 4-byte aligned.
+ */
+ta_status ta_decode_partials(const ta_decode_params *p, float *m, float *l, float *o);
+
+/*
+ * The plan ta_decode_ex would use (pure host computation; launches nothing).
+ * varlen != 0 when seqlens will be passed (the chunking then
+ * over-decomposes, since lengths are only known on the device).
+ * sm_count = 0 queries the current device.  chunk / n_split as in
+ * ta_decode_params.
+ */
+ta_status ta_decode_plan_for(int B, int Hq, int Hkv, int S, int D, int chunk, int n_split, int varlen,
+                             int sm_count, ta_decode_plan *plan);
+
+/* Workspace bytes of ta_decode_plan_for(...) on the current device (0 on error). */
+size_t ta_decode_workspace_bytes(int B, int Hq, int Hkv, int S, int D, int chunk, int n_split,
+                                 int varlen);
+
+/*
+ * Read and clear the device status word (TA_DEVERR_* bits) of a decode
+ * workspace (NULL = the library's own workspace of the current device).
+ * Synchronises `stream` first.
+ */
+ta_status ta_decode_status(void *workspace, void *stream, int32_t *flags);
+
+/*
+ * Log-sum-exp merge of N split-KV partials for each of R rows (the tree
+ * combine of the Tree Attention explainer, sections 1 and 3, on one GPU):
+ *   m, l [R, N] fp32 (m natural-log units; any finite reference point, or
+ *   -inf with l = 0 for an empty partial), o [R, N, D] fp32 unnormalised.
+ *   m* = max_i m_i, l* = sum_i l_i e^(m_i - m*), o* = sum_i o_i e^(m_i - m*)
+ *   out [R, D] (out_dtype) = o* / l*;  lse [R] = m* + ln l* (may be NULL).
+ *   A row whose partials are all empty gives out = 0, lse = -inf.
+ * Fan-in <= 64 is one warp per row; larger N merges in levels of 64, with
+ * intermediates in `workspace` (>= ta_combine_workspace_bytes(R, N, D);
+ * NULL = library workspace).  D in {64, 128}; R >= 1; N >= 1.
+ */
+ta_status ta_combine(const float *m, const float *l, const float *o, int R, int N, int D,
+                     void *out, ta_dtype out_dtype, float *lse,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Scratch bytes ta_combine needs for (R, N, D); 0 when no level writes intermediates. */
+size_t ta_combine_workspace_bytes(int R, int N, int D);
+
+/*
+ * Causal prefill, fused QK^T * scale -> softmax -> PV on the tensor cores
+ * (the fusion of matmul, scaling and softmax that the Grayskull SRAM
+ * attention explainer, aibr.jp/archives/146339, section 3, describes),
+ * bf16 in and out, fp32 accumulation.
+ *   q, out [B, H, S, D] bf16; k, v [B, Hkv, S, D] bf16; lse [B, H, S] fp32
+ *   (may be NULL).  Query row i attends keys 0..i (top-left aligned, square).
+ * Supported: D = 128; H % Hkv == 0; S >= 1; pointers 16-byte aligned.
+ */
+ta_status ta_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse,
+                            int B, int H, int Hkv, int S, int D, float scale, void *stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char *ta_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TA_H */

@@ -1,0 +1,228 @@
+"""Python binding of the C ABI in include/ta.h (ctypes; argument marshalling only).
+
+Every step of the computation runs in the CUDA kernels of libta.so; this
+module only allocates outputs and workspaces with torch, passes raw device
+pointers and the current CUDA stream, and turns a non-OK status into an
+exception.  There is no fallback: if libta.so is missing the import of
+``lib()`` fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libta.so")
+
+TA_OK, TA_ERR_INVALID_ARG, TA_ERR_UNSUPPORTED, TA_ERR_WORKSPACE, TA_ERR_CUDA = range(5)
+TA_F32, TA_BF16 = 0, 1
+TA_DEVERR_SEQLEN, TA_DEVERR_TIMEOUT = 1, 2
+STATUS_NAMES = {0: "TA_OK", 1: "TA_ERR_INVALID_ARG", 2: "TA_ERR_UNSUPPORTED", 3: "TA_ERR_WORKSPACE",
+                4: "TA_ERR_CUDA"}
+
+
+class TAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class DecodePlan(ctypes.Structure):
+    _fields_ = [("n_split", ctypes.c_int32), ("chunk", ctypes.c_int32), ("levels", ctypes.c_int32),
+                ("fanin", ctypes.c_int32), ("grid", ctypes.c_int32), ("sm_count", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+class DecodeParams(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("S", ctypes.c_int32), ("D", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("seqlens", ctypes.c_void_p), ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("chunk", ctypes.c_int32), ("n_split", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("stream", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libta.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with long_context_decode_04_b300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, st, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+        L.ta_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
+        L.ta_decode_ex.argtypes = [ctypes.POINTER(DecodeParams)]
+        L.ta_decode_partials.argtypes = [ctypes.POINTER(DecodeParams), vp, vp, vp]
+        L.ta_decode_plan_for.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.POINTER(DecodePlan)]
+        L.ta_decode_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        L.ta_decode_workspace_bytes.restype = st
+        L.ta_decode_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+        L.ta_combine.argtypes = [vp, vp, vp, i, i, i, vp, i, vp, vp, st, vp]
+        L.ta_combine_workspace_bytes.argtypes = [i, i, i]
+        L.ta_combine_workspace_bytes.restype = st
+        L.ta_prefill_causal.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        L.ta_last_error.argtypes = []
+        L.ta_last_error.restype = ctypes.c_char_p
+        for fn in ("ta_decode", "ta_decode_ex", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
+                   "ta_prefill_causal"):
+            getattr(L, fn).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != TA_OK:
+        raise TAError(status, lib().ta_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return TA_BF16
+    if dt == torch.float32:
+        return TA_F32
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def plan_decode(B, Hq, Hkv, S, D, *, chunk=0, n_split=0, varlen=False, sm_count=0) -> DecodePlan:
+    """The split-KV plan the library would use (host computation only)."""
+    p = DecodePlan()
+    _check(lib().ta_decode_plan_for(B, Hq, Hkv, S, D, chunk, n_split, int(bool(varlen)), sm_count,
+                                    ctypes.byref(p)))
+    return p
+
+
+def decode_workspace(B, Hq, Hkv, S, D, *, chunk=0, n_split=0, varlen=False, device="cuda") -> torch.Tensor:
+    """A zeroed device workspace big enough for ``decode(..., workspace=...)``."""
+    plan = plan_decode(B, Hq, Hkv, S, D, chunk=chunk, n_split=n_split, varlen=varlen)
+    return torch.zeros(max(256, plan.workspace_bytes), dtype=torch.uint8, device=device)
+
+
+def decode(q, k, v, *, seqlens=None, scale=None, out_dtype=None, chunk=0, n_split=0, workspace=None,
+           out=None, lse=None):
+    """Split-KV decode.  q [B,Hq,D], k/v [B,Hkv,S,D] (bf16 or fp32, CUDA), seqlens [B] int32.
+
+    Returns (out [B,Hq,D], lse [B,Hq] fp32).  ``workspace`` (uint8 CUDA tensor
+    from ``decode_workspace``) makes the call allocation-free; without it the
+    library uses its own per-device workspace.
+    """
+    B, Hq, D = q.shape
+    _, Hkv, S, _ = k.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    p = DecodeParams()
+    p.q, p.k, p.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    p.out, p.lse = out.data_ptr(), lse.data_ptr()
+    p.B, p.Hq, p.Hkv, p.S, p.D = B, Hq, Hkv, S, D
+    p.scale = scale
+    p.seqlens = seqlens.data_ptr() if seqlens is not None else None
+    p.in_dtype = _dtype_code(q.dtype)
+    p.out_dtype = _dtype_code(out.dtype)
+    p.chunk, p.n_split = chunk, n_split
+    if workspace is not None:
+        p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    p.stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(lib().ta_decode_ex(ctypes.byref(p)))
+    return out, lse
+
+
+def _params(q, k, v, seqlens, scale, chunk, n_split, workspace, out=None, lse=None, out_dtype=None):
+    B, Hq, D = q.shape
+    _, Hkv, S, _ = k.shape
+    p = DecodeParams()
+    p.q, p.k, p.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    p.out = out.data_ptr() if out is not None else None
+    p.lse = lse.data_ptr() if lse is not None else None
+    p.B, p.Hq, p.Hkv, p.S, p.D = B, Hq, Hkv, S, D
+    p.scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    p.seqlens = seqlens.data_ptr() if seqlens is not None else None
+    p.in_dtype = _dtype_code(q.dtype)
+    p.out_dtype = _dtype_code(out_dtype if out_dtype is not None else q.dtype)
+    p.chunk, p.n_split = chunk, n_split
+    if workspace is not None:
+        p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    p.stream = torch.cuda.current_stream(q.device).cuda_stream
+    return p
+
+
+def decode_partials(q, k, v, *, seqlens=None, scale=None, chunk=0, n_split=0, workspace=None,
+                    m=None, l=None, o=None):
+    """The split phase alone: (m, l [B*Hq, n_split], o [B*Hq, n_split, D]) fp32 partials."""
+    B, Hq, D = q.shape
+    _, Hkv, S, _ = k.shape
+    plan = plan_decode(B, Hq, Hkv, S, D, chunk=chunk, n_split=n_split, varlen=seqlens is not None)
+    N = plan.n_split
+    if m is None:
+        m = torch.empty((B * Hq, N), dtype=torch.float32, device=q.device)
+        l = torch.empty((B * Hq, N), dtype=torch.float32, device=q.device)
+        o = torch.empty((B * Hq, N, D), dtype=torch.float32, device=q.device)
+    p = _params(q, k, v, seqlens, scale, chunk, n_split, workspace)
+    _check(lib().ta_decode_partials(ctypes.byref(p), _ptr(m), _ptr(l), _ptr(o)))
+    return m, l, o
+
+
+def decode_bf16(q, k, v, out, lse, scale, seqlens=None):
+    """The plain ``ta_decode`` entry point (bf16 in and out, library workspace)."""
+    B, Hq, D = q.shape
+    _, Hkv, S, _ = k.shape
+    _check(lib().ta_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, D, float(scale),
+                           _ptr(seqlens), _stream(q.device)))
+    return out, lse
+
+
+def decode_status(workspace=None, device="cuda") -> int:
+    """Read and clear the device status word (TA_DEVERR_* bits)."""
+    flags = ctypes.c_int32(0)
+    _check(lib().ta_decode_status(_ptr(workspace), _stream(torch.device(device)), ctypes.byref(flags)))
+    return flags.value
+
+
+def combine(m, l, o, *, out_dtype=torch.float32, workspace=None, out=None, lse=None):
+    """Log-sum-exp merge of partials m, l [R,N], o [R,N,D] (fp32, CUDA) -> (out [R,D], lse [R])."""
+    R, N = m.shape
+    D = o.shape[2]
+    if out is None:
+        out = torch.empty((R, D), dtype=out_dtype, device=m.device)
+    if lse is None:
+        lse = torch.empty((R,), dtype=torch.float32, device=m.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().ta_combine(_ptr(m), _ptr(l), _ptr(o), R, N, D, _ptr(out), _dtype_code(out.dtype), _ptr(lse),
+                            _ptr(workspace), ws_bytes, _stream(m.device)))
+    return out, lse
+
+
+def combine_workspace_bytes(R, N, D) -> int:
+    return int(lib().ta_combine_workspace_bytes(R, N, D))
+
+
+def prefill_causal(q, k, v, *, scale=None, out=None, lse=None):
+    """Causal prefill. q [B,H,S,D], k/v [B,Hkv,S,D] bf16 CUDA -> (out [B,H,S,D] bf16, lse [B,H,S] fp32)."""
+    B, H, S, D = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    _check(lib().ta_prefill_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, S, D, scale,
+                                   _stream(q.device)))
+    return out, lse

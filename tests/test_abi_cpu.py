@@ -1,0 +1,133 @@
+"""The C ABI on the host: exported symbols, the KV-chunk scheduler, and argument
+validation (which rejects bad calls before any CUDA call, so it runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from long_context_decode_04_b300 import ta
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "ta.h")
+SMS = 148
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(ta_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert {"ta_decode", "ta_decode_ex", "ta_combine", "ta_prefill_causal", "ta_last_error"} <= set(names)
+    L = ctypes.CDLL(ta.LIB_PATH)
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, f"declared in include/ta.h but not exported: {missing}"
+
+
+def _chunks(plan, S):
+    return [(c * plan.chunk, min((c + 1) * plan.chunk, S)) for c in range(plan.n_split)]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D", [
+    (1, 32, 8, 131072, 128), (16, 32, 8, 32768, 128), (1, 32, 8, 1 << 20, 128), (1, 1, 1, 4096, 64),
+    (1, 1, 1, 1, 64), (3, 4, 2, 255, 128), (2, 8, 8, 257, 64), (1, 32, 8, 1000, 128), (64, 32, 8, 8192, 128)])
+@pytest.mark.parametrize("varlen", [False, True])
+def test_plan_covers_every_key_once(B, Hq, Hkv, S, D, varlen):
+    plan = ta.plan_decode(B, Hq, Hkv, S, D, varlen=varlen, sm_count=SMS)
+    ch = _chunks(plan, S)
+    assert ch[0][0] == 0 and ch[-1][1] == S
+    for (a0, a1), (b0, b1) in zip(ch, ch[1:]):
+        assert a1 == b0 and a0 < a1  # contiguous, non-empty, no overlap
+    assert ch[-1][0] < ch[-1][1]
+    items = B * Hkv * plan.n_split
+    assert plan.grid == min(items, SMS)
+    if plan.n_split == 1:
+        assert plan.levels == 0
+    else:
+        n, lv = plan.n_split, 1
+        while n > plan.fanin:
+            n, lv = -(-n // plan.fanin), lv + 1
+        assert plan.levels == lv
+    if S >= 256 * SMS and not varlen:
+        assert items >= SMS  # every SM gets work
+
+
+def test_plan_of_the_128k_workload_fills_the_sms_evenly():
+    plan = ta.plan_decode(1, 32, 8, 131072, 128, sm_count=SMS)
+    items = 8 * plan.n_split
+    assert items % SMS == 0 and plan.grid == SMS
+    assert plan.chunk % 64 == 0 and plan.chunk >= 256
+
+
+def test_plan_overrides():
+    p = ta.plan_decode(1, 32, 8, 1 << 20, 128, chunk=256, sm_count=SMS)
+    assert p.chunk == 256 and p.n_split == 4096 and p.levels == 2
+    p = ta.plan_decode(1, 32, 8, 1000, 128, n_split=7, sm_count=SMS)
+    assert p.n_split == 7 and p.chunk == 143
+    p = ta.plan_decode(1, 32, 8, 5, 128, n_split=9, sm_count=SMS)  # more splits than keys
+    assert p.n_split == 5 and p.chunk == 1
+
+
+def test_workspace_size_formula():
+    def a256(x):
+        return (x + 255) // 256 * 256
+    B, Hq, Hkv, S, D = 1, 32, 8, 1 << 20, 128
+    p = ta.plan_decode(B, Hq, Hkv, S, D, chunk=256, sm_count=SMS)
+    R, N = B * Hq, p.n_split
+    n1 = -(-N // 64)
+    comb = 2 * (2 * a256(4 * R * n1) + a256(4 * R * n1 * D))
+    assert p.workspace_bytes == 256 + 2 * a256(4 * R * N) + a256(4 * R * N * D) + comb
+    p1 = ta.plan_decode(1, 1, 1, 100, 64, sm_count=SMS)
+    assert p1.n_split == 1 and p1.workspace_bytes == 256
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=6, Hkv=4), ta.TA_ERR_INVALID_ARG),
+    (dict(S=0), ta.TA_ERR_INVALID_ARG),
+    (dict(B=0), ta.TA_ERR_INVALID_ARG),
+    (dict(D=96), ta.TA_ERR_UNSUPPORTED),
+    (dict(Hq=16, Hkv=2, D=128), ta.TA_ERR_UNSUPPORTED),
+    (dict(q=0x1008), ta.TA_ERR_INVALID_ARG),
+    (dict(k=None), ta.TA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), ta.TA_ERR_INVALID_ARG),
+    (dict(chunk=-1), ta.TA_ERR_INVALID_ARG),
+    (dict(in_dtype=7), ta.TA_ERR_INVALID_ARG),
+    (dict(in_dtype=ta.TA_F32, out_dtype=ta.TA_BF16), ta.TA_ERR_UNSUPPORTED),
+])
+def test_decode_rejects_bad_arguments_before_launch(kw, status):
+    base = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, B=1, Hq=8, Hkv=2, S=64, D=128,
+                scale=0.1, seqlens=None, in_dtype=ta.TA_BF16, out_dtype=ta.TA_BF16, chunk=0, n_split=0,
+                workspace=None, workspace_bytes=0, stream=None)
+    base.update(kw)
+    p = ta.DecodeParams(**base)
+    rc = ta.lib().ta_decode_ex(ctypes.byref(p))
+    assert rc == status
+    assert len(ta.lib().ta_last_error()) > 0
+
+
+def test_combine_and_prefill_reject_bad_arguments():
+    L = ta.lib()
+    vp = ctypes.c_void_p
+    assert L.ta_combine(vp(0x1000), vp(0x2000), vp(0x3000), 4, 0, 128, vp(0x4000), ta.TA_F32, None, None, 0,
+                        None) == ta.TA_ERR_INVALID_ARG
+    assert L.ta_combine(vp(0x1000), vp(0x2000), vp(0x3000), 4, 2, 96, vp(0x4000), ta.TA_F32, None, None, 0,
+                        None) == ta.TA_ERR_UNSUPPORTED
+    assert L.ta_combine(None, vp(0x2000), vp(0x3000), 4, 2, 128, vp(0x4000), ta.TA_F32, None, None, 0,
+                        None) == ta.TA_ERR_INVALID_ARG
+    assert L.ta_prefill_causal(vp(0x1000), vp(0x2000), vp(0x3000), vp(0x4000), None, 1, 6, 4, 128, 128,
+                               ctypes.c_float(0.1), None) == ta.TA_ERR_INVALID_ARG
+    assert L.ta_prefill_causal(vp(0x1000), vp(0x2000), vp(0x3000), vp(0x4000), None, 1, 8, 2, 128, 64,
+                               ctypes.c_float(0.1), None) == ta.TA_ERR_UNSUPPORTED
+    assert L.ta_prefill_causal(vp(0x1004), vp(0x2000), vp(0x3000), vp(0x4000), None, 1, 8, 2, 128, 128,
+                               ctypes.c_float(0.1), None) == ta.TA_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_valid_call_without_gpu_reports_cuda_error():
+    p = ta.DecodeParams(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, B=1, Hq=8, Hkv=2, S=64, D=128,
+                        scale=0.1, in_dtype=ta.TA_BF16, out_dtype=ta.TA_BF16)
+    assert ta.lib().ta_decode_ex(ctypes.byref(p)) == ta.TA_ERR_CUDA
+    assert b"cuda" in ta.lib().ta_last_error().lower()
