@@ -128,6 +128,33 @@ ta_status ta_decode(const void *q, const void *k, const void *v, void *out, floa
                     int B, int Hq, int Hkv, int S, int D, float scale,
                     const int32_t *seqlens, void *stream);
 
+/*
+ * Split-KV decode like ta_decode (bf16 q/K/V/out, fp32 lse, default plan),
+ * for callers that cannot allocate device memory: it calls no cudaMalloc,
+ * cudaFree or other allocating routine.  (The pages this library follows
+ * describe no such entry point; it exists for deployment reasons only.)
+ * Such callers include programs whose GPU memory is already reserved by a
+ * pool allocator (a framework's caching allocator, a serving arena), loops
+ * that cannot afford the device-wide synchronisation an allocation can
+ * cause, and deployments that forbid allocation after start-up.
+ *   Scratch: a fixed 8 MiB array in this library's device code, reserved on
+ *   every GPU that loads the library and held until the process exits.  A
+ *   shape whose plan needs more (ta_decode_workspace_bytes(B, Hq, Hkv, S, D,
+ *   0, 0, seqlens != NULL) > 8 MiB) is rejected with TA_ERR_WORKSPACE and
+ *   nothing is launched; such shapes need ta_decode or ta_decode_ex.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address with that device current; make that first call before any
+ *   stream capture.
+ *   Every call clears the scratch's status word on `stream` before the
+ *   kernels run.  All calls on one GPU share the one array: calls that may
+ *   overlap on the GPU (different streams or host threads with no ordering
+ *   between them) race on it and give wrong results.
+ * Arguments, layouts, alignment and errors as for ta_decode.
+ */
+ta_status ta_decode_noalloc(const void *q, const void *k, const void *v, void *out, float *lse,
+                            int B, int Hq, int Hkv, int S, int D, float scale,
+                            const int32_t *seqlens, void *stream);
+
 /* Split-KV decode with every option of ta_decode_params. */
 ta_status ta_decode_ex(const ta_decode_params *p);
 

@@ -149,6 +149,10 @@ ta_status validate_decode(const ta_decode_params *p)
 
 }  // namespace
 
+void ta::record_error(const std::string &msg) { g_error = msg; }
+
+ta_status ta::check_decode_params(const ta_decode_params *p) { return validate_decode(p); }
+
 extern "C" {
 
 const char *ta_last_error(void) { return g_error.c_str(); }

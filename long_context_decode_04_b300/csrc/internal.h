@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <string>
 #include <cuda_runtime.h>
 
 #include "../../include/ta.h"
@@ -26,6 +27,13 @@ struct DecodeLaunch {
     bool force_partials;               // write partials even when n_split == 1
     cudaStream_t stream;
 };
+
+// Set the calling thread's message returned by ta_last_error (api.cpp).
+void record_error(const std::string &msg);
+
+// The argument checks of ta_decode_ex, on their own (api.cpp): TA_OK or the
+// status (with its message recorded) that ta_decode_ex would return.
+ta_status check_decode_params(const ta_decode_params *p);
 
 // Scheduler (sched.cpp).
 ta_status plan_decode(int B, int Hq, int Hkv, int S, int D, int chunk, int n_split, int varlen,

@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         vp, i, st, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
         L.ta_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
+        L.ta_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
         L.ta_decode_ex.argtypes = [ctypes.POINTER(DecodeParams)]
         L.ta_decode_partials.argtypes = [ctypes.POINTER(DecodeParams), vp, vp, vp]
         L.ta_decode_plan_for.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.POINTER(DecodePlan)]
@@ -71,7 +72,7 @@ def lib() -> ctypes.CDLL:
         L.ta_prefill_causal.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         L.ta_last_error.argtypes = []
         L.ta_last_error.restype = ctypes.c_char_p
-        for fn in ("ta_decode", "ta_decode_ex", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
+        for fn in ("ta_decode", "ta_decode_noalloc", "ta_decode_ex", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
                    "ta_prefill_causal"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
@@ -186,6 +187,15 @@ def decode_bf16(q, k, v, out, lse, scale, seqlens=None):
     _, Hkv, S, _ = k.shape
     _check(lib().ta_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, D, float(scale),
                            _ptr(seqlens), _stream(q.device)))
+    return out, lse
+
+
+def decode_noalloc(q, k, v, out, lse, scale, seqlens=None):
+    """``ta_decode_noalloc``: bf16 decode whose scratch is the library's fixed device array."""
+    B, Hq, D = q.shape
+    _, Hkv, S, _ = k.shape
+    _check(lib().ta_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, D,
+                                   float(scale), _ptr(seqlens), _stream(q.device)))
     return out, lse
 
 
