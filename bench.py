@@ -171,8 +171,8 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true", help="time the decode path only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -238,15 +238,43 @@ def main():
             do_prefill = False
     launches_per_step = 1 + combine_levels + (1 if do_prefill else 0)
 
+    def run_split():
+        ta.decode_partials(q, k, v, scale=w.scale, workspace=ws, m=pm, l=pl, o=po)
+
+    def run_combine():
+        ta.combine(pm, pl, po, workspace=cws, out=out, lse=lse)
+
+    def run_prefill():
+        pw_, pq_, pk_, pv_, pout_, plse_ = pf
+        ta.prefill_causal(pq_, pk_, pv_, scale=pw_.scale, out=pout_, lse=plse_)
+
+    for _ in range(args.warmup):
+        run_split()
+        run_combine()
+        if do_prefill:
+            run_prefill()
+    torch.cuda.synchronize()
+
+    # Each phase is captured once into a CUDA graph, so that a timed step is
+    # a few graph launches and the host never holds the GPU back: the events
+    # between replays then measure device time only.
+    graphs = []
+    for fn in (run_split, run_combine) + ((run_prefill,) if do_prefill else ()):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+
     def step(ev):
         ev[0].record(stream)
-        ta.decode_partials(q, k, v, scale=w.scale, workspace=ws, m=pm, l=pl, o=po)
+        graphs[0].replay()
         ev[1].record(stream)
-        ta.combine(pm, pl, po, workspace=cws, out=out, lse=lse)
+        graphs[1].replay()
         ev[2].record(stream)
         if do_prefill:
-            pw_, pq_, pk_, pv_, pout_, plse_ = pf
-            ta.prefill_causal(pq_, pk_, pv_, scale=pw_.scale, out=pout_, lse=plse_)
+            graphs[2].replay()
         ev[3].record(stream)
 
     def new_events():

@@ -62,7 +62,8 @@ typedef enum { TA_F32 = 0, TA_BF16 = 1 } ta_dtype;
 /* Device-side conditions recorded in the workspace status word (bit set). */
 enum {
     TA_DEVERR_SEQLEN = 1,   /* some seqlens[b] < 0 or > S; clamped to [0, S]     */
-    TA_DEVERR_TIMEOUT = 2   /* a pipeline wait exceeded its time limit; output invalid */
+    TA_DEVERR_TIMEOUT = 2,  /* a pipeline wait exceeded its time limit; output invalid */
+    TA_DEVERR_RANGE = 4     /* prefill: some |V| > 65280 (outside fp16); output undefined */
 };
 
 /*
@@ -218,7 +219,12 @@ size_t ta_combine_workspace_bytes(int R, int N, int D);
  * bf16 in and out, fp32 accumulation.
  *   q, out [B, H, S, D] bf16; k, v [B, Hkv, S, D] bf16; lse [B, H, S] fp32
  *   (may be NULL).  Query row i attends keys 0..i (top-left aligned, square).
- * Supported: D = 128; H % Hkv == 0; S >= 1; pointers 16-byte aligned.
+ * The softmax weights P enter the PV product as fp16 (relative rounding
+ * 2^-12), with V converted to fp16 on chip; |V| must be <= 65280.
+ * Supported: D = 128; H % Hkv == 0; S >= 1; scale > 0; q, k, v, out
+ * 16-byte aligned.  The library's status word (read with
+ * ta_decode_status(NULL, ...)) records TA_DEVERR_TIMEOUT if a pipeline wait
+ * gave up and TA_DEVERR_RANGE if some |V| exceeded the fp16 range.
  */
 ta_status ta_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse,
                             int B, int H, int Hkv, int S, int D, float scale, void *stream);

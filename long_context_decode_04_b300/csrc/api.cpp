@@ -412,6 +412,8 @@ ta_status ta_prefill_causal(const void *q, const void *k, const void *v, void *o
         return fail(TA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned, lse 4-byte aligned");
     if (D != 128)
         return fail(TA_ERR_UNSUPPORTED, "prefill supports head dim D = 128");
+    if (!(scale > 0.f))
+        return fail(TA_ERR_UNSUPPORTED, "prefill supports scale > 0");
     if ((double)B * H * S * D > 9.0e18 / 4)
         return fail(TA_ERR_INVALID_ARG, "tensor size overflows");
     void *ws = nullptr;

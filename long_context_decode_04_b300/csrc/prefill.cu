@@ -1,13 +1,472 @@
 // prefill.cu -- fused causal prefill on the tensor cores (tcgen05 / TMEM).
+//
+// What is computed (Attention glossary, jisaku.com/glossary/attention,
+// "basic concepts and operating principle"): for query row i of each
+// (sequence b, head h), scores s_ij = scale * <q_i, k_j> over keys j <= i
+// (causal, top-left aligned), softmax weights, and the weighted mean of the
+// values, plus lse_i = ln sum_j exp(s_ij).  The Grayskull SRAM attention
+// explainer (aibr.jp/archives/146339, section 3) fuses the score matmul,
+// the scaling and the softmax into one kernel so that no intermediate goes
+// back to DRAM; here the score tile S and the output accumulator O live in
+// tensor memory and never leave the SM.
+//
+// One CTA owns two 128-row query tiles (rows q0 .. q0 + 255) of one
+// (b, h) and walks the 128-key K/V tiles up to the causal diagonal:
+//   warp 8   TMA producer: loads both Q tiles once, then K and V tiles into
+//            a 2-stage shared-memory ring (128-byte swizzle, two 64-column
+//            boxes per tile).  It also allocates and frees the TMEM.
+//   warp 9   MMA issuer (one thread): per K tile j and query tile t,
+//              PV_t(j-1): O_t += P_t(j-1) V_{j-1}  (P from TMEM, V MN-major)
+//              S_t(j)   = Q_t K_j^T                (both K-major)
+//            Tensor-core operations of one thread run in issue order, so
+//            S_t(j) overwrites the TMEM that holds P_t(j-1) only after the
+//            PV that reads it, and the commit that signals S_t(j) also
+//            guarantees that O_t holds every PV before it.
+//   warps 10-11  V converters: each staged V tile is rewritten in place
+//            from bf16 to fp16 (same swizzled layout) before the PV that
+//            reads it.  P is stored as fp16, whose 11-bit significand keeps
+//            the weights' rounding error near 2^-12 (bf16 would give 2^-9,
+//            enough to move early causal rows by several 1e-3), and a
+//            tcgen05 kind::f16 MMA takes A and B of one type.  bf16 values
+//            with |v| <= 65280 convert exactly (subnormal fp16 results lose
+//            at most 2^-25 absolute); larger ones set TA_DEVERR_RANGE.
+//   warps 0-3 / 4-7   softmax for query tile 0 / 1, one thread per row:
+//            read the S row from TMEM, apply the causal mask on the diagonal
+//            tile, keep the running reference m (rescaled lazily: only when
+//            the row maximum exceeds it by more than 2^8, and then also
+//            O_t in TMEM), write P = 2^(s*scale*log2e - m) as fp16 into the
+//            first 64 columns of the S tile, and accumulate the row sum
+//            twice: from the fp16-rounded P that enters PV (it normalises
+//            the output, so numerator and denominator use the same weights)
+//            and from P before rounding (it gives lse).  The two warpgroups
+//            ping-pong: while one does its softmax the tensor cores run the
+//            other's PV and QK^T.
+//            Epilogue: out = O / l_p in bf16, lse = (m + log2 l) * ln 2.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
+// Every wait is bounded; on expiry TA_DEVERR_TIMEOUT is recorded, all roles
+// stop, outstanding copies and MMAs are drained and the TMEM is freed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace ta {
+namespace {
 
-cudaError_t launch_prefill_causal(const void *, const void *, const void *, void *, float *, int, int, int, int,
-                                  int, float, int32_t *, cudaStream_t)
+constexpr int kBM = 128;      // query rows per tile
+constexpr int kBN = 128;      // keys per K/V tile
+constexpr int kHD = 128;      // head dim
+constexpr int kThreads = 384; // 12 warps
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kConvWarp0 = 10;  // warps 10, 11
+constexpr int kConvThreads = 64;
+constexpr uint32_t kTileBytes = kBM * kHD * 2;  // 32 KiB (one bf16 tile)
+constexpr uint32_t kHalfBytes = kTileBytes / 2; // one 64-column box
+constexpr uint32_t kQOff = 0;                   // 2 Q tiles
+constexpr uint32_t kKOff = 2 * kTileBytes;      // 2 K stages
+constexpr uint32_t kVOff = 4 * kTileBytes;      // 2 V stages
+constexpr uint32_t kBarOff = 6 * kTileBytes;
+constexpr size_t kSmemBytes = kBarOff + 256 + 1024;  // + alignment slack
+constexpr float kRescaleLog2 = 8.0f;
+
+struct PrefillParams {
+    CUtensorMap qmap;  // [B*H, S, D] bf16, box {64, 128, 1}
+    CUtensorMap kmap;  // [B*Hkv, S, D]
+    CUtensorMap vmap;
+    __nv_bfloat16 *out;
+    float *lse;
+    int S, H, G, n_qt, BH;
+    float c;  // scale * log2(e)
+    int32_t *status;
+};
+
+struct Bars {
+    uint64_t q_full;
+    uint64_t k_full[2];
+    uint64_t v_full[2];
+    uint64_t v_conv[2];
+    uint64_t kv_empty[2];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_full[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __grid_constant__ PrefillParams p)
 {
-    return cudaErrorNotSupported;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    Bars *bars = reinterpret_cast<Bars *>(smem + kBarOff);
+    volatile int *abort_flag = &bars->abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Heaviest query tiles first: they walk the most K/V tiles.
+    const int qt = p.n_qt - 1 - (int)(blockIdx.x / p.BH);
+    const int bh = (int)(blockIdx.x % p.BH);
+    const int q0 = qt * 2 * kBM;
+    const int bh_kv = (bh / p.H) * (p.H / p.G) + (bh % p.H) / p.G;
+    const bool active1 = q0 + kBM < p.S;
+    const int diag0 = 2 * qt, diag1 = 2 * qt + 1;
+    const int nk = (active1 ? diag1 : diag0) + 1;  // K/V tiles this CTA walks
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_conv[s], kConvThreads);
+            mbar_init(&bars->kv_empty[s], 1);
+            mbar_init(&bars->s_full[s], 1);
+            mbar_init(&bars->p_full[s], kBM);
+            mbar_init(&bars->o_full[s], 1);
+        }
+        mbar_init(&bars->mma_done, 1);
+        bars->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kProducerWarp) {
+        tc::tmem_alloc(&bars->tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tc::prefetch_tensormap(&p.qmap);
+            tc::prefetch_tensormap(&p.kmap);
+            tc::prefetch_tensormap(&p.vmap);
+            const int n_q = active1 ? 2 : 1;
+            mbar_arrive_expect_tx(&bars->q_full, n_q * kTileBytes);
+            for (int t = 0; t < n_q; ++t) {
+                unsigned char *dst = smem + kQOff + t * kTileBytes;
+                tc::tma_load_3d(dst, &p.qmap, 0, q0 + t * kBM, bh, &bars->q_full);
+                tc::tma_load_3d(dst + kHalfBytes, &p.qmap, 64, q0 + t * kBM, bh, &bars->q_full);
+            }
+            int armed[2] = {0, 0};
+            for (int j = 0; j < nk; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !mbar_wait_bounded(&bars->kv_empty[st], ((j >> 1) & 1) ^ 1, abort_flag))
+                    break;
+                unsigned char *kd = smem + kKOff + st * kTileBytes;
+                unsigned char *vd = smem + kVOff + st * kTileBytes;
+                mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
+                tc::tma_load_3d(kd, &p.kmap, 0, j * kBN, bh_kv, &bars->k_full[st]);
+                tc::tma_load_3d(kd + kHalfBytes, &p.kmap, 64, j * kBN, bh_kv, &bars->k_full[st]);
+                mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
+                tc::tma_load_3d(vd, &p.vmap, 0, j * kBN, bh_kv, &bars->v_full[st]);
+                tc::tma_load_3d(vd + kHalfBytes, &p.vmap, 64, j * kBN, bh_kv, &bars->v_full[st]);
+                ++armed[st];
+            }
+            if (*abort_flag) {
+                // Every copy issued must land before the CTA exits.
+                int drain_abort = 0;
+                mbar_wait_bounded(&bars->q_full, 0, &drain_abort);
+                for (int st = 0; st < 2; ++st)
+                    if (armed[st] > 0) {
+                        mbar_wait_bounded(&bars->k_full[st], (armed[st] - 1) & 1, &drain_abort);
+                        mbar_wait_bounded(&bars->v_full[st], (armed[st] - 1) & 1, &drain_abort);
+                    }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kBM, kBN, false);
+            constexpr uint32_t kIdescPV = tc::idesc_f16_f32(kBM, kHD, true);
+            const uint32_t sbase = smem_u32(smem);
+            bool ok = mbar_wait_bounded(&bars->q_full, 0, abort_flag);
+            tc::fence_after_sync();
+            for (int j = 0; ok && j <= nk; ++j) {
+                const int st = j & 1;
+                if (j < nk) {
+                    ok = mbar_wait_bounded(&bars->k_full[st], (j >> 1) & 1, abort_flag);
+                    if (!ok)
+                        break;
+                    tc::fence_after_sync();
+                }
+                bool v_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    const int diag = t == 0 ? diag0 : diag1;
+                    const bool t_active = t == 0 || active1;
+                    const uint32_t s_tmem = tmem + t * kBN;
+                    const uint32_t o_tmem = tmem + 2 * kBN + t * kHD;
+                    if (j > 0 && t_active && j - 1 <= diag) {
+                        // O_t += P_t(j-1) V_{j-1}
+                        ok = mbar_wait_bounded(&bars->p_full[t], (j - 1) & 1, abort_flag);
+                        if (ok && !v_ready) {
+                            ok = mbar_wait_bounded(&bars->v_conv[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag);
+                            v_ready = true;
+                        }
+                        if (!ok)
+                            break;
+                        tc::fence_after_sync();
+                        const uint32_t vb = sbase + kVOff + ((j - 1) & 1) * kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk) {
+                            // B = V rows [16kk, 16kk+16): MN-major, the two
+                            // 64-column halves are 16 KiB apart (LBO), 8-key
+                            // groups 1 KiB apart (SBO).
+                            const uint64_t bdesc = tc::sw128_desc(vb + kk * 2048, kHalfBytes, 1024);
+                            tc::mma_ts(o_tmem, s_tmem + kk * 8, bdesc, kIdescPV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        if (j > diag)
+                            tc::commit(&bars->o_full[t]);  // last PV of this tile
+                    }
+                    if (j < nk && t_active && j <= diag) {
+                        // S_t = Q_t K_j^T
+                        const uint32_t qb = sbase + kQOff + t * kTileBytes;
+                        const uint32_t kb = sbase + kKOff + st * kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kHD / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                            tc::mma_ss(s_tmem, tc::sw128_desc(qb + off, 16, 1024), tc::sw128_desc(kb + off, 16, 1024),
+                                       kIdescS, kk > 0 ? 1u : 0u);
+                        }
+                        tc::commit(&bars->s_full[t]);
+                    }
+                }
+                if (!ok)
+                    break;
+                if (j > 0)
+                    tc::commit(&bars->kv_empty[(j - 1) & 1]);
+            }
+            // Every MMA this thread issued completes before the TMEM is freed.
+            tc::commit(&bars->mma_done);
+            int drain_abort = 0;
+            mbar_wait_bounded(&bars->mma_done, 0, &drain_abort);
+        }
+        __syncwarp();
+    } else if (warp >= kConvWarp0) {
+        // ------------------------------------------------------------ V bf16 -> fp16
+        const int ct = threadIdx.x - kConvWarp0 * 32;
+        uint32_t vmax = 0;  // largest |v| bit pattern seen, per 16-bit half
+        for (int j = 0; j < nk; ++j) {
+            const int st = j & 1;
+            bool ok = mbar_wait_bounded(&bars->v_full[st], (j >> 1) & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            uint4 *vt = reinterpret_cast<uint4 *>(smem + kVOff + st * kTileBytes);
+#pragma unroll 4
+            for (int i = ct; i < (int)(kTileBytes / 16); i += kConvThreads) {
+                uint4 w = vt[i];
+                vmax = __vmaxu2(vmax, w.x & 0x7fff7fffu);
+                vmax = __vmaxu2(vmax, w.y & 0x7fff7fffu);
+                vmax = __vmaxu2(vmax, w.z & 0x7fff7fffu);
+                vmax = __vmaxu2(vmax, w.w & 0x7fff7fffu);
+                w.x = tc::bf16x2_to_f16x2(w.x);
+                w.y = tc::bf16x2_to_f16x2(w.y);
+                w.z = tc::bf16x2_to_f16x2(w.z);
+                w.w = tc::bf16x2_to_f16x2(w.w);
+                vt[i] = w;
+            }
+            // generic-proxy writes, read next by the tensor cores (async proxy)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&bars->v_conv[st]);
+        }
+        if ((vmax & 0xffffu) > 0x477fu || (vmax >> 16) > 0x477fu)
+            atomicOr(p.status, TA_DEVERR_RANGE);
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int t = warp >> 2;  // query tile
+        const int r = threadIdx.x & (kBM - 1);
+        const int qrow0 = q0 + t * kBM;
+        if (qrow0 < p.S) {
+            const int diag = qrow0 / kBN;
+            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+            const uint32_t s_tmem = tmem + lane_base + t * kBN;
+            const uint32_t o_tmem = tmem + lane_base + 2 * kBN + t * kHD;
+            const float c = p.c;
+            // l_p: sum of the bf16-rounded weights that enter PV (normalises
+            // the output); l: the same weights before rounding (gives lse).
+            float m_used = -INFINITY, l = 0.f, l_p = 0.f;
+            bool ok = true;
+            for (int j = 0; j <= diag; ++j) {
+                ok = mbar_wait_bounded(&bars->s_full[t], j & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok)
+                    break;
+                tc::fence_after_sync();
+                float s[kBN];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t u[32];
+                    tc::tmem_ld32(s_tmem + ch * 32, u);
+                    tc::tmem_wait_ld(u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        s[ch * 32 + i] = __uint_as_float(u[i]);
+                }
+                if (j == diag) {
+#pragma unroll
+                    for (int i = 0; i < kBN; ++i)
+                        if (i > r)
+                            s[i] = -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int i = 1; i < kBN; ++i)
+                    mx = fmaxf(mx, s[i]);
+                const float mcand = mx * c;
+                const bool resc = mcand > m_used + kRescaleLog2;
+                float alpha = 1.f;
+                if (resc) {
+                    alpha = fast_exp2(m_used - mcand);
+                    m_used = mcand;
+                }
+                const float neg_m = -m_used;
+                float ls = 0.f, ls_p = 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float p0 = fast_exp2(fmaf(s[half * 64 + 2 * i], c, neg_m));
+                        const float p1 = fast_exp2(fmaf(s[half * 64 + 2 * i + 1], c, neg_m));
+                        const uint32_t w = tc::pack_f16x2(p0, p1);
+                        pk[i] = w;
+                        ls += p0 + p1;
+                        const float2 pr = tc::unpack_f16x2(w);
+                        ls_p += pr.x + pr.y;
+                    }
+                    tc::tmem_st32(s_tmem + half * 32, pk);
+                }
+                l = l * alpha + ls;
+                l_p = l_p * alpha + ls_p;
+                if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                    // O_t holds every PV up to j-1 (see the MMA issuer);
+                    // bring it to the new reference.
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t u[32];
+                        tc::tmem_ld32(o_tmem + ch * 32, u);
+                        tc::tmem_wait_ld(u);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                        tc::tmem_st32(o_tmem + ch * 32, u);
+                    }
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                mbar_arrive(&bars->p_full[t]);
+            }
+            if (ok) {
+                ok = mbar_wait_bounded(&bars->o_full[t], 0, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+            }
+            if (ok) {
+                tc::fence_after_sync();
+                const int row = qrow0 + r;
+                const float inv = 1.0f / l_p;
+                __nv_bfloat16 *orow = p.out + ((size_t)bh * p.S + row) * kHD;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t u[32];
+                    tc::tmem_ld32(o_tmem + ch * 32, u);
+                    tc::tmem_wait_ld(u);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = tc::pack_bf16x2(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
+                    if (row < p.S) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
+                }
+                if (row < p.S && p.lse)
+                    p.lse[(size_t)bh * p.S + row] = (m_used + fast_log2(l)) * kLn2;
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag)
+        atomicOr(p.status, TA_DEVERR_TIMEOUT);
+    if (warp == kProducerWarp) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// 3-D map over a [rows3, S, D] bf16 tensor, box {64, 128, 1}, 128-byte
+// swizzle; out-of-range rows read as zero.
+bool make_map(CUtensorMap *m, const void *base, int S, int rows3)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kHD, (cuuint64_t)S, (cuuint64_t)rows3};
+    const cuuint64_t strides[2] = {(cuuint64_t)kHD * 2, (cuuint64_t)S * kHD * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kBM, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                                  int Hkv, int S, int D, float scale, int32_t *status, cudaStream_t stream)
+{
+    if (D != kHD)
+        return cudaErrorNotSupported;
+    PrefillParams p;
+    if (!make_map(&p.qmap, q, S, B * H) || !make_map(&p.kmap, k, S, B * Hkv) || !make_map(&p.vmap, v, S, B * Hkv))
+        return cudaErrorInvalidValue;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.S = S;
+    p.H = H;
+    p.G = H / Hkv;
+    p.n_qt = (S + 2 * kBM - 1) / (2 * kBM);
+    p.BH = B * H;
+    p.c = scale * kLog2e;
+    p.status = status;
+    cudaError_t e = cudaFuncSetAttribute(prefill_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    const long long grid = (long long)p.n_qt * p.BH;
+    prefill_causal_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace ta

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(HERE, "libta.so")
 
 TA_OK, TA_ERR_INVALID_ARG, TA_ERR_UNSUPPORTED, TA_ERR_WORKSPACE, TA_ERR_CUDA = range(5)
 TA_F32, TA_BF16 = 0, 1
-TA_DEVERR_SEQLEN, TA_DEVERR_TIMEOUT = 1, 2
+TA_DEVERR_SEQLEN, TA_DEVERR_TIMEOUT, TA_DEVERR_RANGE = 1, 2, 4
 STATUS_NAMES = {0: "TA_OK", 1: "TA_ERR_INVALID_ARG", 2: "TA_ERR_UNSUPPORTED", 3: "TA_ERR_WORKSPACE",
                 4: "TA_ERR_CUDA"}
 

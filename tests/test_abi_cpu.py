@@ -123,6 +123,8 @@ def test_combine_and_prefill_reject_bad_arguments():
                                ctypes.c_float(0.1), None) == ta.TA_ERR_UNSUPPORTED
     assert L.ta_prefill_causal(vp(0x1004), vp(0x2000), vp(0x3000), vp(0x4000), None, 1, 8, 2, 128, 128,
                                ctypes.c_float(0.1), None) == ta.TA_ERR_INVALID_ARG
+    assert L.ta_prefill_causal(vp(0x1000), vp(0x2000), vp(0x3000), vp(0x4000), None, 1, 8, 2, 128, 128,
+                               ctypes.c_float(0.0), None) == ta.TA_ERR_UNSUPPORTED
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")

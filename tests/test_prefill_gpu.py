@@ -1,0 +1,115 @@
+"""Fused causal prefill (tcgen05 / TMEM) on the GPU against the float64 oracle,
+through the C ABI.
+
+Small shapes cover one and several 128-row query tiles, the second query
+tile of a CTA being partly or wholly past S, K/V tiles cut by S, and every
+supported GQA grouping; the full-size workload is checked on a fixed row
+sample in the launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_decode_04_b300 import synth, ta
+from tests.parity import check_lse, check_out
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _inputs(B, H, Hkv, S, seed, scale=None):
+    w = synth.Workload("prefill_test", 5, "prefill", B, H, Hkv, S, 128, "bf16")
+    x = synth.make_inputs(w, seed=seed)
+    if scale is not None:
+        x["scale"] = scale
+    return x
+
+
+def _run(x):
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    out, lse = ta.prefill_causal(q, k, v, scale=x["scale"])
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _check(x, out, lse, rows=None):
+    ro, rl = oracle.prefill_causal(x["q"], x["k"], x["v"], x["scale"], rows=rows)
+    o = out.reshape(-1, 128)
+    l = lse.reshape(-1)
+    if rows is not None:
+        o, l = o[rows], l[rows]
+    return check_out(o, ro, bf16=True), check_lse(l, rl)
+
+
+@pytest.mark.parametrize("S", [1, 2, 7, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 512, 513, 1000])
+def test_small_shapes_all_rows(S):
+    x = _inputs(1, 4, 2, S, seed=2000 + S)
+    out, lse = _run(x)
+    _check(x, out, lse)
+
+
+@pytest.mark.parametrize("B,H,Hkv", [(1, 1, 1), (2, 3, 1), (1, 8, 8), (2, 8, 2), (1, 32, 8), (3, 4, 4)])
+def test_head_groupings_and_batches(B, H, Hkv):
+    x = _inputs(B, H, Hkv, 700, seed=3000 + 7 * B + H)
+    out, lse = _run(x)
+    _check(x, out, lse)
+
+
+@pytest.mark.parametrize("scale", [0.02, 0.25, 1.0])
+def test_scales(scale):
+    """Larger scales make the softmax peaked and exercise the lazy rescale of O."""
+    x = _inputs(1, 4, 1, 1100, seed=4000, scale=scale)
+    out, lse = _run(x)
+    _check(x, out, lse)
+
+
+def test_growing_logits_force_rescales():
+    """Keys whose norm grows along the sequence: every K tile raises the row maximum,
+    so the running reference and O in TMEM are rescaled many times."""
+    x = _inputs(1, 2, 1, 1536, seed=4100)
+    k = x["k"].float()
+    k *= torch.linspace(0.2, 3.0, 1536).view(1, 1, 1536, 1)
+    x["k"] = k.to(torch.bfloat16)
+    out, lse = _run(x)
+    _check(x, out, lse)
+
+
+def test_identical_keys_give_running_mean_of_v():
+    """All keys equal: row i is the mean of V[0..i] exactly (closed form)."""
+    x = _inputs(1, 2, 2, 600, seed=4200)
+    x["k"] = x["k"][:, :, :1, :].expand(-1, -1, 600, -1).contiguous()
+    out, lse = _run(x)
+    v = x["v"].double().numpy()
+    cum = np.cumsum(v, axis=2) / np.arange(1, 601).reshape(1, 1, 600, 1)
+    check_out(out.reshape(-1, 128), cum.reshape(-1, 128), bf16=True, what="running mean")
+    _check(x, out, lse)
+
+
+def test_results_are_deterministic_and_writes_stay_in_bounds():
+    x = _inputs(2, 4, 2, 300, seed=4300)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    n_out = q.numel()
+    out_buf = torch.full((n_out + 4096,), 3.0, dtype=torch.bfloat16, device=DEV)
+    lse_buf = torch.full((2 * 4 * 300 + 512,), 3.0, dtype=torch.float32, device=DEV)
+    out = out_buf[:n_out].view(q.shape)
+    lse = lse_buf[:2 * 4 * 300].view(2, 4, 300)
+    ta.prefill_causal(q, k, v, scale=x["scale"], out=out, lse=lse)
+    o1 = out.clone()
+    l1 = lse.clone()
+    ta.prefill_causal(q, k, v, scale=x["scale"], out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, out) and torch.equal(l1, lse)
+    assert torch.all(out_buf[n_out:] == 3.0) and torch.all(lse_buf[2 * 4 * 300:] == 3.0)
+    assert ta.decode_status() == 0
+
+
+def test_full_causal_prefill_s16384_row_sample():
+    """The 32-head, S = 16384 workload as the benchmark runs it; the oracle checks the
+    first and last 256 rows and every 61st row of every head."""
+    w = synth.WORKLOADS["causal_prefill_32x8_d128_s16384"]
+    x = synth.make_inputs(w)
+    out, lse = _run(x)
+    per_head = np.unique(np.concatenate([np.arange(256), np.arange(w.S - 256, w.S), np.arange(0, w.S, 61)]))
+    rows = (np.arange(w.B * w.Hq)[:, None] * w.S + per_head[None, :]).reshape(-1)
+    _check(x, out, lse, rows=rows)
