@@ -1,16 +1,18 @@
 #!/usr/bin/env python3
-"""Benchmark of the hot path on B300: split-KV decode at S = 131072 (and, when
-the build has it, the fused causal prefill at S = 16384).
+"""Benchmark of the hot path on B300: split-KV decode at S = 131072 and the
+fused causal prefill at S = 16384.
 
 One step = one pass of the path over one batch of synthetic input:
-  1. the split phase: every (KV head, chunk) partial (ta_decode_partials),
-  2. the log-sum-exp merge of the partials (ta_combine),
-  3. the causal prefill of the prefill workload (ta_prefill_causal), if built.
-Each call is bracketed by CUDA events on the stream it is launched on.
+  1. one decode token (ta_decode_ex): the KV-chunk plan, the split-KV
+     partials of every (KV head, chunk) and their log-sum-exp merge -- one
+     launch, since the decode kernel merges up to 64 chunks itself;
+  2. the causal prefill of the prefill workload (ta_prefill_causal).
+Each phase is a CUDA graph replay bracketed by CUDA events on the stream it
+is launched on.
 
 The JSON line's ``value`` is decode KV-cache throughput in GB/s (the K and V
-bytes a decode step must read, over the time of steps 1-2), summed over
-ranks; ``us_per_token`` is the decode time of one step; ``prefill_tflops`` the
+bytes a decode step must read, over the time of step 1), summed over ranks;
+``us_per_token`` is the decode time of one step; ``prefill_tflops`` the
 causal FLOPs over the prefill time.  Inputs are larger than L2 (512 MiB of
 K/V per decode step), so no flush is needed between steps.
 
@@ -207,17 +209,12 @@ def main():
     x = synth.make_inputs(w)
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     plan = ta.plan_decode(w.B, w.Hq, w.Hkv, w.S, w.D)
-    R, N = w.B * w.Hq, plan.n_split
     ws = ta.decode_workspace(w.B, w.Hq, w.Hkv, w.S, w.D, device=dev)
-    pm = torch.empty((R, N), dtype=torch.float32, device=dev)
-    pl = torch.empty((R, N), dtype=torch.float32, device=dev)
-    po = torch.empty((R, N, w.D), dtype=torch.float32, device=dev)
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
-    cws_bytes = ta.combine_workspace_bytes(R, N, w.D)
-    cws = torch.zeros(max(256, cws_bytes), dtype=torch.uint8, device=dev)
     kv_bytes = accounting.decode_kv_bytes(w.B, w.Hkv, w.D, w.S, 2)
-    combine_levels = plan.levels
+    # up to 64 chunks the decode kernel merges them itself: one launch
+    decode_launches = 1 if plan.n_split <= 64 else 1 + plan.levels
 
     # ---------------- prefill workload
     do_prefill = not args.no_prefill
@@ -236,30 +233,26 @@ def main():
             if e.status != ta.TA_ERR_UNSUPPORTED:
                 raise
             do_prefill = False
-    launches_per_step = 1 + combine_levels + (1 if do_prefill else 0)
+    launches_per_step = decode_launches + (1 if do_prefill else 0)
 
-    def run_split():
-        ta.decode_partials(q, k, v, scale=w.scale, workspace=ws, m=pm, l=pl, o=po)
-
-    def run_combine():
-        ta.combine(pm, pl, po, workspace=cws, out=out, lse=lse)
+    def run_decode():
+        ta.decode(q, k, v, scale=w.scale, workspace=ws, out=out, lse=lse)
 
     def run_prefill():
         pw_, pq_, pk_, pv_, pout_, plse_ = pf
         ta.prefill_causal(pq_, pk_, pv_, scale=pw_.scale, out=pout_, lse=plse_)
 
     for _ in range(args.warmup):
-        run_split()
-        run_combine()
+        run_decode()
         if do_prefill:
             run_prefill()
     torch.cuda.synchronize()
 
     # Each phase is captured once into a CUDA graph, so that a timed step is
-    # a few graph launches and the host never holds the GPU back: the events
-    # between replays then measure device time only.
+    # a couple of graph launches and the host never holds the GPU back: the
+    # events between replays then measure device time only.
     graphs = []
-    for fn in (run_split, run_combine) + ((run_prefill,) if do_prefill else ()):
+    for fn in (run_decode,) + ((run_prefill,) if do_prefill else ()):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             fn()
@@ -271,14 +264,12 @@ def main():
         ev[0].record(stream)
         graphs[0].replay()
         ev[1].record(stream)
-        graphs[1].replay()
-        ev[2].record(stream)
         if do_prefill:
-            graphs[2].replay()
-        ev[3].record(stream)
+            graphs[1].replay()
+        ev[2].record(stream)
 
     def new_events():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        return [torch.cuda.Event(enable_timing=True) for _ in range(3)]
 
     warm = new_events()
     for _ in range(args.warmup):
@@ -308,10 +299,9 @@ def main():
     clocks = sampler.stop(wall0, wall1)
 
     total_ms = t_start.elapsed_time(t_end)
-    split_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    comb_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    pre_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    dec_total = sum(split_ms) + sum(comb_ms)
+    dec_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    pre_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    dec_total = sum(dec_ms)
     pre_total = sum(pre_ms)
 
     def max_over_ranks(val):
@@ -324,7 +314,7 @@ def main():
     total_ms = max_over_ranks(total_ms)
     dec_total = max_over_ranks(dec_total)
     pre_total = max_over_ranks(pre_total)
-    split_avg = max_over_ranks(sum(split_ms) / len(split_ms))
+    dec_avg = dec_total / len(dec_ms)
 
     # ---------------- end to end through the public single call, host buffers
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
@@ -374,8 +364,7 @@ def main():
 
     dec_s = dec_total / 1e3
     value = world * kv_bytes * args.steps / dec_s / 1e9
-    split_s = split_avg / 1e3
-    achieved = kv_bytes / split_s / 1e9
+    achieved = kv_bytes / (dec_avg / 1e3) / 1e9
     line = {
         "metric": "decode KV-cache GB/s (% of B300 HBM peak) and us/token at S=131072; prefill TFLOP/s",
         "value": round(value, 2),
@@ -394,19 +383,20 @@ def main():
             "workload": f"{DECODE_WORKLOAD}: B=1, Hq=32, Hkv=8, D=128, S=131072, bf16 q/K/V N(0,1), "
                         f"scale=1/sqrt(128)",
             "split_kv": {"n_split": plan.n_split, "chunk": plan.chunk, "grid": plan.grid,
-                         "merge_levels": plan.levels},
+                         "merge": "fused in the decode kernel" if plan.n_split <= 64
+                         else f"{plan.levels} merge launches"},
             "prefill_workload": (f"{PREFILL_WORKLOAD}: B=1, H=32, Hkv=8, D=128, S=16384, causal, bf16"
                                  if do_prefill else "not in this build"),
-            "l2": "inputs larger than L2 (512 MiB of K/V per decode step); no flush",
+            "l2": "inputs larger than L2 (512 MiB of K/V per decode step, 335 MB per prefill); no flush",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
-        "us_per_token": round(1e3 * dec_total / args.steps, 3),
+        "us_per_token": round(1e3 * dec_avg, 3),
         "decode_hbm_frac": round(value / world / peaks["hbm_gbs"], 4),
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": kv_bytes,
-                     "peak_source": peaks["source"], "avg_launch_us": round(1e3 * split_avg, 3)},
-        "combine_us": round(1e3 * sum(comb_ms) / len(comb_ms), 3),
+                     "peak_source": peaks["source"] + " (copy bandwidth)",
+                     "avg_launch_us": round(1e3 * dec_avg, 3), "launches_per_token": decode_launches},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "e2e": {"value": round(world * kv_bytes * e2e_steps / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",

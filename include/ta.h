@@ -94,10 +94,18 @@ typedef struct {
  *   chunk / n_split: 0 = scheduler default; chunk > 0 forces keys per chunk
  *     (takes precedence), else n_split > 0 forces the number of chunks.
  *   workspace: device scratch of at least ta_decode_plan.workspace_bytes,
- *     256-byte aligned, whose first 256 bytes (the status word) the caller
- *     zeroes once when it sets the workspace up.  NULL = use the library's
- *     own per-device workspace (grown on demand with cudaMalloc, which
- *     synchronises; calls using it on different streams must not overlap).
+ *     256-byte aligned, that the caller zeroes once when it sets it up and
+ *     uses for decodes only.  A split decode keeps its status word and one
+ *     chunk counter per (sequence, KV head) in the first 16 KiB; every
+ *     completed call leaves them zero again (after TA_DEVERR_TIMEOUT, zero
+ *     that region again before reuse).
+ *     NULL = use the library's own per-device workspace (grown on demand
+ *     with cudaMalloc, which synchronises; calls using it on different
+ *     streams must not overlap).
+ *   With up to 64 chunks (and B * Hkv <= 4032) the decode kernel merges a
+ *   sequence's partials itself (the last CTA to finish a chunk of a
+ *   (sequence, KV head) merges them); otherwise a separate tree of merge
+ *   launches follows it.
  * Supported: D in {64, 128}; in_dtype = out_dtype family F32 or BF16
  * (out may be F32 for BF16 inputs); G in {1, 2, 4} for D = 128 and
  * G in {1, 2, 4, 8} for D = 64.  Pointers q, k, v, out 16-byte aligned.
@@ -146,8 +154,8 @@ ta_status ta_decode(const void *q, const void *k, const void *v, void *out, floa
  *   Set-up: the first call on each device looks up the array's device
  *   address with that device current; make that first call before any
  *   stream capture.
- *   Every call clears the scratch's status word on `stream` before the
- *   kernels run.  All calls on one GPU share the one array: calls that may
+ *   Every call clears the scratch's status word and chunk counters on
+ *   `stream` before the kernels run.  All calls on one GPU share the one array: calls that may
  *   overlap on the GPU (different streams or host threads with no ordering
  *   between them) race on it and give wrong results.
  * Arguments, layouts, alignment and errors as for ta_decode.
@@ -188,7 +196,8 @@ size_t ta_decode_workspace_bytes(int B, int Hq, int Hkv, int S, int D, int chunk
 
 /*
  * Read and clear the device status word (TA_DEVERR_* bits) of a decode
- * workspace (NULL = the library's own workspace of the current device).
+ * workspace (NULL = the library's own workspace of the current device; if
+ * TA_DEVERR_TIMEOUT is set its whole 16 KiB control region is cleared too).
  * Synchronises `stream` first.
  */
 ta_status ta_decode_status(void *workspace, void *stream, int32_t *flags);

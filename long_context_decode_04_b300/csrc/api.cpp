@@ -1,6 +1,7 @@
 // api.cpp -- the C ABI: argument validation, the library workspace, and
 // dispatch to the scheduler and the kernels.  Nothing here computes
 // attention; every arithmetic step runs in the CUDA kernels.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -223,9 +224,11 @@ ta_status ta_decode_ex(const ta_decode_params *p)
     a.status = reinterpret_cast<int32_t *>(base);
     const size_t R = (size_t)p->B * p->Hq, N = (size_t)plan.n_split;
     a.part_m = a.part_l = a.part_o = nullptr;
+    a.counters = nullptr;
     char *scratch = nullptr;
     if (N > 1) {
-        size_t off = ta::kStatusBytes;
+        a.counters = reinterpret_cast<int32_t *>(base + ta::kStatusBytes);
+        size_t off = ta::kCtrlBytes;
         a.part_m = reinterpret_cast<float *>(base + off);
         off += align256(4 * R * N);
         a.part_l = reinterpret_cast<float *>(base + off);
@@ -237,7 +240,7 @@ ta_status ta_decode_ex(const ta_decode_params *p)
     cudaError_t e = ta::launch_decode(a);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode kernel launch");
-    if (N > 1) {
+    if (N > 1 && !ta::decode_merges_itself(plan.n_split, p->B * p->Hkv)) {
         e = ta::launch_combine(a.part_m, a.part_l, a.part_o, (int)R, (int)N, p->D, p->out, p->out_dtype, p->lse,
                                scratch, a.stream);
         if (e != cudaSuccess)
@@ -294,6 +297,7 @@ ta_status ta_decode_partials(const ta_decode_params *p, float *m, float *l, floa
     a.force_partials = true;
     a.stream = static_cast<cudaStream_t>(p->stream);
     a.status = static_cast<int32_t *>(ws);
+    a.counters = nullptr;
     a.part_m = m;
     a.part_l = l;
     a.part_o = o;
@@ -331,10 +335,15 @@ ta_status ta_decode_status(void *workspace, void *stream, int32_t *flags)
     if (!flags)
         return fail(TA_ERR_INVALID_ARG, "flags pointer is NULL");
     void *ws = workspace;
+    size_t clear = ta::kStatusBytes;
     if (!ws) {
         ta_status s = library_workspace(256, &ws);
         if (s != TA_OK)
             return s;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        std::lock_guard<std::mutex> lock(g_mu);
+        clear = std::min(state_for(dev).ws_bytes, (size_t)ta::kCtrlBytes);
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(st);
@@ -344,7 +353,9 @@ ta_status ta_decode_status(void *workspace, void *stream, int32_t *flags)
     e = cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMemcpy(status)");
-    e = cudaMemset(ws, 0, ta::kStatusBytes);
+    // A launch that gave up can leave chunk counters behind: clear the
+    // whole control region of the library's workspace then.
+    e = cudaMemset(ws, 0, (word & TA_DEVERR_TIMEOUT) ? clear : ta::kStatusBytes);
     if (e == cudaSuccess)
         e = cudaDeviceSynchronize();
     if (e != cudaSuccess)
@@ -384,11 +395,11 @@ ta_status ta_combine(const float *m, const float *l, const float *o, int R, int 
             if (workspace_bytes < need)
                 return fail(TA_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes");
         } else {
-            // the library workspace keeps its first 256 bytes for the status word
-            ta_status s = library_workspace(need + ta::kStatusBytes, &ws);
+            // the library workspace keeps its control region for decodes
+            ta_status s = library_workspace(need + ta::kCtrlBytes, &ws);
             if (s != TA_OK)
                 return s;
-            ws = static_cast<char *>(ws) + ta::kStatusBytes;
+            ws = static_cast<char *>(ws) + ta::kCtrlBytes;
         }
     }
     cudaError_t e = ta::launch_combine(m, l, o, R, N, D, out, out_dtype, lse, ws, static_cast<cudaStream_t>(stream));

@@ -19,10 +19,11 @@
 // exits.
 //
 // What the scratch holds: the decode workspace (status word and work-queue
-// counter in its first 256 bytes, then the per-chunk partials (m, l, o) and
-// the merge's intermediates).  The first 256 bytes are cleared on the call's
-// stream at the start of every call; the rest is fully written before it is
-// read.  All calls on a GPU share the one array, so calls that overlap on the
+// counter in its first 256 bytes, the per-(sequence, KV head) chunk
+// counters, then the per-chunk partials (m, l, o) and the merge's
+// intermediates).  The status word and the counters are cleared on the
+// call's stream at the start of every call; the rest is fully written before
+// it is read.  All calls on a GPU share the one array, so calls that overlap on the
 // GPU (different streams, or different host threads, with no ordering
 // between them) race on it and give wrong results.
 #include <cstring>
@@ -112,8 +113,10 @@ ta_status ta_decode_noalloc(const void *q, const void *k, const void *v, void *o
     s = scratch_for_current_device(&scratch);
     if (s != TA_OK)
         return s;
-    // The status word and the work-queue counter must start at zero.
-    cudaError_t e = cudaMemsetAsync(scratch, 0, ta::kStatusBytes, static_cast<cudaStream_t>(stream));
+    // The status word, the work-queue counter and the per-unit chunk
+    // counters must start at zero.
+    const size_t zero_bytes = plan.n_split > 1 ? ta::kCtrlBytes : ta::kStatusBytes;
+    cudaError_t e = cudaMemsetAsync(scratch, 0, zero_bytes, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return fail(TA_ERR_CUDA, std::string("cudaMemsetAsync(status word): ") + cudaGetErrorString(e));
     p.workspace = scratch;

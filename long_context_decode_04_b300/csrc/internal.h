@@ -12,6 +12,16 @@ namespace ta {
 
 constexpr int kFanin = 64;            // partials merged by one warp per level
 constexpr int kStatusBytes = 256;     // status word region at the workspace start
+constexpr int kDecodeTileKeys = 96;   // keys the decode kernel stages per tile
+// A split decode's workspace starts with a fixed control region that no
+// other use of the workspace writes: the status word and work-queue counter
+// (first 256 bytes), then one chunk counter per (sequence, KV head).
+// Every completed launch leaves the region zero.
+constexpr int kCtrlBytes = 16384;
+constexpr int kMaxFusedUnits = (kCtrlBytes - kStatusBytes) / 4;
+// Up to this many chunks per (sequence, KV head), and kMaxFusedUnits units,
+// the decode kernel merges the partials itself.
+constexpr int kFusedMergeMaxSplits = 64;
 
 struct DecodeLaunch {
     const void *q, *k, *v;
@@ -23,6 +33,7 @@ struct DecodeLaunch {
     ta_dtype in_dtype, out_dtype;
     ta_decode_plan plan;
     int32_t *status;       // device status word
+    int32_t *counters;     // [B * Hkv] finished chunks per unit, zero between launches
     float *part_m, *part_l, *part_o;   // [R, n_split], [R, n_split], [R, n_split, D]
     bool force_partials;               // write partials even when n_split == 1
     cudaStream_t stream;
@@ -34,6 +45,13 @@ void record_error(const std::string &msg);
 // The argument checks of ta_decode_ex, on their own (api.cpp): TA_OK or the
 // status (with its message recorded) that ta_decode_ex would return.
 ta_status check_decode_params(const ta_decode_params *p);
+
+// Whether the decode kernel merges a sequence's chunks itself (else a
+// separate merge launch follows it).
+inline bool decode_merges_itself(int n_split, int units)
+{
+    return n_split > 1 && n_split <= kFusedMergeMaxSplits && units <= kMaxFusedUnits;
+}
 
 // Scheduler (sched.cpp).
 ta_status plan_decode(int B, int Hq, int Hkv, int S, int D, int chunk, int n_split, int varlen,

@@ -7,7 +7,8 @@
 // associative tree.  The pages give no rule for the chunk size; the rule
 // here keeps every SM busy: the persistent decode kernel runs
 // sm_count * ctas_per_sm CTAs, and the chunk count is chosen so that the
-// (sequence, KV head, chunk) work items fill those CTAs evenly.
+// (sequence, KV head, chunk) work items fill those CTAs evenly.  Chunks are
+// whole numbers of the kernel's 96-key tiles.
 #include <algorithm>
 #include <climits>
 
@@ -73,8 +74,9 @@ ta_status plan_decode(int B, int Hq, int Hkv, int S, int D, int chunk, int n_spl
     const int64_t units = (int64_t)B * Hkv;           // independent (sequence, KV head) pairs
     const int64_t slots = (int64_t)sm_count * decode_ctas_per_sm();
     auto chunk_for = [&](int64_t ns) {
-        int64_t c = ceil_div(ceil_div(S, ns), 64) * 64;  // multiple of 64 keys
-        c = std::max<int64_t>(c, 256);                   // at least 256 keys
+        // a whole number of the kernel's tiles, at least two
+        int64_t c = ceil_div(ceil_div(S, ns), kDecodeTileKeys) * kDecodeTileKeys;
+        c = std::max<int64_t>(c, 2 * kDecodeTileKeys);
         return std::min<int64_t>(c, S);
     };
     int64_t c;
@@ -91,7 +93,7 @@ ta_status plan_decode(int B, int Hq, int Hkv, int S, int D, int chunk, int n_spl
         // minimises (waves of items over the CTA slots) x (keys per item +
         // a fixed per-item cost of 64 keys), preferring fewer chunks on ties.
         int64_t best_c = chunk_for(1), best_cost = INT64_MAX;
-        const int64_t max_ns = std::min<int64_t>(ceil_div(S, 256), 8 * ceil_div(slots, units) + 1);
+        const int64_t max_ns = std::min<int64_t>(ceil_div(S, 2 * kDecodeTileKeys), 8 * ceil_div(slots, units) + 1);
         for (int64_t ns = 1; ns <= std::max<int64_t>(1, max_ns); ++ns) {
             const int64_t cc = chunk_for(ns);
             const int64_t real_ns = ceil_div(S, cc);
@@ -123,6 +125,7 @@ ta_status plan_decode(int B, int Hq, int Hkv, int S, int D, int chunk, int n_spl
     auto align = [](int64_t x) { return (x + 255) / 256 * 256; };
     int64_t ws = kStatusBytes;  // status word + work-queue counter
     if (ns > 1) {
+        ws = kCtrlBytes;  // + the chunk counters
         ws += align(4 * R * ns) * 2 + align(4 * R * ns * D);
         ws += (int64_t)combine_scratch_bytes((int)R, (int)ns, D);
     }

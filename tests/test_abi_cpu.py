@@ -59,7 +59,7 @@ def test_plan_of_the_128k_workload_fills_the_sms_evenly():
     plan = ta.plan_decode(1, 32, 8, 131072, 128, sm_count=SMS)
     items = 8 * plan.n_split
     assert items % SMS == 0 and plan.grid == SMS
-    assert plan.chunk % 64 == 0 and plan.chunk >= 256
+    assert plan.chunk % 96 == 0 and plan.chunk >= 192  # whole 96-key tiles
 
 
 def test_plan_overrides():
@@ -79,7 +79,8 @@ def test_workspace_size_formula():
     R, N = B * Hq, p.n_split
     n1 = -(-N // 64)
     comb = 2 * (2 * a256(4 * R * n1) + a256(4 * R * n1 * D))
-    assert p.workspace_bytes == 256 + 2 * a256(4 * R * N) + a256(4 * R * N * D) + comb
+    control = 16384  # status word, work-queue counter and per-unit chunk counters
+    assert p.workspace_bytes == control + 2 * a256(4 * R * N) + a256(4 * R * N * D) + comb
     p1 = ta.plan_decode(1, 1, 1, 100, 64, sm_count=SMS)
     assert p1.n_split == 1 and p1.workspace_bytes == 256
 

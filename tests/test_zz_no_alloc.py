@@ -61,11 +61,11 @@ def test_noalloc_matches_ta_decode_on_two_calls_in_a_row(name, kw):
 
 
 def test_noalloc_rejects_a_shape_beyond_its_scratch():
-    # 256 sequences x 32 heads x 8192 keys: the default plan splits each
-    # sequence in two and needs just over 8 MiB of partials.  K/V are real
-    # buffers of the full size (16 GiB, shared by K and V, never written),
-    # so even a call that slipped through would stay in bounds.
-    B, Hq, Hkv, S, D = 256, 32, 32, 8192, 128
+    # 192 sequences x 8 KV heads x 65536 keys: the default plan splits each
+    # (sequence, KV head) in five and needs about 15 MiB of partials.  K/V
+    # are real buffers of the full size (24 GiB, shared by K and V, never
+    # written), so even a call that slipped through would stay in bounds.
+    B, Hq, Hkv, S, D = 192, 32, 8, 65536, 128
     need = ta.plan_decode(B, Hq, Hkv, S, D).workspace_bytes
     assert need > SCRATCH_BYTES
     q = torch.zeros(B, Hq, D, dtype=torch.bfloat16, device=DEV)
