@@ -28,16 +28,18 @@
 //     two steps of 4 keys.
 //       scores: 8 lanes share a key, each holding 16 bytes x NCH of the
 //         row; the G query heads of the KV head (grouped-query attention)
-//         use each staged row, with q in registers pre-multiplied by
-//         scale * log2(e), products taken two lanes of fp32 at a time
-//         (packed f32x2 FMA) and the 8-lane sums closed by 3 xor shuffles.
+//         use each staged row.  For bf16 K the products use the
+//         mixed-precision FMA (bf16 x bf16 + fp32), so neither q nor K is
+//         widened; the 8 lanes' partial sums of the G heads are reduced by
+//         a reduce-scatter over 3 xor shuffles (G/2 + G/4 + ... exchanges),
+//         after which each lane holds one head's full score.
 //       online softmax: one running reference m per head for the whole
 //         warp, raised lazily (only when a score exceeds it by more than
 //         2^8, with a warp vote), so the weights stay below 2^8 and the
-//         result is exact up to rounding.
-//       PV: the weights go through shared memory, and every lane owns
-//         D/32 output dimensions of every head, accumulated with packed
-//         f32x2 FMAs over the warp's keys.
+//         result is exact up to rounding.  Each lane takes one exp.
+//       PV: the weights go through shared memory (one vector load per key),
+//         and every lane owns D/32 output dimensions of every head,
+//         accumulated in fp32 over the warp's keys.
 //     At the end of an item the 12 warps are merged through shared memory
 //     by the log-sum-exp rule and the item's partial (or, with one chunk,
 //     the final output and lse) is written.
@@ -103,24 +105,72 @@ struct Elem<__nv_bfloat16> {
 __device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
-// 16 bytes of K or V as floats.
-__device__ __forceinline__ void unpack16(const uint4 &r, float (&f)[4], float *)
+// ae += a.lo * b.lo, ao += a.hi * b.hi for packed bf16 pairs a, b: the
+// mixed-precision FMA takes bf16 operands and an fp32 accumulator, so K
+// needs no conversion (exactly fmaf of the widened values).
+__device__ __forceinline__ void fma_bf16x2(float &ae, float &ao, uint32_t a, uint32_t b)
 {
-    f[0] = __uint_as_float(r.x);
-    f[1] = __uint_as_float(r.y);
-    f[2] = __uint_as_float(r.z);
-    f[3] = __uint_as_float(r.w);
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "mov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+        : "+f"(ae), "+f"(ao)
+        : "r"(a), "r"(b));
 }
-__device__ __forceinline__ void unpack16(const uint4 &r, float (&f)[8], __nv_bfloat16 *)
+
+// The G weights of one key from shared memory (one vector load).
+template <int G>
+__device__ __forceinline__ void load_weights(const float *src, float (&pk)[G])
 {
-    f[0] = bf16_lo(r.x);
-    f[1] = bf16_hi(r.x);
-    f[2] = bf16_lo(r.y);
-    f[3] = bf16_hi(r.y);
-    f[4] = bf16_lo(r.z);
-    f[5] = bf16_hi(r.z);
-    f[6] = bf16_lo(r.w);
-    f[7] = bf16_hi(r.w);
+    if constexpr (G == 1) {
+        pk[0] = *src;
+    } else if constexpr (G == 2) {
+        const float2 x = *reinterpret_cast<const float2 *>(src);
+        pk[0] = x.x;
+        pk[1] = x.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < G; i += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(src + i);
+            pk[i] = x.x;
+            pk[i + 1] = x.y;
+            pk[i + 2] = x.z;
+            pk[i + 3] = x.w;
+        }
+    }
+}
+
+// The DPL consecutive values of a V row that this lane owns, as floats.
+template <int DPL>
+__device__ __forceinline__ void load_v_slice(const unsigned char *src, float (&vf)[DPL], __nv_bfloat16 *)
+{
+    if constexpr (DPL == 4) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(src);
+        vf[0] = bf16_lo(w.x);
+        vf[1] = bf16_hi(w.x);
+        vf[2] = bf16_lo(w.y);
+        vf[3] = bf16_hi(w.y);
+    } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
+        vf[0] = bf16_lo(w);
+        vf[1] = bf16_hi(w);
+    }
+}
+template <int DPL>
+__device__ __forceinline__ void load_v_slice(const unsigned char *src, float (&vf)[DPL], float *)
+{
+    if constexpr (DPL == 4) {
+        const float4 w = *reinterpret_cast<const float4 *>(src);
+        vf[0] = w.x;
+        vf[1] = w.y;
+        vf[2] = w.z;
+        vf[3] = w.w;
+    } else {
+        const float2 w = *reinterpret_cast<const float2 *>(src);
+        vf[0] = w.x;
+        vf[1] = w.y;
+    }
 }
 
 template <int D, int G, typename KV>
@@ -128,7 +178,7 @@ struct Cfg {
     static constexpr int RB = D * (int)sizeof(KV);  // bytes per K or V row
     static constexpr int NCH = RB / 128;            // 16-byte chunks per lane per row (8 lanes per key)
     static constexpr int EPC = Elem<KV>::kPerChunk; // elements per chunk
-    static constexpr int QPL = NCH * EPC;           // q elements held by a lane per head
+    static constexpr int QPL_W = NCH * 4;           // 32-bit q words held by a lane per head
     static constexpr int DPL = D / 32;              // output dims owned by a lane (PV)
     static constexpr int VB = DPL * (int)sizeof(KV);// V bytes read by a lane per key
     static constexpr int KV_OFF = kTile * RB;       // V tile offset inside a stage
@@ -267,10 +317,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
     const int g = lane >> 3;  // key slot within a 4-key step
     const int t = lane & 7;   // lane within the 8-lane key group
     const int tid = threadIdx.x;
+    // After the reduce-scatter of the scores, lane t of a key group holds
+    // the score of head hm = t / (8 / G); 8 / G lanes share each head.
+    constexpr int kLanesPerHead = 8 / G;
+    const int hm = t / kLanesPerHead;
 
-    float qr[G][C::QPL];       // q * scale * log2(e), this lane's slice
-    float2 o[G][C::DPL / 2];   // this lane's output dims, unnormalised
-    float m_run[G], l[G];      // warp-uniform reference; this lane group's sum
+    uint32_t qw[G][C::QPL_W];  // this lane's q slice: bf16 pairs, or fp32 bits
+    float o[G][C::DPL];        // this lane's output dims of every head, unnormalised
+    float m_mine = -INFINITY;  // running reference of head hm (log2 units), warp-uniform per head
+    float l_mine = 0.f;        // sum of this key group's weights for head hm
     int stage = 0;
     uint32_t phase = 0;
     uint32_t merge_phase = 0, ticket_phase = 0;
@@ -296,18 +351,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
 #pragma unroll
                 for (int i = 0; i < C::NCH; ++i) {
                     const uint4 raw = *reinterpret_cast<const uint4 *>(qrow + (t + 8 * i) * C::EPC);
-                    float f[C::EPC];
-                    unpack16(raw, f, (KV *)nullptr);
-#pragma unroll
-                    for (int e = 0; e < C::EPC; ++e)
-                        qr[h][i * C::EPC + e] = f[e] * p.qscale;
+                    qw[h][4 * i + 0] = raw.x;
+                    qw[h][4 * i + 1] = raw.y;
+                    qw[h][4 * i + 2] = raw.z;
+                    qw[h][4 * i + 3] = raw.w;
                 }
-                m_run[h] = -INFINITY;
-                l[h] = 0.f;
 #pragma unroll
-                for (int e = 0; e < C::DPL / 2; ++e)
-                    o[h][e] = make_float2(0.f, 0.f);
+                for (int e = 0; e < C::DPL; ++e)
+                    o[h][e] = 0.f;
             }
+            m_mine = -INFINITY;
+            l_mine = 0.f;
         }
 
         const unsigned char *Ks = smem + stage * C::STAGE;
@@ -319,108 +373,93 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
                 break;  // warp-uniform
             const int key = kbeg + st4 + g;
             const bool valid = key < d.n;
-            // ---- scores of this lane group's key for the G heads
-            float2 acc[G];
+            // ---- <q_h, k> partial sums over this lane's slice of the row
+            float ae[G], ao[G];
 #pragma unroll
             for (int h = 0; h < G; ++h)
-                acc[h] = make_float2(0.f, 0.f);
+                ae[h] = ao[h] = 0.f;
             if (valid) {
 #pragma unroll
                 for (int i = 0; i < C::NCH; ++i) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(Ks + key * C::RB + (t + 8 * i) * 16);
-                    float kf[C::EPC];
-                    unpack16(raw, kf, (KV *)nullptr);
+                    const uint4 kr = *reinterpret_cast<const uint4 *>(Ks + key * C::RB + (t + 8 * i) * 16);
+                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
 #pragma unroll
                     for (int h = 0; h < G; ++h)
 #pragma unroll
-                        for (int e = 0; e < C::EPC; e += 2)
-                            acc[h] = __ffma2_rn(make_float2(qr[h][i * C::EPC + e], qr[h][i * C::EPC + e + 1]),
-                                                make_float2(kf[e], kf[e + 1]), acc[h]);
+                        for (int w = 0; w < 4; ++w) {
+                            if constexpr (sizeof(KV) == 2) {
+                                fma_bf16x2(ae[h], ao[h], qw[h][4 * i + w], kw[w]);
+                            } else if (w & 1) {
+                                ao[h] = fmaf(__uint_as_float(qw[h][4 * i + w]), __uint_as_float(kw[w]), ao[h]);
+                            } else {
+                                ae[h] = fmaf(__uint_as_float(qw[h][4 * i + w]), __uint_as_float(kw[w]), ae[h]);
+                            }
+                        }
                 }
             }
-            float s[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float x = acc[h].x + acc[h].y;
-                x += __shfl_xor_sync(kFull, x, 4);
-                x += __shfl_xor_sync(kFull, x, 2);
-                x += __shfl_xor_sync(kFull, x, 1);
-                s[h] = valid ? x : -INFINITY;
-            }
-            // ---- lazy, warp-uniform rescale of the running reference
-            bool need = false;
+            // ---- 8-lane reduce-scatter: head hm's full score lands in this lane
+            float v[G];
 #pragma unroll
             for (int h = 0; h < G; ++h)
-                need |= s[h] > m_run[h] + kRescaleLog2;
-            if (__any_sync(kFull, need)) {
+                v[h] = ae[h] + ao[h];
+            int n = G;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float mx = s[h];
-                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-                    if (mx > m_run[h] + kRescaleLog2) {
-                        const float a = m_run[h] == -INFINITY ? 0.f : fast_exp2(m_run[h] - mx);
-                        l[h] *= a;
+            for (int r = 0; r < 3; ++r) {
+                const int mask = 4 >> r;
+                if (n > 1) {
+                    const bool upper = (t & mask) != 0;
 #pragma unroll
-                        for (int e = 0; e < C::DPL / 2; ++e)
-                            o[h][e] = make_float2(o[h][e].x * a, o[h][e].y * a);
-                        m_run[h] = mx;
+                    for (int i = 0; i < n / 2; ++i) {
+                        const float send = upper ? v[i] : v[i + n / 2];
+                        const float keep = upper ? v[i + n / 2] : v[i];
+                        v[i] = keep + __shfl_xor_sync(kFull, send, mask);
                     }
+                    n /= 2;
+                } else {
+                    v[0] += __shfl_xor_sync(kFull, v[0], mask);
                 }
             }
-            float pw[G];
+            const float sc = valid ? v[0] * p.qscale : -INFINITY;  // log2 units
+            // ---- lazy rescale of the running reference (warp vote)
+            if (__any_sync(kFull, sc > m_mine + kRescaleLog2)) {
+                float mx = sc;
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+                float alpha = 1.f;
+                if (mx > m_mine + kRescaleLog2) {
+                    alpha = m_mine == -INFINITY ? 0.f : fast_exp2(m_mine - mx);
+                    m_mine = mx;
+                    l_mine *= alpha;
+                }
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                pw[h] = valid ? fast_exp2(s[h] - m_run[h]) : 0.f;
-                l[h] += pw[h];
+                for (int h = 0; h < G; ++h) {
+                    const float a = __shfl_sync(kFull, alpha, h * kLanesPerHead);
+#pragma unroll
+                    for (int e = 0; e < C::DPL; ++e)
+                        o[h][e] *= a;
+                }
             }
+            const float pw = valid ? fast_exp2(sc - m_mine) : 0.f;
+            l_mine += pw;
             // ---- PV: the 4 keys' weights through shared memory, lanes own dims
             float *slot = my_pbuf + pslot * (4 * G);
-            if (t == 0) {
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-                    slot[g * G + h] = pw[h];
-            }
+            if (t % kLanesPerHead == 0)
+                slot[g * G + hm] = pw;
             __syncwarp();
 #pragma unroll
             for (int gg = 0; gg < 4; ++gg) {
                 const int key2 = kbeg + st4 + gg;
                 if (key2 >= d.n)
                     break;  // warp-uniform
+                float pk[G];
+                load_weights<G>(slot + gg * G, pk);
                 float vf[C::DPL];
-                const unsigned char *vrow = Vs + key2 * C::RB + lane * C::VB;
-                if constexpr (sizeof(KV) == 2) {
-                    if constexpr (C::DPL == 4) {
-                        const uint2 w = *reinterpret_cast<const uint2 *>(vrow);
-                        vf[0] = bf16_lo(w.x);
-                        vf[1] = bf16_hi(w.x);
-                        vf[2] = bf16_lo(w.y);
-                        vf[3] = bf16_hi(w.y);
-                    } else {
-                        const uint32_t w = *reinterpret_cast<const uint32_t *>(vrow);
-                        vf[0] = bf16_lo(w);
-                        vf[1] = bf16_hi(w);
-                    }
-                } else {
-                    if constexpr (C::DPL == 4) {
-                        const float4 w = *reinterpret_cast<const float4 *>(vrow);
-                        vf[0] = w.x;
-                        vf[1] = w.y;
-                        vf[2] = w.z;
-                        vf[3] = w.w;
-                    } else {
-                        const float2 w = *reinterpret_cast<const float2 *>(vrow);
-                        vf[0] = w.x;
-                        vf[1] = w.y;
-                    }
-                }
+                load_v_slice<C::DPL>(Vs + key2 * C::RB + lane * C::VB, vf, (KV *)nullptr);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float pk = slot[gg * G + h];
+                for (int h = 0; h < G; ++h)
 #pragma unroll
-                    for (int e = 0; e < C::DPL / 2; ++e)
-                        o[h][e] = __ffma2_rn(make_float2(pk, pk), make_float2(vf[2 * e], vf[2 * e + 1]), o[h][e]);
-                }
+                    for (int e = 0; e < C::DPL; ++e)
+                        o[h][e] = fmaf(pk[h], vf[e], o[h][e]);
             }
             pslot ^= 1;
         }
@@ -434,12 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         if (!(d.flags & kLast))
             continue;
 
-        // ---- end of item: the lane groups' sums, then merge the 12 warps
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            l[h] += __shfl_xor_sync(kFull, l[h], 8);
-            l[h] += __shfl_xor_sync(kFull, l[h], 16);
-        }
+        // ---- end of item: the key groups' sums, then merge the 12 warps
+        l_mine += __shfl_xor_sync(kFull, l_mine, 8);
+        l_mine += __shfl_xor_sync(kFull, l_mine, 16);
         ok = mbar_wait_bounded(merge_out, merge_phase ^ 1, abort_flag);
         if (!__all_sync(kFull, ok))
             break;
@@ -447,15 +483,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         for (int h = 0; h < G; ++h) {
             float *dst = merge_o + (warp * G + h) * D + lane * C::DPL;
 #pragma unroll
-            for (int e = 0; e < C::DPL / 2; ++e)
-                *reinterpret_cast<float2 *>(dst + 2 * e) = o[h][e];
+            for (int e = 0; e < C::DPL; e += 2)
+                *reinterpret_cast<float2 *>(dst + e) = make_float2(o[h][e], o[h][e + 1]);
         }
-        if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                merge_m[warp * G + h] = m_run[h];
-                merge_l[warp * G + h] = l[h];
-            }
+        if (lane < 8 && t % kLanesPerHead == 0) {
+            merge_m[warp * G + hm] = m_mine;
+            merge_l[warp * G + hm] = l_mine;
         }
         __syncwarp();
         if (lane == 0)
