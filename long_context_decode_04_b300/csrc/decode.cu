@@ -51,6 +51,8 @@
 //     TA_DEVERR_TIMEOUT, stops, and drains its own outstanding copies.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -181,13 +183,15 @@ struct Cfg {
     static constexpr int QPL_W = NCH * 4;           // 32-bit q words held by a lane per head
     static constexpr int DPL = D / 32;              // output dims owned by a lane (PV)
     static constexpr int VB = DPL * (int)sizeof(KV);// V bytes read by a lane per key
+    static constexpr int PB = (G * (DPL + 1) > 24) ? 2 : 4;  // keys per PV load batch (register budget)
     static constexpr int KV_OFF = kTile * RB;       // V tile offset inside a stage
     static constexpr int STAGE = 2 * kTile * RB;
     static constexpr int STAGES = (196608 / STAGE) > 6 ? 6 : (196608 / STAGE);
     static constexpr int MERGE_FLOATS = kConsumerWarps * G * (D + 2);
     static constexpr int PBUF_FLOATS = kConsumerWarps * 2 * 4 * G;
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE + (size_t)(MERGE_FLOATS + PBUF_FLOATS) * 4 +
-                                   (2 * STAGES + 4) * 8 + STAGES * sizeof(TileDesc) + 16;
+    static constexpr int FM_FLOATS = 2 * G * kFusedMergeMaxSplits;  // partial m, l of one unit
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE + (size_t)(MERGE_FLOATS + PBUF_FLOATS + FM_FLOATS) * 4 +
+                                   (2 * STAGES + 5) * 8 + STAGES * sizeof(TileDesc) + 16;
     static_assert(NCH >= 1 && RB % 128 == 0, "row must be a multiple of 128 bytes");
     static_assert(STAGES >= 2, "need at least two stages");
     static_assert(DPL % 2 == 0, "lanes own an even number of output dims");
@@ -202,14 +206,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
     float *merge_m = merge_o + kConsumerWarps * G * D;                         // [W][G]
     float *merge_l = merge_m + kConsumerWarps * G;                             // [W][G]
     float *pbuf = merge_l + kConsumerWarps * G;                                // [W][2][4][G]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(pbuf + C::PBUF_FLOATS);
+    float *fm_m = pbuf + C::PBUF_FLOATS;                                       // [G][n_split]
+    float *fm_l = fm_m + G * kFusedMergeMaxSplits;                             // [G][n_split]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(fm_l + G * kFusedMergeMaxSplits);
     uint64_t *full = bars;
     uint64_t *empty = bars + C::STAGES;
     uint64_t *merge_in = bars + 2 * C::STAGES;
     uint64_t *merge_out = merge_in + 1;
     uint64_t *written = merge_in + 2;  // consumers' partial stores done (fused mode)
     uint64_t *ticket = merge_in + 3;   // the ticket's outcome is in *ticket_flag
-    TileDesc *desc = reinterpret_cast<TileDesc *>(bars + 2 * C::STAGES + 4);
+    uint64_t *fm_ready = merge_in + 4; // fm_m / fm_l staged (fused merge)
+    TileDesc *desc = reinterpret_cast<TileDesc *>(bars + 2 * C::STAGES + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(desc + C::STAGES);
     volatile int *ticket_flag = abort_flag + 1;
 
@@ -225,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         mbar_init(merge_out, kConsumerWarps);
         mbar_init(written, kConsumerThreads);
         mbar_init(ticket, 1);
+        mbar_init(fm_ready, kConsumerThreads);
         *abort_flag = 0;
         *ticket_flag = 0;
         fence_barrier_init();
@@ -328,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
     float l_mine = 0.f;        // sum of this key group's weights for head hm
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t merge_phase = 0, ticket_phase = 0;
+    uint32_t merge_phase = 0, ticket_phase = 0, fm_phase = 0;
     int b = 0, kvh = 0, split = 0, unit = 0;
     int pslot = 0;
     float *my_pbuf = pbuf + warp * (2 * 4 * G);
@@ -367,12 +375,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         const unsigned char *Ks = smem + stage * C::STAGE;
         const unsigned char *Vs = Ks + C::KV_OFF;
         const int kbeg = warp * kKeysPerWarp;
-#pragma unroll
-        for (int st4 = 0; st4 < kKeysPerWarp; st4 += 4) {
-            if (kbeg + st4 >= d.n)
-                break;  // warp-uniform
+        // One 4-key step.  FULL: all keys of this warp's slice are present
+        // (every tile but a chunk's last), so no key needs a bounds check.
+        auto step = [&](int st4, auto full_tag) {
+            constexpr bool FULL = decltype(full_tag)::value;
             const int key = kbeg + st4 + g;
-            const bool valid = key < d.n;
+            const bool valid = FULL || key < d.n;
             // ---- <q_h, k> partial sums over this lane's slice of the row
             float ae[G], ao[G];
 #pragma unroll
@@ -446,22 +454,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
             if (t % kLanesPerHead == 0)
                 slot[g * G + hm] = pw;
             __syncwarp();
+            const int nk = FULL ? 4 : min(4, d.n - (kbeg + st4));
+            // keys are loaded C::PB at a time, then accumulated
 #pragma unroll
-            for (int gg = 0; gg < 4; ++gg) {
-                const int key2 = kbeg + st4 + gg;
-                if (key2 >= d.n)
-                    break;  // warp-uniform
-                float pk[G];
-                load_weights<G>(slot + gg * G, pk);
-                float vf[C::DPL];
-                load_v_slice<C::DPL>(Vs + key2 * C::RB + lane * C::VB, vf, (KV *)nullptr);
+            for (int g0 = 0; g0 < 4; g0 += C::PB) {
+                float pk[C::PB][G];
+                float vf[C::PB][C::DPL];
 #pragma unroll
-                for (int h = 0; h < G; ++h)
+                for (int gg = 0; gg < C::PB; ++gg) {
+                    if (FULL || g0 + gg < nk) {
+                        load_weights<G>(slot + (g0 + gg) * G, pk[gg]);
+                        load_v_slice<C::DPL>(Vs + (kbeg + st4 + g0 + gg) * C::RB + lane * C::VB, vf[gg],
+                                             (KV *)nullptr);
+                    }
+                }
 #pragma unroll
-                    for (int e = 0; e < C::DPL; ++e)
-                        o[h][e] = fmaf(pk[h], vf[e], o[h][e]);
+                for (int gg = 0; gg < C::PB; ++gg) {
+                    if (FULL || g0 + gg < nk) {
+#pragma unroll
+                        for (int h = 0; h < G; ++h)
+#pragma unroll
+                            for (int e = 0; e < C::DPL; ++e)
+                                o[h][e] = fmaf(pk[gg][h], vf[gg][e], o[h][e]);
+                    }
+                }
             }
             pslot ^= 1;
+        };
+        if (d.n == kTile) {
+#pragma unroll
+            for (int st4 = 0; st4 < kKeysPerWarp; st4 += 4)
+                step(st4, std::true_type{});
+        } else {
+            for (int st4 = 0; st4 < kKeysPerWarp && kbeg + st4 < d.n; st4 += 4)
+                step(st4, std::false_type{});
         }
         __syncwarp();
         if (lane == 0)
@@ -556,30 +582,53 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
             break;
         if (!*ticket_flag)
             continue;
+        // Stage the unit's partial m and l in shared memory, then every thread
+        // owns 4 consecutive dims of one head, with its loads of o in flight
+        // together.
         const int ns = p.n_split;
-        for (int idx = tid; idx < G * D; idx += kConsumerThreads) {
-            const int h = idx / D;
-            const int dd = idx - h * D;
-            const size_t row = row0 + h;
-            const float *pm = p.part_m + row * ns;
-            const float *pl = p.part_l + row * ns;
-            const float *po = p.part_o + row * ns * D + dd;
+        for (int i = tid; i < G * ns; i += kConsumerThreads) {
+            const int h = i / ns;
+            const size_t pi = (row0 + h) * ns + (i - h * ns);
+            fm_m[i] = __ldcg(p.part_m + pi);
+            fm_l[i] = __ldcg(p.part_l + pi);
+        }
+        mbar_arrive(fm_ready);
+        ok = mbar_wait_bounded(fm_ready, fm_phase, abort_flag);
+        fm_phase ^= 1;
+        if (!__all_sync(kFull, ok))
+            break;
+        for (int idx = tid; idx < G * D / 4; idx += kConsumerThreads) {
+            const int h = idx / (D / 4);
+            const int d4 = (idx - h * (D / 4)) * 4;
+            const float *mh = fm_m + h * ns;
+            const float *lh = fm_l + h * ns;
             float mx = -INFINITY;
             for (int n = 0; n < ns; ++n)
-                mx = fmaxf(mx, __ldcg(pm + n));
-            float ls = 0.f, os = 0.f;
+                mx = fmaxf(mx, mh[n]);
+            float ls = 0.f;
+            float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
             if (mx != -INFINITY) {
+                const float4 *po = reinterpret_cast<const float4 *>(p.part_o + (row0 + h) * ns * D + d4);
+#pragma unroll 4
                 for (int n = 0; n < ns; ++n) {
-                    const float mn = __ldcg(pm + n);
+                    const float mn = mh[n];
                     const float a = mn == -INFINITY ? 0.f : fast_exp2((mn - mx) * kLog2e);
-                    ls = fmaf(a, __ldcg(pl + n), ls);
-                    os = fmaf(a, __ldcg(po + (size_t)n * D), os);
+                    const float4 x = __ldcg(po + (size_t)n * (D / 4));
+                    ls = fmaf(a, lh[n], ls);
+                    os.x = fmaf(a, x.x, os.x);
+                    os.y = fmaf(a, x.y, os.y);
+                    os.z = fmaf(a, x.z, os.z);
+                    os.w = fmaf(a, x.w, os.w);
                 }
             }
             const float inv = ls > 0.f ? 1.0f / ls : 0.f;
-            store_out(static_cast<OUT *>(p.out) + row * D + dd, os * inv);
-            if (dd == 0 && p.lse)
-                p.lse[row] = ls > 0.f ? mx + fast_log2(ls) * kLn2 : -INFINITY;
+            OUT *dst = static_cast<OUT *>(p.out) + (row0 + h) * D + d4;
+            store_out(dst + 0, os.x * inv);
+            store_out(dst + 1, os.y * inv);
+            store_out(dst + 2, os.z * inv);
+            store_out(dst + 3, os.w * inv);
+            if (d4 == 0 && p.lse)
+                p.lse[row0 + h] = ls > 0.f ? mx + fast_log2(ls) * kLn2 : -INFINITY;
         }
     }
 }
