@@ -17,15 +17,16 @@
 // the kernel streams K and V at full bandwidth and keeps the arithmetic
 // (about 4 FLOP per byte at G = 4) under it.
 //
-// Kernel layout (one persistent CTA per SM, 13 warps):
-//   * warp 12, lane 0 is the producer.  It pulls work items
+// Kernel layout (one persistent CTA per SM, 16 warps):
+//   * warp 15, lane 0 is the producer.  It pulls work items
 //     (sequence, KV head, chunk) from a device-wide queue and stages the
-//     chunk's K and V rows into shared memory, kTile keys at a time, with
+//     chunk's K and V rows into shared memory, a tile at a time, with
 //     one-dimensional bulk async copies into a ring of stages guarded by
 //     mbarriers.  Each stage carries a descriptor (item, first key, key
 //     count, first/last flags) so the consumers need no schedule.
-//   * warps 0-11 consume; warp w owns keys [8w, 8w + 8) of every tile, in
-//     two steps of 4 keys.
+//   * warps 0-14 consume; warp w owns keys [KPW w, KPW w + KPW) of every
+//     tile (KPW = 8 keys, two steps of 4; 4 for 512-byte rows), so a tile
+//     is 120 (or 60) keys.
 //       scores: 8 lanes share a key, each holding 16 bytes x NCH of the
 //         row; the G query heads of the KV head (grouped-query attention)
 //         use each staged row.  For bf16 K the products use the
@@ -40,7 +41,7 @@
 //       PV: the weights go through shared memory (one vector load per key),
 //         and every lane owns D/32 output dimensions of every head,
 //         accumulated in fp32 over the warp's keys.
-//     At the end of an item the 12 warps are merged through shared memory
+//     At the end of an item the 15 warps are merged through shared memory
 //     by the log-sum-exp rule and the item's partial (or, with one chunk,
 //     the final output and lse) is written.
 //   * Fused merge: the CTA that finishes the last chunk of a (sequence,
@@ -59,15 +60,12 @@
 namespace ta {
 namespace {
 
-constexpr int kConsumerWarps = 12;
+constexpr int kConsumerWarps = 15;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;
-constexpr int kKeysPerWarp = 8;                        // per stage
-constexpr int kTile = kConsumerWarps * kKeysPerWarp;  // keys per stage
+constexpr int kThreads = kConsumerThreads + 32;  // 16 warps: 128 registers a thread
 constexpr float kRescaleLog2 = 8.0f;
 constexpr unsigned kFull = 0xffffffffu;
 
-static_assert(kTile == kDecodeTileKeys, "scheduler and kernel disagree on the tile");
 
 enum : int { kFirst = 1, kLast = 2, kEnd = 4 };
 enum : int { kModeFinal = 0, kModePartials = 1, kModeFused = 2 };
@@ -184,8 +182,10 @@ struct Cfg {
     static constexpr int DPL = D / 32;              // output dims owned by a lane (PV)
     static constexpr int VB = DPL * (int)sizeof(KV);// V bytes read by a lane per key
     static constexpr int PB = (G * (DPL + 1) > 24) ? 2 : 4;  // keys per PV load batch (register budget)
-    static constexpr int KV_OFF = kTile * RB;       // V tile offset inside a stage
-    static constexpr int STAGE = 2 * kTile * RB;
+    static constexpr int KPW = RB > 256 ? 4 : 8;    // keys per consumer warp per stage
+    static constexpr int TILE = kConsumerWarps * KPW;  // keys per stage
+    static constexpr int KV_OFF = TILE * RB;        // V tile offset inside a stage
+    static constexpr int STAGE = 2 * TILE * RB;
     static constexpr int STAGES = (196608 / STAGE) > 6 ? 6 : (196608 / STAGE);
     static constexpr int MERGE_FLOATS = kConsumerWarps * G * (D + 2);
     static constexpr int PBUF_FLOATS = kConsumerWarps * 2 * 4 * G;
@@ -194,6 +194,7 @@ struct Cfg {
                                    (2 * STAGES + 5) * 8 + STAGES * sizeof(TileDesc) + 16;
     static_assert(NCH >= 1 && RB % 128 == 0, "row must be a multiple of 128 bytes");
     static_assert(STAGES >= 2, "need at least two stages");
+    static_assert(kDecodeTileKeys % TILE == 0, "chunks must be whole tiles");
     static_assert(DPL % 2 == 0, "lanes own an even number of output dims");
 };
 
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
             int j0 = c0;
             int flags = kFirst;
             for (;;) {
-                const int n = max(0, min(kTile, c1 - j0));
+                const int n = max(0, min(C::TILE, c1 - j0));
                 const bool last = j0 + n >= c1;
                 if (last)
                     flags |= kLast;
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
 
         const unsigned char *Ks = smem + stage * C::STAGE;
         const unsigned char *Vs = Ks + C::KV_OFF;
-        const int kbeg = warp * kKeysPerWarp;
+        const int kbeg = warp * C::KPW;
         // One 4-key step.  FULL: all keys of this warp's slice are present
         // (every tile but a chunk's last), so no key needs a bounds check.
         auto step = [&](int st4, auto full_tag) {
@@ -481,12 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
             }
             pslot ^= 1;
         };
-        if (d.n == kTile) {
+        if (d.n == C::TILE) {
 #pragma unroll
-            for (int st4 = 0; st4 < kKeysPerWarp; st4 += 4)
+            for (int st4 = 0; st4 < C::KPW; st4 += 4)
                 step(st4, std::true_type{});
         } else {
-            for (int st4 = 0; st4 < kKeysPerWarp && kbeg + st4 < d.n; st4 += 4)
+            for (int st4 = 0; st4 < C::KPW && kbeg + st4 < d.n; st4 += 4)
                 step(st4, std::false_type{});
         }
         __syncwarp();
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         if (!(d.flags & kLast))
             continue;
 
-        // ---- end of item: the key groups' sums, then merge the 12 warps
+        // ---- end of item: the key groups' sums, then merge the consumer warps
         l_mine += __shfl_xor_sync(kFull, l_mine, 8);
         l_mine += __shfl_xor_sync(kFull, l_mine, 16);
         ok = mbar_wait_bounded(merge_out, merge_phase ^ 1, abort_flag);

@@ -12,7 +12,7 @@ namespace ta {
 
 constexpr int kFanin = 64;            // partials merged by one warp per level
 constexpr int kStatusBytes = 256;     // status word region at the workspace start
-constexpr int kDecodeTileKeys = 96;   // keys the decode kernel stages per tile
+constexpr int kDecodeTileKeys = 120;  // chunks are whole multiples of this many keys (the decode tile)
 // A split decode's workspace starts with a fixed control region that no
 // other use of the workspace writes: the status word and work-queue counter
 // (first 256 bytes), then one chunk counter per (sequence, KV head).

@@ -8,7 +8,7 @@
 // here keeps every SM busy: the persistent decode kernel runs
 // sm_count * ctas_per_sm CTAs, and the chunk count is chosen so that the
 // (sequence, KV head, chunk) work items fill those CTAs evenly.  Chunks are
-// whole numbers of the kernel's 96-key tiles.
+// whole numbers of the kernel's 120-key tiles.
 #include <algorithm>
 #include <climits>
 

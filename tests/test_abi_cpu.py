@@ -59,7 +59,7 @@ def test_plan_of_the_128k_workload_fills_the_sms_evenly():
     plan = ta.plan_decode(1, 32, 8, 131072, 128, sm_count=SMS)
     items = 8 * plan.n_split
     assert items % SMS == 0 and plan.grid == SMS
-    assert plan.chunk % 96 == 0 and plan.chunk >= 192  # whole 96-key tiles
+    assert plan.chunk % 120 == 0 and plan.chunk >= 240  # whole 120-key tiles
 
 
 def test_plan_overrides():
