@@ -105,19 +105,64 @@ struct Elem<__nv_bfloat16> {
 __device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
-// ae += a.lo * b.lo, ao += a.hi * b.hi for packed bf16 pairs a, b: the
-// mixed-precision FMA takes bf16 operands and an fp32 accumulator, so K
-// needs no conversion (exactly fmaf of the widened values).
-__device__ __forceinline__ void fma_bf16x2(float &ae, float &ao, uint32_t a, uint32_t b)
+// acc += a.lo * b.lo + a.hi * b.hi for packed bf16 pairs a, b: the
+// mixed-precision FMA takes bf16 operands and an fp32 accumulator, so
+// neither operand is widened (each step is exactly fmaf of the widened
+// values).
+__device__ __forceinline__ void fma_bf16(float &acc, uint32_t a, uint32_t b)
 {
     asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
-        "mov.b32 {al, ah}, %2;\n\t"
-        "mov.b32 {bl, bh}, %3;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
         "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
-        "fma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
-        : "+f"(ae), "+f"(ao)
+        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+        : "+f"(acc)
         : "r"(a), "r"(b));
 }
+
+// Where the scores of a step land after the 8-lane reduce-scatter.  A lane
+// group has NV = KPG * G (key, head) dot products; lane t ends with NVL of
+// them, score index (t / RED) * NVL + j, key kk = index / G, head
+// h = index % G, and RED lanes hold each one when NV < 8.
+template <int KPG_, int G>
+struct Lay {
+    static constexpr int KPG = KPG_;
+    static constexpr int NV = KPG * G;
+    static constexpr int NVL = NV >= 8 ? NV / 8 : 1;
+    static constexpr int RED = NV >= 8 ? 1 : 8 / NV;
+    __host__ __device__ static constexpr int idx_of(int t, int j) { return (t / RED) * NVL + j; }
+    __host__ __device__ static constexpr int kk_of(int t, int j) { return idx_of(t, j) / G; }
+    __host__ __device__ static constexpr int h_of(int t, int j) { return idx_of(t, j) % G; }
+    // Whether xor-ing the lane index with `mask` keeps the head of every
+    // value j (masks 8 and 16 only change the group).
+    __host__ __device__ static constexpr bool preserves_head(int mask)
+    {
+        if (mask >= 8)
+            return true;
+        for (int tt = 0; tt < 8; ++tt)
+            for (int j = 0; j < NVL; ++j)
+                if (h_of(tt, j) != h_of(tt ^ mask, j))
+                    return false;
+        return true;
+    }
+    // A lane of group 0 that holds head h (as its value j_of_head(h), key 0).
+    __host__ __device__ static constexpr int lane_of_head(int h)
+    {
+        for (int tt = 0; tt < 8; ++tt)
+            for (int j = 0; j < NVL; ++j)
+                if (h_of(tt, j) == h && kk_of(tt, j) == 0 && tt % RED == 0)
+                    return tt;
+        return 0;
+    }
+    __host__ __device__ static constexpr int j_of_head(int h)
+    {
+        for (int tt = 0; tt < 8; ++tt)
+            for (int j = 0; j < NVL; ++j)
+                if (h_of(tt, j) == h && kk_of(tt, j) == 0 && tt % RED == 0)
+                    return j;
+        return 0;
+    }
+};
 
 // The G weights of one key from shared memory (one vector load).
 template <int G>
@@ -188,7 +233,7 @@ struct Cfg {
     static constexpr int STAGE = 2 * TILE * RB;
     static constexpr int STAGES = (196608 / STAGE) > 6 ? 6 : (196608 / STAGE);
     static constexpr int MERGE_FLOATS = kConsumerWarps * G * (D + 2);
-    static constexpr int PBUF_FLOATS = kConsumerWarps * 2 * 4 * G;
+    static constexpr int PBUF_FLOATS = kConsumerWarps * KPW * G;
     static constexpr int FM_FLOATS = 2 * G * kFusedMergeMaxSplits;  // partial m, l of one unit
     static constexpr size_t SMEM = (size_t)STAGES * STAGE + (size_t)(MERGE_FLOATS + PBUF_FLOATS + FM_FLOATS) * 4 +
                                    (2 * STAGES + 5) * 8 + STAGES * sizeof(TileDesc) + 16;
@@ -206,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
     float *merge_o = reinterpret_cast<float *>(smem + C::STAGES * C::STAGE);  // [W][G][D]
     float *merge_m = merge_o + kConsumerWarps * G * D;                         // [W][G]
     float *merge_l = merge_m + kConsumerWarps * G;                             // [W][G]
-    float *pbuf = merge_l + kConsumerWarps * G;                                // [W][2][4][G]
+    float *pbuf = merge_l + kConsumerWarps * G;                                // [W][KPW][G]
     float *fm_m = pbuf + C::PBUF_FLOATS;                                       // [G][n_split]
     float *fm_l = fm_m + G * kFusedMergeMaxSplits;                             // [G][n_split]
     uint64_t *bars = reinterpret_cast<uint64_t *>(fm_l + G * kFusedMergeMaxSplits);
@@ -323,24 +368,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
     }
 
     // ---------------------------------------------------------------- consumers
-    const int g = lane >> 3;  // key slot within a 4-key step
-    const int t = lane & 7;   // lane within the 8-lane key group
+    // Score layout.  A warp's KPW keys of a tile are processed in one step:
+    // lane group g (8 lanes) takes keys kbeg + g*KPG + kk, kk < KPG.  Each
+    // group reduces its NV = KPG*G (key, head) dot products by a
+    // reduce-scatter, after which lane t holds NVL of them (score index
+    // (t / RED) * NVL + j, RED lanes holding each when NV < 8).
+    using L = Lay<C::KPW / 4, G>;
+    const int g = lane >> 3;  // lane group
+    const int t = lane & 7;   // lane within the group
     const int tid = threadIdx.x;
-    // After the reduce-scatter of the scores, lane t of a key group holds
-    // the score of head hm = t / (8 / G); 8 / G lanes share each head.
-    constexpr int kLanesPerHead = 8 / G;
-    const int hm = t / kLanesPerHead;
 
     uint32_t qw[G][C::QPL_W];  // this lane's q slice: bf16 pairs, or fp32 bits
     float o[G][C::DPL];        // this lane's output dims of every head, unnormalised
-    float m_mine = -INFINITY;  // running reference of head hm (log2 units), warp-uniform per head
-    float l_mine = 0.f;        // sum of this key group's weights for head hm
+    float m_run[L::NVL];       // running reference (log2 units) of this lane's heads, warp-uniform per head
+    float l_run[L::NVL];       // this lane's share of those heads' weight sums
     int stage = 0;
     uint32_t phase = 0;
     uint32_t merge_phase = 0, ticket_phase = 0, fm_phase = 0;
     int b = 0, kvh = 0, split = 0, unit = 0;
-    int pslot = 0;
-    float *my_pbuf = pbuf + warp * (2 * 4 * G);
+    float *slot = pbuf + warp * (C::KPW * G);  // this warp's weights [KPW][G]
+    int my_kidx[L::NVL], my_h[L::NVL];          // key (within the warp's KPW) and head of value j
+#pragma unroll
+    for (int j = 0; j < L::NVL; ++j) {
+        my_kidx[j] = g * L::KPG + L::kk_of(t, j);
+        my_h[j] = L::h_of(t, j);
+    }
 
     for (;;) {
         bool ok = mbar_wait_bounded(&full[stage], phase, abort_flag);
@@ -369,49 +421,50 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
                 for (int e = 0; e < C::DPL; ++e)
                     o[h][e] = 0.f;
             }
-            m_mine = -INFINITY;
-            l_mine = 0.f;
+#pragma unroll
+            for (int j = 0; j < L::NVL; ++j) {
+                m_run[j] = -INFINITY;
+                l_run[j] = 0.f;
+            }
         }
 
         const unsigned char *Ks = smem + stage * C::STAGE;
         const unsigned char *Vs = Ks + C::KV_OFF;
         const int kbeg = warp * C::KPW;
-        // One 4-key step.  FULL: all keys of this warp's slice are present
-        // (every tile but a chunk's last), so no key needs a bounds check.
-        auto step = [&](int st4, auto full_tag) {
+        // FULL: all KPW keys of this warp are present (every tile but a
+        // chunk's last), so no key needs a bounds check.
+        auto step = [&](auto full_tag) {
             constexpr bool FULL = decltype(full_tag)::value;
-            const int key = kbeg + st4 + g;
-            const bool valid = FULL || key < d.n;
-            // ---- <q_h, k> partial sums over this lane's slice of the row
-            float ae[G], ao[G];
+            const int nvalid = FULL ? C::KPW : min(C::KPW, d.n - kbeg);
+            // ---- <q_h, k> partial sums over this lane's slice of each row
+            float v[L::NV];
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-                ae[h] = ao[h] = 0.f;
-            if (valid) {
+            for (int i = 0; i < L::NV; ++i)
+                v[i] = 0.f;
 #pragma unroll
-                for (int i = 0; i < C::NCH; ++i) {
-                    const uint4 kr = *reinterpret_cast<const uint4 *>(Ks + key * C::RB + (t + 8 * i) * 16);
-                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+            for (int kk = 0; kk < L::KPG; ++kk) {
+                const int kidx = g * L::KPG + kk;
+                if (FULL || kidx < nvalid) {
 #pragma unroll
-                    for (int h = 0; h < G; ++h)
+                    for (int i = 0; i < C::NCH; ++i) {
+                        const uint4 kr =
+                            *reinterpret_cast<const uint4 *>(Ks + (kbeg + kidx) * C::RB + (t + 8 * i) * 16);
+                        const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            if constexpr (sizeof(KV) == 2) {
-                                fma_bf16x2(ae[h], ao[h], qw[h][4 * i + w], kw[w]);
-                            } else if (w & 1) {
-                                ao[h] = fmaf(__uint_as_float(qw[h][4 * i + w]), __uint_as_float(kw[w]), ao[h]);
-                            } else {
-                                ae[h] = fmaf(__uint_as_float(qw[h][4 * i + w]), __uint_as_float(kw[w]), ae[h]);
+                        for (int h = 0; h < G; ++h)
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                if constexpr (sizeof(KV) == 2)
+                                    fma_bf16(v[kk * G + h], qw[h][4 * i + w], kw[w]);
+                                else
+                                    v[kk * G + h] = fmaf(__uint_as_float(qw[h][4 * i + w]), __uint_as_float(kw[w]),
+                                                         v[kk * G + h]);
                             }
-                        }
+                    }
                 }
             }
-            // ---- 8-lane reduce-scatter: head hm's full score lands in this lane
-            float v[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-                v[h] = ae[h] + ao[h];
-            int n = G;
+            // ---- 8-lane reduce-scatter (then all-reduce while NV < 8)
+            int n = L::NV;
 #pragma unroll
             for (int r = 0; r < 3; ++r) {
                 const int mask = 4 >> r;
@@ -428,68 +481,75 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
                     v[0] += __shfl_xor_sync(kFull, v[0], mask);
                 }
             }
-            const float sc = valid ? v[0] * p.qscale : -INFINITY;  // log2 units
-            // ---- lazy rescale of the running reference (warp vote)
-            if (__any_sync(kFull, sc > m_mine + kRescaleLog2)) {
-                float mx = sc;
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-                float alpha = 1.f;
-                if (mx > m_mine + kRescaleLog2) {
-                    alpha = m_mine == -INFINITY ? 0.f : fast_exp2(m_mine - mx);
-                    m_mine = mx;
-                    l_mine *= alpha;
+            float sc[L::NVL];
+            bool need = false;
+#pragma unroll
+            for (int j = 0; j < L::NVL; ++j) {
+                sc[j] = (FULL || my_kidx[j] < nvalid) ? v[j] * p.qscale : -INFINITY;  // log2 units
+                need |= sc[j] > m_run[j] + kRescaleLog2;
+            }
+            // ---- lazy rescale of the running references (warp vote)
+            if (__any_sync(kFull, need)) {
+                float alpha[L::NVL];
+#pragma unroll
+                for (int j = 0; j < L::NVL; ++j) {
+                    float mx = sc[j];
+#pragma unroll
+                    for (int mask = 1; mask < 32; mask <<= 1)
+                        if (L::preserves_head(mask))
+                            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, mask));
+                    alpha[j] = 1.f;
+                    if (mx > m_run[j] + kRescaleLog2) {
+                        alpha[j] = m_run[j] == -INFINITY ? 0.f : fast_exp2(m_run[j] - mx);
+                        m_run[j] = mx;
+                        l_run[j] *= alpha[j];
+                    }
                 }
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    const float a = __shfl_sync(kFull, alpha, h * kLanesPerHead);
+                    const float a = __shfl_sync(kFull, alpha[L::j_of_head(h)], L::lane_of_head(h));
 #pragma unroll
                     for (int e = 0; e < C::DPL; ++e)
                         o[h][e] *= a;
                 }
             }
-            const float pw = valid ? fast_exp2(sc - m_mine) : 0.f;
-            l_mine += pw;
-            // ---- PV: the 4 keys' weights through shared memory, lanes own dims
-            float *slot = my_pbuf + pslot * (4 * G);
-            if (t % kLanesPerHead == 0)
-                slot[g * G + hm] = pw;
-            __syncwarp();
-            const int nk = FULL ? 4 : min(4, d.n - (kbeg + st4));
-            // keys are loaded C::PB at a time, then accumulated
+            // ---- weights: one exp per score, into shared memory for PV
 #pragma unroll
-            for (int g0 = 0; g0 < 4; g0 += C::PB) {
+            for (int j = 0; j < L::NVL; ++j) {
+                const float pw = (FULL || my_kidx[j] < nvalid) ? fast_exp2(sc[j] - m_run[j]) : 0.f;
+                l_run[j] += pw;
+                if (t % L::RED == 0)
+                    slot[my_kidx[j] * G + my_h[j]] = pw;
+            }
+            __syncwarp();
+            // ---- PV: lanes own D/32 dims of every head; keys C::PB at a time
+#pragma unroll
+            for (int k0 = 0; k0 < C::KPW; k0 += C::PB) {
                 float pk[C::PB][G];
                 float vf[C::PB][C::DPL];
 #pragma unroll
-                for (int gg = 0; gg < C::PB; ++gg) {
-                    if (FULL || g0 + gg < nk) {
-                        load_weights<G>(slot + (g0 + gg) * G, pk[gg]);
-                        load_v_slice<C::DPL>(Vs + (kbeg + st4 + g0 + gg) * C::RB + lane * C::VB, vf[gg],
-                                             (KV *)nullptr);
+                for (int kk = 0; kk < C::PB; ++kk) {
+                    if (FULL || k0 + kk < nvalid) {
+                        load_weights<G>(slot + (k0 + kk) * G, pk[kk]);
+                        load_v_slice<C::DPL>(Vs + (kbeg + k0 + kk) * C::RB + lane * C::VB, vf[kk], (KV *)nullptr);
                     }
                 }
 #pragma unroll
-                for (int gg = 0; gg < C::PB; ++gg) {
-                    if (FULL || g0 + gg < nk) {
+                for (int kk = 0; kk < C::PB; ++kk) {
+                    if (FULL || k0 + kk < nvalid) {
 #pragma unroll
                         for (int h = 0; h < G; ++h)
 #pragma unroll
                             for (int e = 0; e < C::DPL; ++e)
-                                o[h][e] = fmaf(pk[gg][h], vf[gg][e], o[h][e]);
+                                o[h][e] = fmaf(pk[kk][h], vf[kk][e], o[h][e]);
                     }
                 }
             }
-            pslot ^= 1;
         };
-        if (d.n == C::TILE) {
-#pragma unroll
-            for (int st4 = 0; st4 < C::KPW; st4 += 4)
-                step(st4, std::true_type{});
-        } else {
-            for (int st4 = 0; st4 < C::KPW && kbeg + st4 < d.n; st4 += 4)
-                step(st4, std::false_type{});
-        }
+        if (d.n >= kbeg + C::KPW)
+            step(std::true_type{});
+        else if (d.n > kbeg)
+            step(std::false_type{});
         __syncwarp();
         if (lane == 0)
             mbar_arrive(&empty[stage]);
@@ -500,9 +560,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         if (!(d.flags & kLast))
             continue;
 
-        // ---- end of item: the key groups' sums, then merge the consumer warps
-        l_mine += __shfl_xor_sync(kFull, l_mine, 8);
-        l_mine += __shfl_xor_sync(kFull, l_mine, 16);
+        // ---- end of item: each head's weight sum over the warp, then merge
+        // the consumer warps
+#pragma unroll
+        for (int j = 0; j < L::NVL; ++j) {
+            if (t % L::RED != 0)
+                l_run[j] = 0.f;  // redundant copies count once
+#pragma unroll
+            for (int mask = 1; mask < 32; mask <<= 1)
+                if (L::preserves_head(mask))
+                    l_run[j] += __shfl_xor_sync(kFull, l_run[j], mask);
+        }
         ok = mbar_wait_bounded(merge_out, merge_phase ^ 1, abort_flag);
         if (!__all_sync(kFull, ok))
             break;
@@ -513,9 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
             for (int e = 0; e < C::DPL; e += 2)
                 *reinterpret_cast<float2 *>(dst + e) = make_float2(o[h][e], o[h][e + 1]);
         }
-        if (lane < 8 && t % kLanesPerHead == 0) {
-            merge_m[warp * G + hm] = m_mine;
-            merge_l[warp * G + hm] = l_mine;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            if (lane == L::lane_of_head(h)) {
+                merge_m[warp * G + h] = m_run[L::j_of_head(h)];
+                merge_l[warp * G + h] = l_run[L::j_of_head(h)];
+            }
         }
         __syncwarp();
         if (lane == 0)
