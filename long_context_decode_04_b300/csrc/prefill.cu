@@ -12,9 +12,10 @@
 //
 // One CTA owns two 128-row query tiles (rows q0 .. q0 + 255) of one
 // (b, h) and walks the 128-key K/V tiles up to the causal diagonal:
-//   warp 8   TMA producer: loads both Q tiles once, then K and V tiles into
-//            a 2-stage shared-memory ring (128-byte swizzle, two 64-column
-//            boxes per tile).  It also allocates and frees the TMEM.
+//   warp 8   TMA producer: loads both Q tiles once, then K tiles into a
+//            3-stage and V tiles into a 2-stage shared-memory ring (128-byte
+//            swizzle, two 64-column boxes per tile), K one tile ahead of V.
+//            It also allocates and frees the TMEM.
 //   warp 9   MMA issuer (one thread): per K tile j and query tile t,
 //              PV_t(j-1): O_t += P_t(j-1) V_{j-1}  (P from TMEM, V MN-major)
 //              S_t(j)   = Q_t K_j^T                (both K-major)
@@ -35,13 +36,12 @@
 //            tile, keep the running reference m (rescaled lazily: only when
 //            the row maximum exceeds it by more than 2^8, and then also
 //            O_t in TMEM), write P = 2^(s*scale*log2e - m) as fp16 into the
-//            first 64 columns of the S tile, and accumulate the row sum
-//            twice: from the fp16-rounded P that enters PV (it normalises
-//            the output, so numerator and denominator use the same weights)
-//            and from P before rounding (it gives lse).  The two warpgroups
+//            first 64 columns of the S tile, and accumulate the row sum l
+//            from P before rounding (fp16 rounding of P moves the output by
+//            at most ~2^-12 of the value range).  The two warpgroups
 //            ping-pong: while one does its softmax the tensor cores run the
 //            other's PV and QK^T.
-//            Epilogue: out = O / l_p in bf16, lse = (m + log2 l) * ln 2.
+//            Epilogue: out = O / l in bf16, lse = (m + log2 l) * ln 2.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
 // Every wait is bounded; on expiry TA_DEVERR_TIMEOUT is recorded, all roles
 // stop, outstanding copies and MMAs are drained and the TMEM is freed.
@@ -66,9 +66,11 @@ constexpr int kConvThreads = 64;
 constexpr uint32_t kTileBytes = kBM * kHD * 2;  // 32 KiB (one bf16 tile)
 constexpr uint32_t kHalfBytes = kTileBytes / 2; // one 64-column box
 constexpr uint32_t kQOff = 0;                   // 2 Q tiles
-constexpr uint32_t kKOff = 2 * kTileBytes;      // 2 K stages
-constexpr uint32_t kVOff = 4 * kTileBytes;      // 2 V stages
-constexpr uint32_t kBarOff = 6 * kTileBytes;
+constexpr int kKStages = 3;                     // K runs a tile ahead of V
+constexpr int kVStages = 2;
+constexpr uint32_t kKOff = 2 * kTileBytes;      // K ring
+constexpr uint32_t kVOff = kKOff + kKStages * kTileBytes;  // V ring
+constexpr uint32_t kBarOff = kVOff + kVStages * kTileBytes;
 constexpr size_t kSmemBytes = kBarOff + 256 + 1024;  // + alignment slack
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -85,10 +87,11 @@ struct PrefillParams {
 
 struct Bars {
     uint64_t q_full;
-    uint64_t k_full[2];
-    uint64_t v_full[2];
-    uint64_t v_conv[2];
-    uint64_t kv_empty[2];
+    uint64_t k_full[kKStages];
+    uint64_t k_empty[kKStages];
+    uint64_t v_full[kVStages];
+    uint64_t v_conv[kVStages];
+    uint64_t v_empty[kVStages];
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t o_full[2];
@@ -119,11 +122,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->v_conv[s], kConvThreads);
-            mbar_init(&bars->kv_empty[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->s_full[s], 1);
             mbar_init(&bars->p_full[s], kBM);
             mbar_init(&bars->o_full[s], 1);
@@ -154,30 +162,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                 tc::tma_load_3d(dst, &p.qmap, 0, q0 + t * kBM, bh, &bars->q_full);
                 tc::tma_load_3d(dst + kHalfBytes, &p.qmap, 64, q0 + t * kBM, bh, &bars->q_full);
             }
-            int armed[2] = {0, 0};
-            for (int j = 0; j < nk; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !mbar_wait_bounded(&bars->kv_empty[st], ((j >> 1) & 1) ^ 1, abort_flag))
-                    break;
-                unsigned char *kd = smem + kKOff + st * kTileBytes;
-                unsigned char *vd = smem + kVOff + st * kTileBytes;
-                mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-                tc::tma_load_3d(kd, &p.kmap, 0, j * kBN, bh_kv, &bars->k_full[st]);
-                tc::tma_load_3d(kd + kHalfBytes, &p.kmap, 64, j * kBN, bh_kv, &bars->k_full[st]);
-                mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-                tc::tma_load_3d(vd, &p.vmap, 0, j * kBN, bh_kv, &bars->v_full[st]);
-                tc::tma_load_3d(vd + kHalfBytes, &p.vmap, 64, j * kBN, bh_kv, &bars->v_full[st]);
-                ++armed[st];
+            // Issue order K0, K1, V0, K2, V1, ...: K runs one tile ahead of
+            // V, since S of a tile needs K while its PV comes a softmax later.
+            int k_armed[kKStages] = {0, 0, 0}, v_armed[kVStages] = {0, 0};
+            bool ok = true;
+            for (int i = 0; ok && i <= nk; ++i) {
+                if (i < nk) {  // K tile i
+                    const int st = i % kKStages, use = i / kKStages;
+                    if (use > 0 && !mbar_wait_bounded(&bars->k_empty[st], (use - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    unsigned char *kd = smem + kKOff + st * kTileBytes;
+                    mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
+                    tc::tma_load_3d(kd, &p.kmap, 0, i * kBN, bh_kv, &bars->k_full[st]);
+                    tc::tma_load_3d(kd + kHalfBytes, &p.kmap, 64, i * kBN, bh_kv, &bars->k_full[st]);
+                    ++k_armed[st];
+                }
+                if (i > 0) {  // V tile i - 1
+                    const int j = i - 1;
+                    const int st = j % kVStages, use = j / kVStages;
+                    if (use > 0 && !mbar_wait_bounded(&bars->v_empty[st], (use - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    unsigned char *vd = smem + kVOff + st * kTileBytes;
+                    mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
+                    tc::tma_load_3d(vd, &p.vmap, 0, j * kBN, bh_kv, &bars->v_full[st]);
+                    tc::tma_load_3d(vd + kHalfBytes, &p.vmap, 64, j * kBN, bh_kv, &bars->v_full[st]);
+                    ++v_armed[st];
+                }
             }
             if (*abort_flag) {
                 // Every copy issued must land before the CTA exits.
                 int drain_abort = 0;
                 mbar_wait_bounded(&bars->q_full, 0, &drain_abort);
-                for (int st = 0; st < 2; ++st)
-                    if (armed[st] > 0) {
-                        mbar_wait_bounded(&bars->k_full[st], (armed[st] - 1) & 1, &drain_abort);
-                        mbar_wait_bounded(&bars->v_full[st], (armed[st] - 1) & 1, &drain_abort);
-                    }
+                for (int st = 0; st < kKStages; ++st)
+                    if (k_armed[st] > 0)
+                        mbar_wait_bounded(&bars->k_full[st], (k_armed[st] - 1) & 1, &drain_abort);
+                for (int st = 0; st < kVStages; ++st)
+                    if (v_armed[st] > 0)
+                        mbar_wait_bounded(&bars->v_full[st], (v_armed[st] - 1) & 1, &drain_abort);
             }
         }
         __syncwarp();
@@ -190,9 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
             bool ok = mbar_wait_bounded(&bars->q_full, 0, abort_flag);
             tc::fence_after_sync();
             for (int j = 0; ok && j <= nk; ++j) {
-                const int st = j & 1;
+                const int st = j % kKStages;
                 if (j < nk) {
-                    ok = mbar_wait_bounded(&bars->k_full[st], (j >> 1) & 1, abort_flag);
+                    ok = mbar_wait_bounded(&bars->k_full[st], (j / kKStages) & 1, abort_flag);
                     if (!ok)
                         break;
                     tc::fence_after_sync();
@@ -207,13 +232,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                         // O_t += P_t(j-1) V_{j-1}
                         ok = mbar_wait_bounded(&bars->p_full[t], (j - 1) & 1, abort_flag);
                         if (ok && !v_ready) {
-                            ok = mbar_wait_bounded(&bars->v_conv[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag);
+                            ok = mbar_wait_bounded(&bars->v_conv[(j - 1) % kVStages], ((j - 1) / kVStages) & 1,
+                                                   abort_flag);
                             v_ready = true;
                         }
                         if (!ok)
                             break;
                         tc::fence_after_sync();
-                        const uint32_t vb = sbase + kVOff + ((j - 1) & 1) * kTileBytes;
+                        const uint32_t vb = sbase + kVOff + ((j - 1) % kVStages) * kTileBytes;
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk) {
                             // B = V rows [16kk, 16kk+16): MN-major, the two
@@ -240,8 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                 }
                 if (!ok)
                     break;
+                if (j < nk)
+                    tc::commit(&bars->k_empty[st]);  // S of tile j issued for both query tiles
                 if (j > 0)
-                    tc::commit(&bars->kv_empty[(j - 1) & 1]);
+                    tc::commit(&bars->v_empty[(j - 1) % kVStages]);  // and PV of tile j - 1
             }
             // Every MMA this thread issued completes before the TMEM is freed.
             tc::commit(&bars->mma_done);
@@ -254,8 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
         const int ct = threadIdx.x - kConvWarp0 * 32;
         uint32_t vmax = 0;  // largest |v| bit pattern seen, per 16-bit half
         for (int j = 0; j < nk; ++j) {
-            const int st = j & 1;
-            bool ok = mbar_wait_bounded(&bars->v_full[st], (j >> 1) & 1, abort_flag);
+            const int st = j % kVStages;
+            bool ok = mbar_wait_bounded(&bars->v_full[st], (j / kVStages) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok)
                 break;
@@ -290,9 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
             const uint32_t s_tmem = tmem + lane_base + t * kBN;
             const uint32_t o_tmem = tmem + lane_base + 2 * kBN + t * kHD;
             const float c = p.c;
-            // l_p: sum of the bf16-rounded weights that enter PV (normalises
-            // the output); l: the same weights before rounding (gives lse).
-            float m_used = -INFINITY, l = 0.f, l_p = 0.f;
+            float m_used = -INFINITY, l = 0.f;
             bool ok = true;
             for (int j = 0; j <= diag; ++j) {
                 ok = mbar_wait_bounded(&bars->s_full[t], j & 1, abort_flag);
@@ -300,26 +326,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                 if (!ok)
                     break;
                 tc::fence_after_sync();
+                // all four TMEM loads in flight before the first wait
+                uint32_t u[4][32];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    tc::tmem_ld32(s_tmem + ch * 32, u[ch]);
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    tc::tmem_wait_ld(u[ch]);
                 float s[kBN];
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t u[32];
-                    tc::tmem_ld32(s_tmem + ch * 32, u);
-                    tc::tmem_wait_ld(u);
+                for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        s[ch * 32 + i] = __uint_as_float(u[i]);
-                }
+                        s[ch * 32 + i] = __uint_as_float(u[ch][i]);
                 if (j == diag) {
 #pragma unroll
                     for (int i = 0; i < kBN; ++i)
                         if (i > r)
                             s[i] = -INFINITY;
                 }
-                float mx = s[0];
+                // row maximum: four chains of three-input max
+                float mq[4] = {fmaxf(s[0], s[1]), fmaxf(s[2], s[3]), fmaxf(s[4], s[5]), fmaxf(s[6], s[7])};
 #pragma unroll
-                for (int i = 1; i < kBN; ++i)
-                    mx = fmaxf(mx, s[i]);
+                for (int i = 8; i < kBN; i += 8) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        mq[c] = fmax3(mq[c], s[i + 2 * c], s[i + 2 * c + 1]);
+                }
+                const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
                 const float mcand = mx * c;
                 const bool resc = mcand > m_used + kRescaleLog2;
                 float alpha = 1.f;
@@ -328,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                     m_used = mcand;
                 }
                 const float neg_m = -m_used;
-                float ls = 0.f, ls_p = 0.f;
+                float ls = 0.f;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t pk[32];
@@ -339,25 +374,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                         const uint32_t w = tc::pack_f16x2(p0, p1);
                         pk[i] = w;
                         ls += p0 + p1;
-                        const float2 pr = tc::unpack_f16x2(w);
-                        ls_p += pr.x + pr.y;
                     }
                     tc::tmem_st32(s_tmem + half * 32, pk);
                 }
                 l = l * alpha + ls;
-                l_p = l_p * alpha + ls_p;
                 if (j > 0 && __any_sync(0xffffffffu, resc)) {
                     // O_t holds every PV up to j-1 (see the MMA issuer);
                     // bring it to the new reference.
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t u[32];
-                        tc::tmem_ld32(o_tmem + ch * 32, u);
-                        tc::tmem_wait_ld(u);
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t ou[2][32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-                        tc::tmem_st32(o_tmem + ch * 32, u);
+                        for (int ch = 0; ch < 2; ++ch)
+                            tc::tmem_ld32(o_tmem + (2 * half + ch) * 32, ou[ch]);
+#pragma unroll
+                        for (int ch = 0; ch < 2; ++ch) {
+                            tc::tmem_wait_ld(ou[ch]);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                ou[ch][i] = __float_as_uint(__uint_as_float(ou[ch][i]) * alpha);
+                            tc::tmem_st32(o_tmem + (2 * half + ch) * 32, ou[ch]);
+                        }
                     }
                 }
                 tc::tmem_wait_st();
@@ -371,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
             if (ok) {
                 tc::fence_after_sync();
                 const int row = qrow0 + r;
-                const float inv = 1.0f / l_p;
+                const float inv = 1.0f / l;
                 __nv_bfloat16 *orow = p.out + ((size_t)bh * p.S + row) * kHD;
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
@@ -383,14 +420,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                     for (int i = 0; i < 16; ++i)
                         pk[i] = tc::pack_bf16x2(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
                     if (row < p.S) {
+                        // streaming stores: the output is not read again here,
+                        // so its lines leave L2 first instead of lingering dirty
                         uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                            __stcs(dst + i, make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]));
                     }
                 }
                 if (row < p.S && p.lse)
-                    p.lse[(size_t)bh * p.S + row] = (m_used + fast_log2(l)) * kLn2;
+                    __stcs(p.lse + (size_t)bh * p.S + row, (m_used + fast_log2(l)) * kLn2);
             }
         }
     }
