@@ -37,7 +37,10 @@ if ROOT not in sys.path:
 
 DECODE_WORKLOAD = "gqa_32x8_d128_s131072"
 PREFILL_WORKLOAD = "causal_prefill_32x8_d128_s16384"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_split_kernel_gqa_32x8_d128_s131072.md")
+PROFILES = {  # committed ncu summaries: (file, kernel source they were taken on)
+    "decode": ("decode_split_kernel_gqa_32x8_d128_s131072.md", "decode.cu"),
+    "prefill": ("prefill_causal_kernel_causal_prefill_32x8_d128_s16384.md", "prefill.cu"),
+}
 
 
 def dist_env():
@@ -113,11 +116,12 @@ def source_hash(path):
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if
-    the kernel source is unchanged since that capture; else None."""
+def profiled_traffic(which):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, if the
+    kernel source is unchanged since that capture; else None."""
+    name, src_name = PROFILES[which]
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
         return None
     kv = {}
@@ -125,8 +129,8 @@ def profiled_traffic():
         if ":" in line and line.startswith("- "):
             key, _, val = line[2:].partition(":")
             kv[key.strip()] = val.strip().strip("`")
-    src = os.path.join(ROOT, "long_context_decode_04_b300", "csrc", "decode.cu")
-    if kv.get("decode.cu sha256") != source_hash(src):
+    src = os.path.join(ROOT, "long_context_decode_04_b300", "csrc", src_name)
+    if kv.get(f"{src_name} sha256") != source_hash(src):
         return None
     try:
         return int(kv["dram bytes per launch"])
@@ -316,6 +320,17 @@ def main():
     pre_total = max_over_ranks(pre_total)
     dec_avg = dec_total / len(dec_ms)
 
+    # ---------------- context: decode replays back to back, no prefill between
+    # (a decode that follows a prefill also writes back the prefill's dirty
+    # output lines from L2)
+    alone = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for a, b_ in alone:
+        a.record(stream)
+        graphs[0].replay()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    alone_us = sorted(1e3 * a.elapsed_time(b_) for a, b_ in alone)[len(alone) // 2]
+
     # ---------------- end to end through the public single call, host buffers
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
     hq = x["q"].pin_memory()
@@ -391,10 +406,14 @@ def main():
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "us_per_token": round(1e3 * dec_avg, 3),
+        "decode_alone": {"us_per_token": round(alone_us, 3),
+                         "gbs": round(kv_bytes / (alone_us / 1e6) / 1e9, 1),
+                         "frac": round(kv_bytes / (alone_us / 1e6) / 1e9 / peaks["hbm_gbs"], 4),
+                         "note": "median of 50 decode replays back to back, after the timed region"},
         "decode_hbm_frac": round(value / world / peaks["hbm_gbs"], 4),
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": kv_bytes,
+                     "traffic": profiled_traffic("decode"), "algorithmic_bytes_per_launch": kv_bytes,
                      "peak_source": peaks["source"] + " (copy bandwidth)",
                      "avg_launch_us": round(1e3 * dec_avg, 3), "launches_per_token": decode_launches},
         "gpu_launches": launches_per_step * args.steps,
@@ -413,7 +432,9 @@ def main():
                                     "achieved": round(tflops / world, 2), "peak": peaks["bf16_tflops_sustained"],
                                     "unit": "TFLOP/s",
                                     "frac": round(tflops / world / peaks["bf16_tflops_sustained"], 4),
-                                    "traffic": None, "peak_source": peaks["source"] + " (sustained)",
+                                    "traffic": profiled_traffic("prefill"),
+                                    "frac_of_burst_peak": round(tflops / world / peaks["bf16_tflops"], 4),
+                                    "peak_source": peaks["source"] + " (sustained)",
                                     "avg_launch_us": round(1e3 * pre_total / args.steps, 2)}
     print(json.dumps(line), flush=True)
     if world > 1:
