@@ -138,6 +138,24 @@ def profiled_traffic(which):
         return None
 
 
+def reduce_max(val, world, device):
+    """The largest of the ranks' values (every rank gets it); the job's time is
+    its slowest replica's."""
+    if world == 1:
+        return val
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([val], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank, world, seconds_max):
+    """Whole-job throughput of `world` independent replicas (weak scaling):
+    every rank processes units_per_rank in at most seconds_max."""
+    return world * units_per_rank / seconds_max
+
+
 def cpu_oracle_decode(x, rows, threads):
     import oracle
     t = time.perf_counter()
@@ -309,11 +327,7 @@ def main():
     pre_total = sum(pre_ms)
 
     def max_over_ranks(val):
-        if world == 1:
-            return val
-        t = torch.tensor([val], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(val, world, dev)
 
     total_ms = max_over_ranks(total_ms)
     dec_total = max_over_ranks(dec_total)
@@ -378,7 +392,7 @@ def main():
                "sample": "one full decode step: all 32 query heads over all 131072 keys (512 MiB of K/V)"}
 
     dec_s = dec_total / 1e3
-    value = world * kv_bytes * args.steps / dec_s / 1e9
+    value = replica_throughput(kv_bytes * args.steps, world, dec_s) / 1e9
     achieved = kv_bytes / (dec_avg / 1e3) / 1e9
     line = {
         "metric": "decode KV-cache GB/s (% of B300 HBM peak) and us/token at S=131072; prefill TFLOP/s",
