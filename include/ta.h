@@ -63,7 +63,8 @@ typedef enum { TA_F32 = 0, TA_BF16 = 1 } ta_dtype;
 enum {
     TA_DEVERR_SEQLEN = 1,   /* some seqlens[b] < 0 or > S; clamped to [0, S]     */
     TA_DEVERR_TIMEOUT = 2,  /* a pipeline wait exceeded its time limit; output invalid */
-    TA_DEVERR_RANGE = 4     /* prefill: some |V| > 65280 (outside fp16); output undefined */
+    TA_DEVERR_RANGE = 4,    /* prefill: some |V| > 65280 (outside fp16); output undefined */
+    TA_DEVERR_PAGE = 8      /* paged decode: a block-table entry outside [0, num_pages); output undefined */
 };
 
 /*
@@ -166,6 +167,49 @@ ta_status ta_decode_noalloc(const void *q, const void *k, const void *v, void *o
 
 /* Split-KV decode with every option of ta_decode_params. */
 ta_status ta_decode_ex(const ta_decode_params *p);
+
+/*
+ * Split-KV decode over a paged KV cache (block table).  The step beside the
+ * variable-length batch: the KV cache is a pool of fixed-size pages and each
+ * sequence lists its pages, so sequences grow without copying (Attention
+ * glossary, jisaku.com/glossary/attention, "the memory bandwidth and VRAM
+ * wall": the KV cache dominates decode memory).  Same result as ta_decode_ex
+ * on the gathered contiguous cache.
+ *   k_pages, v_pages [num_pages, Hkv, page_size, D] (head-major inside a
+ *     page, so one head's rows of a page are contiguous), in_dtype;
+ *   block_table [B, pages_per_seq] int32 on the device: key j of sequence b
+ *     is row j % page_size of page block_table[b][j / page_size];
+ *   seqlens [B] int32 on the device, required; 0 <= seqlens[b] <=
+ *     pages_per_seq * page_size (else clamped, TA_DEVERR_SEQLEN).  Entries
+ *     beyond a sequence's last page are never read.  A page id outside
+ *     [0, num_pages) is not followed: TA_DEVERR_PAGE is recorded and the
+ *     output is undefined.
+ *   q, out, lse, dtypes, chunk / n_split and workspace as in
+ *   ta_decode_params, with S = pages_per_seq * page_size (the plan and
+ *   workspace are those of ta_decode_plan_for(B, Hq, Hkv, S, D, chunk,
+ *   n_split, 1, 0, ...)).  k_pages, v_pages 16-byte aligned.
+ */
+typedef struct {
+    const void *q;
+    const void *k_pages;
+    const void *v_pages;
+    const int32_t *block_table;
+    const int32_t *seqlens;
+    void *out;
+    float *lse;
+    int32_t B, Hq, Hkv, D;
+    int32_t page_size, pages_per_seq, num_pages;
+    float scale;
+    ta_dtype in_dtype;
+    ta_dtype out_dtype;
+    int32_t chunk;
+    int32_t n_split;
+    void *workspace;
+    size_t workspace_bytes;
+    void *stream;
+} ta_paged_decode_params;
+
+ta_status ta_decode_paged(const ta_paged_decode_params *p);
 
 /*
  * The split phase alone: every (sequence b, query head h, chunk c) partial

@@ -2,6 +2,7 @@
 // dispatch to the scheduler and the kernels.  Nothing here computes
 // attention; every arithmetic step runs in the CUDA kernels.
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -181,11 +182,16 @@ size_t ta_decode_workspace_bytes(int B, int Hq, int Hkv, int S, int D, int chunk
     return plan.workspace_bytes;
 }
 
-ta_status ta_decode_ex(const ta_decode_params *p)
+}  // extern "C"
+
+namespace {
+
+// The decode of ta_decode_ex, reading K/V through a block table when one is
+// given (block_table != nullptr; p->k, p->v are then the page pools).
+ta_status decode_impl(const ta_decode_params *p, const int32_t *block_table, int page_size, int pages_per_seq,
+                      int num_pages)
 {
-    ta_status s = validate_decode(p);
-    if (s != TA_OK)
-        return s;
+    ta_status s;
     ta_decode_plan plan;
     s = ta_decode_plan_for(p->B, p->Hq, p->Hkv, p->S, p->D, p->chunk, p->n_split, p->seqlens != nullptr, 0, &plan);
     if (s != TA_OK)
@@ -204,6 +210,10 @@ ta_status ta_decode_ex(const ta_decode_params *p)
     }
     ta::DecodeLaunch a;
     a.force_partials = false;
+    a.block_table = block_table;
+    a.page_size = page_size;
+    a.pages_per_seq = pages_per_seq;
+    a.num_pages = num_pages;
     a.q = p->q;
     a.k = p->k;
     a.v = p->v;
@@ -247,6 +257,59 @@ ta_status ta_decode_ex(const ta_decode_params *p)
             return cuda_fail(e, "combine kernel launch");
     }
     return TA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ta_status ta_decode_ex(const ta_decode_params *p)
+{
+    ta_status s = validate_decode(p);
+    if (s != TA_OK)
+        return s;
+    return decode_impl(p, nullptr, 0, 0, 0);
+}
+
+ta_status ta_decode_paged(const ta_paged_decode_params *pp)
+{
+    if (!pp)
+        return fail(TA_ERR_INVALID_ARG, "params pointer is NULL");
+    if (!pp->block_table || !pp->seqlens)
+        return fail(TA_ERR_INVALID_ARG, "block_table and seqlens must be non-NULL");
+    if (pp->page_size < 1 || pp->pages_per_seq < 1 || pp->num_pages < 1)
+        return fail(TA_ERR_INVALID_ARG, "page_size, pages_per_seq and num_pages must all be >= 1");
+    if ((int64_t)pp->page_size * pp->pages_per_seq > INT32_MAX)
+        return fail(TA_ERR_INVALID_ARG, "page_size * pages_per_seq overflows");
+    if (!aligned(pp->block_table, 4))
+        return fail(TA_ERR_INVALID_ARG, "block_table must be 4-byte aligned");
+    if ((double)pp->num_pages * pp->Hkv * pp->page_size * pp->D > 9.0e18 / 4)
+        return fail(TA_ERR_INVALID_ARG, "page pool size overflows");
+    ta_decode_params p;
+    std::memset(&p, 0, sizeof p);
+    p.q = pp->q;
+    p.k = pp->k_pages;
+    p.v = pp->v_pages;
+    p.out = pp->out;
+    p.lse = pp->lse;
+    p.B = pp->B;
+    p.Hq = pp->Hq;
+    p.Hkv = pp->Hkv;
+    p.S = pp->page_size * pp->pages_per_seq;
+    p.D = pp->D;
+    p.scale = pp->scale;
+    p.seqlens = pp->seqlens;
+    p.in_dtype = pp->in_dtype;
+    p.out_dtype = pp->out_dtype;
+    p.chunk = pp->chunk;
+    p.n_split = pp->n_split;
+    p.workspace = pp->workspace;
+    p.workspace_bytes = pp->workspace_bytes;
+    p.stream = pp->stream;
+    ta_status s = validate_decode(&p);
+    if (s != TA_OK)
+        return s;
+    return decode_impl(&p, pp->block_table, pp->page_size, pp->pages_per_seq, pp->num_pages);
 }
 
 ta_status ta_decode_partials(const ta_decode_params *p, float *m, float *l, float *o)
@@ -295,6 +358,8 @@ ta_status ta_decode_partials(const ta_decode_params *p, float *m, float *l, floa
     a.plan = plan;
     a.plan.n_split = plan.n_split;
     a.force_partials = true;
+    a.block_table = nullptr;
+    a.page_size = a.pages_per_seq = a.num_pages = 0;
     a.stream = static_cast<cudaStream_t>(p->stream);
     a.status = static_cast<int32_t *>(ws);
     a.counters = nullptr;

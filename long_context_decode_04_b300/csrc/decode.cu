@@ -89,6 +89,11 @@ struct DecodeParams {
     int32_t *status;    // [0] flags, [16] work-queue counter
     int32_t *counters;  // [B * Hkv] finished chunks per unit (fused mode)
     float *part_m, *part_l, *part_o;
+    // Paged KV cache (block_table != nullptr): k, v are [num_pages, Hkv,
+    // page_size, D] and key j of sequence b lives in page
+    // block_table[b * pages_per_seq + j / page_size] at row j % page_size.
+    const int32_t *block_table;
+    int page_size, pages_per_seq, num_pages;
 };
 
 template <typename T>
@@ -336,11 +341,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
                 }
                 desc[stage] = TileDesc{item, j0, n, flags};
                 unsigned char *dst = smem + stage * C::STAGE;
-                if (n > 0) {
+                if (n > 0 && !p.block_table) {
                     const uint32_t bytes = (uint32_t)n * C::RB;
                     mbar_arrive_expect_tx(&full[stage], 2 * bytes);
                     bulk_copy_g2s_hint(dst, kbase + (size_t)j0 * D, bytes, &full[stage], policy);
                     bulk_copy_g2s_hint(dst + C::KV_OFF, vbase + (size_t)j0 * D, bytes, &full[stage], policy);
+                } else if (n > 0) {
+                    // paged: one copy per page segment of the tile
+                    mbar_arrive_expect_tx(&full[stage], 2 * (uint32_t)n * C::RB);
+                    const int kvh = unit - b * p.Hkv;
+                    const int32_t *bt = p.block_table + (size_t)b * p.pages_per_seq;
+                    for (int j = j0; j < j0 + n;) {
+                        const int pg = j / p.page_size;
+                        const int off = j - pg * p.page_size;
+                        const int cnt = min(p.page_size - off, j0 + n - j);
+                        int page = bt[pg];
+                        if (page < 0 || page >= p.num_pages) {
+                            atomicOr(&p.status[0], TA_DEVERR_PAGE);
+                            page = 0;  // stay in bounds; the output is flagged invalid
+                        }
+                        const size_t row = ((size_t)page * p.Hkv + kvh) * p.page_size + off;
+                        const uint32_t bytes = (uint32_t)cnt * C::RB;
+                        const uint32_t so = (uint32_t)(j - j0) * C::RB;
+                        bulk_copy_g2s_hint(dst + so, static_cast<const KV *>(p.k) + row * D, bytes, &full[stage],
+                                           policy);
+                        bulk_copy_g2s_hint(dst + C::KV_OFF + so, static_cast<const KV *>(p.v) + row * D, bytes,
+                                           &full[stage], policy);
+                        j += cnt;
+                    }
                 } else {
                     mbar_arrive(&full[stage]);
                 }
@@ -758,6 +786,10 @@ cudaError_t launch_decode(const DecodeLaunch &a)
     p.part_m = a.part_m;
     p.part_l = a.part_l;
     p.part_o = a.part_o;
+    p.block_table = a.block_table;
+    p.page_size = a.page_size;
+    p.pages_per_seq = a.pages_per_seq;
+    p.num_pages = a.num_pages;
     const int G = a.Hq / a.Hkv;
     if (a.D == 128) {
         switch (G) {

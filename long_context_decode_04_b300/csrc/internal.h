@@ -36,6 +36,8 @@ struct DecodeLaunch {
     int32_t *counters;     // [B * Hkv] finished chunks per unit, zero between launches
     float *part_m, *part_l, *part_o;   // [R, n_split], [R, n_split], [R, n_split, D]
     bool force_partials;               // write partials even when n_split == 1
+    const int32_t *block_table;        // paged KV cache, or nullptr (contiguous [B, Hkv, S, D])
+    int page_size, pages_per_seq, num_pages;
     cudaStream_t stream;
 };
 

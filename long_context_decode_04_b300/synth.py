@@ -32,7 +32,7 @@ import torch
 
 BLOCK = 1 << 24  # elements per independently seeded block
 
-_TAGS = {"q": 1, "k": 2, "v": 3, "seqlens": 4, "peak_rows": 5}
+_TAGS = {"q": 1, "k": 2, "v": 3, "seqlens": 4, "peak_rows": 5, "pages": 6}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -159,3 +159,43 @@ def make_inputs(w: Workload, *, seed: int | None = None, S: int | None = None,
             k[b, :, int(seqlens[b]):, :] = pad_value
             v[b, :, int(seqlens[b]):, :] = pad_value
     return {"q": q, "k": k, "v": v, "seqlens": seqlens, "scale": w.scale}
+
+
+def to_pages(k: torch.Tensor, v: torch.Tensor, seqlens, page_size: int, *, seed: int = 7,
+             extra_pages: int = 3, pad_value: float | None = None):
+    """Scatter contiguous K/V [B, Hkv, S, D] into a shuffled page pool.
+
+    Returns (k_pages, v_pages [num_pages, Hkv, page_size, D], block_table
+    [B, pages_per_seq] int32).  Sequence b's key j goes to row j % page_size
+    of page block_table[b, j // page_size]; physical pages are a seeded
+    permutation, ``extra_pages`` pages belong to no sequence, and block-table
+    slots past a sequence's last page point at one of them.  ``pad_value``
+    (e.g. NaN) fills every pool row that holds no attended key, so a kernel
+    reading one shows it.  Pure data movement: no attention arithmetic.
+    """
+    B, Hkv, S, D = k.shape
+    lens = [S] * B if seqlens is None else [int(x) for x in seqlens]
+    pages_per_seq = (S + page_size - 1) // page_size
+    used = [(L + page_size - 1) // page_size for L in lens]
+    num_pages = sum(used) + extra_pages
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, _TAGS["pages"], page_size])))
+    perm = rng.permutation(num_pages)
+    fill = 0.0 if pad_value is None else pad_value
+    kp = torch.full((num_pages, Hkv, page_size, D), fill, dtype=k.dtype)
+    vp = torch.full((num_pages, Hkv, page_size, D), fill, dtype=v.dtype)
+    spare = [int(x) for x in perm[sum(used):]] or [int(perm[0])]
+    table = torch.empty((B, pages_per_seq), dtype=torch.int32)
+    nxt = 0
+    for b in range(B):
+        for pg in range(pages_per_seq):
+            if pg < used[b]:
+                phys = int(perm[nxt])
+                nxt += 1
+                j0 = pg * page_size
+                n = min(page_size, lens[b] - j0)
+                kp[phys, :, :n] = k[b, :, j0:j0 + n]
+                vp[phys, :, :n] = v[b, :, j0:j0 + n]
+            else:
+                phys = spare[pg % len(spare)]
+            table[b, pg] = phys
+    return kp, vp, table

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(HERE, "libta.so")
 
 TA_OK, TA_ERR_INVALID_ARG, TA_ERR_UNSUPPORTED, TA_ERR_WORKSPACE, TA_ERR_CUDA = range(5)
 TA_F32, TA_BF16 = 0, 1
-TA_DEVERR_SEQLEN, TA_DEVERR_TIMEOUT, TA_DEVERR_RANGE = 1, 2, 4
+TA_DEVERR_SEQLEN, TA_DEVERR_TIMEOUT, TA_DEVERR_RANGE, TA_DEVERR_PAGE = 1, 2, 4, 8
 STATUS_NAMES = {0: "TA_OK", 1: "TA_ERR_INVALID_ARG", 2: "TA_ERR_UNSUPPORTED", 3: "TA_ERR_WORKSPACE",
                 4: "TA_ERR_CUDA"}
 
@@ -47,6 +47,18 @@ class DecodeParams(ctypes.Structure):
                 ("stream", ctypes.c_void_p)]
 
 
+class PagedDecodeParams(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k_pages", ctypes.c_void_p), ("v_pages", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("seqlens", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("pages_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("chunk", ctypes.c_int32), ("n_split", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("stream", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -61,6 +73,7 @@ def lib() -> ctypes.CDLL:
         L.ta_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
         L.ta_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
         L.ta_decode_ex.argtypes = [ctypes.POINTER(DecodeParams)]
+        L.ta_decode_paged.argtypes = [ctypes.POINTER(PagedDecodeParams)]
         L.ta_decode_partials.argtypes = [ctypes.POINTER(DecodeParams), vp, vp, vp]
         L.ta_decode_plan_for.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.POINTER(DecodePlan)]
         L.ta_decode_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
@@ -72,7 +85,7 @@ def lib() -> ctypes.CDLL:
         L.ta_prefill_causal.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         L.ta_last_error.argtypes = []
         L.ta_last_error.restype = ctypes.c_char_p
-        for fn in ("ta_decode", "ta_decode_noalloc", "ta_decode_ex", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
+        for fn in ("ta_decode", "ta_decode_noalloc", "ta_decode_ex", "ta_decode_paged", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
                    "ta_prefill_causal"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
@@ -143,6 +156,40 @@ def decode(q, k, v, *, seqlens=None, scale=None, out_dtype=None, chunk=0, n_spli
         p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     p.stream = torch.cuda.current_stream(q.device).cuda_stream
     _check(lib().ta_decode_ex(ctypes.byref(p)))
+    return out, lse
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens, *, scale=None, out_dtype=None, chunk=0, n_split=0,
+                 workspace=None, out=None, lse=None):
+    """Split-KV decode over a paged KV cache.
+
+    q [B,Hq,D]; k_pages/v_pages [num_pages,Hkv,page_size,D]; block_table
+    [B,pages_per_seq] int32; seqlens [B] int32 (all CUDA).  Returns
+    (out [B,Hq,D], lse [B,Hq] fp32).
+    """
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    pages_per_seq = block_table.shape[1]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    p = PagedDecodeParams()
+    p.q, p.k_pages, p.v_pages = q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr()
+    p.block_table, p.seqlens = block_table.data_ptr(), seqlens.data_ptr()
+    p.out, p.lse = out.data_ptr(), lse.data_ptr()
+    p.B, p.Hq, p.Hkv, p.D = B, Hq, Hkv, D
+    p.page_size, p.pages_per_seq, p.num_pages = page_size, pages_per_seq, num_pages
+    p.scale = scale
+    p.in_dtype = _dtype_code(q.dtype)
+    p.out_dtype = _dtype_code(out.dtype)
+    p.chunk, p.n_split = chunk, n_split
+    if workspace is not None:
+        p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    p.stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(lib().ta_decode_paged(ctypes.byref(p)))
     return out, lse
 
 

@@ -145,3 +145,26 @@ def combine(m, l, o):
     rc = lib().oracle_combine(_ptr(m), _ptr(l), _ptr(o), R, N, D, _ptr(out), _ptr(lse))
     _check(rc, "combine")
     return out, lse
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens, scale, rows=None, threads=None):
+    """Decode over a paged KV cache: sequence b's key j is row j % page_size of
+    page block_table[b, j // page_size] of the [num_pages, Hkv, page_size, D]
+    pools.  The definition is unchanged (attention over keys [0, L_b) of each
+    sequence); the pages are gathered into the contiguous cache first with
+    numpy indexing (a library gather) and ``decode`` does the rest."""
+    kp, kt = _raw(k_pages)
+    vp, vt = _raw(v_pages)
+    table = np.asarray(block_table, dtype=np.int64)
+    lens = np.asarray(seqlens, dtype=np.int64)
+    B, P = table.shape
+    _, Hkv, page, D = kp.shape
+    S = P * page
+    kc = np.zeros((B, Hkv, S, D), dtype=kp.dtype)
+    vc = np.zeros((B, Hkv, S, D), dtype=vp.dtype)
+    for b in range(B):
+        npg = (int(lens[b]) + page - 1) // page
+        for pg in range(npg):
+            kc[b, :, pg * page:(pg + 1) * page] = kp[table[b, pg]]
+            vc[b, :, pg * page:(pg + 1) * page] = vp[table[b, pg]]
+    return decode(q, kc, vc, scale, seqlens=lens.astype(np.int32), rows=rows, threads=threads)

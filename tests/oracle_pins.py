@@ -400,4 +400,67 @@ def pin_row_subset_matches_all_rows():
     assert np.array_equal(o2, out[rows]) and np.array_equal(l2, lse[rows])
 
 
+# ------------------------------------------------------------ paged KV cache
+
+def _paged_case(rng, B, Hkv, G, page, lens, D=4, extra=2):
+    """A shuffled page pool built with explicit loops (independent of the
+    oracle's numpy gather): returns q, pools, table, and the key rows of each
+    sequence listed as (page, row) pairs."""
+    P = max((L + page - 1) // page for L in lens)
+    used = [(L + page - 1) // page for L in lens]
+    n_pages = sum(used) + extra
+    perm = rng.permutation(n_pages)
+    kp = (rng.standard_normal((n_pages, Hkv, page, D)) * 1.3).astype(np.float32)
+    vp = rng.standard_normal((n_pages, Hkv, page, D)).astype(np.float32)
+    table = np.zeros((B, P), dtype=np.int32)
+    where = []
+    nxt = 0
+    for b in range(B):
+        rows = []
+        for pg in range(P):
+            if pg < used[b]:
+                table[b, pg] = perm[nxt]
+                nxt += 1
+            else:
+                table[b, pg] = perm[-1]  # a page of no sequence: never read
+        for j in range(lens[b]):
+            rows.append((int(table[b, j // page]), j % page))
+        where.append(rows)
+    q = rng.standard_normal((B, Hkv * G, D)).astype(np.float32)
+    return q, kp, vp, table, where
+
+
+def pin_paged_brute_force():
+    """Paged decode against 50-digit attention over the keys listed page by
+    page with plain loops."""
+    rng = _rng(41)
+    for page in (1, 3, 4):
+        lens = [5, 1, 7]
+        q, kp, vp, table, where = _paged_case(rng, 3, 2, 2, page, lens)
+        out, lse = oracle.decode_paged(q, kp, vp, table, lens, 0.7)
+        for b in range(3):
+            for h in range(4):
+                kv = h // 2
+                ks = np.array([kp[pg, kv, r] for pg, r in where[b]])
+                vs = np.array([vp[pg, kv, r] for pg, r in where[b]])
+                ref, ref_lse = _mp_attend(q[b, h], ks, vs, 0.7)
+                assert np.max(np.abs(out[b * 4 + h] - np.array(ref))) < 1e-13, (page, b, h)
+                assert abs(lse[b * 4 + h] - ref_lse) < 1e-13
+
+
+def pin_paged_page_permutation():
+    """Relabelling the physical pages (and the table with them) changes
+    nothing; pages of no sequence may hold anything."""
+    rng = _rng(42)
+    lens = [23, 9, 16]
+    q, kp, vp, table, _ = _paged_case(rng, 3, 2, 2, 4, lens)
+    a = oracle.decode_paged(q, kp, vp, table, lens, 0.5)
+    perm = rng.permutation(kp.shape[0])
+    inv = np.argsort(perm)
+    kp2, vp2 = kp[perm], vp[perm]
+    table2 = inv[table].astype(np.int32)
+    b_ = oracle.decode_paged(q, kp2, vp2, table2, lens, 0.5)
+    assert np.array_equal(a[0], b_[0]) and np.array_equal(a[1], b_[1])
+
+
 ALL_PINS = [f for name, f in sorted(globals().items()) if name.startswith("pin_") and callable(f)]

@@ -134,3 +134,25 @@ def test_valid_call_without_gpu_reports_cuda_error():
                         scale=0.1, in_dtype=ta.TA_BF16, out_dtype=ta.TA_BF16)
     assert ta.lib().ta_decode_ex(ctypes.byref(p)) == ta.TA_ERR_CUDA
     assert b"cuda" in ta.lib().ta_last_error().lower()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(block_table=None), ta.TA_ERR_INVALID_ARG),
+    (dict(seqlens=None), ta.TA_ERR_INVALID_ARG),
+    (dict(page_size=0), ta.TA_ERR_INVALID_ARG),
+    (dict(pages_per_seq=0), ta.TA_ERR_INVALID_ARG),
+    (dict(num_pages=0), ta.TA_ERR_INVALID_ARG),
+    (dict(block_table=0x6002), ta.TA_ERR_INVALID_ARG),
+    (dict(k_pages=0x2008), ta.TA_ERR_INVALID_ARG),
+    (dict(D=96), ta.TA_ERR_UNSUPPORTED),
+    (dict(Hq=6, Hkv=4), ta.TA_ERR_INVALID_ARG),
+])
+def test_paged_decode_rejects_bad_arguments_before_launch(kw, status):
+    base = dict(q=0x1000, k_pages=0x2000, v_pages=0x3000, block_table=0x6000, seqlens=0x7000, out=0x4000,
+                lse=0x5000, B=2, Hq=8, Hkv=2, D=128, page_size=16, pages_per_seq=4, num_pages=8, scale=0.1,
+                in_dtype=ta.TA_BF16, out_dtype=ta.TA_BF16, chunk=0, n_split=0, workspace=None,
+                workspace_bytes=0, stream=None)
+    base.update(kw)
+    p = ta.PagedDecodeParams(**base)
+    assert ta.lib().ta_decode_paged(ctypes.byref(p)) == status
+    assert len(ta.lib().ta_last_error()) > 0

@@ -83,3 +83,34 @@ def test_mutation_is_caught(tmp_path, monkeypatch, name):
         except (AssertionError, ValueError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught mutation {name}"
+
+
+# Mistakes planted in the paged oracle (a Python function): the mutated source
+# is compiled into a copy of the function, swapped in, and every pin is run.
+PY_MUTATIONS = {
+    "page_rows_offset": ("kc[b, :, pg * page:(pg + 1) * page] = kp[table[b, pg]]",
+                         "kc[b, :, pg * page:(pg + 1) * page] = kp[table[b, max(pg - 1, 0)]]"),
+    "table_transposed": ("kp[table[b, pg]]", "kp[table[pg % B, b % P]]"),
+    "last_page_dropped": ("npg = (int(lens[b]) + page - 1) // page", "npg = int(lens[b]) // page"),
+    "v_from_k_pages": ("vc[b, :, pg * page:(pg + 1) * page] = vp[table[b, pg]]",
+                       "vc[b, :, pg * page:(pg + 1) * page] = kp[table[b, pg]]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTATIONS))
+def test_paged_mutation_is_caught(monkeypatch, name):
+    import inspect
+    import textwrap
+    old, new = PY_MUTATIONS[name]
+    src = textwrap.dedent(inspect.getsource(oracle.decode_paged))
+    assert src.count(old) >= 1, f"mutation {name}: pattern not found"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, "decode_paged", ns["decode_paged"])
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutation {name}"
