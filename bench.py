@@ -156,6 +156,48 @@ def replica_throughput(units_per_rank, world, seconds_max):
     return world * units_per_rank / seconds_max
 
 
+def measure_varlen(ta, synth, accounting, peaks, dev, reps=20):
+    """Decode of the 16-sequence variable-length workload (lengths 1K-32K),
+    with a contiguous and a paged (64-key pages) KV cache: median of `reps`
+    graph replays each, KV bytes of the attended keys only."""
+    import torch
+    w = synth.WORKLOADS["varlen_b16_32x8_d128_s1k_32k"]
+    x = synth.make_inputs(w)
+    lens = [int(v) for v in x["seqlens"]]
+    kv_bytes = accounting.decode_kv_bytes(w.B, w.Hkv, w.D, lens, 2)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    sl = x["seqlens"].to(dev)
+    kp, vp, bt = synth.to_pages(x["k"], x["v"], lens, 64, seed=11)
+    kp, vp, bt = kp.to(dev), vp.to(dev), bt.to(dev)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    ws = ta.decode_workspace(w.B, w.Hq, w.Hkv, w.S, w.D, varlen=True, device=dev)
+    calls = {
+        "contiguous": lambda: ta.decode(q, k, v, seqlens=sl, scale=w.scale, workspace=ws, out=out, lse=lse),
+        "paged_64": lambda: ta.decode_paged(q, kp, vp, bt, sl, scale=w.scale, workspace=ws, out=out, lse=lse),
+    }
+    res = {"workload": "B=16, Hq=32, Hkv=8, D=128, lengths uniform in [1024, 32768] (seeded), bf16",
+           "attended_kv_bytes": kv_bytes}
+    stream = torch.cuda.current_stream(dev)
+    for name, fn in calls.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = sorted(1e3 * a.elapsed_time(b) for a, b in ev)[reps // 2]
+        gbs = kv_bytes / (us / 1e6) / 1e9
+        res[name] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    return res
+
+
 def cpu_oracle_decode(x, rows, threads):
     import oracle
     t = time.perf_counter()
@@ -201,6 +243,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="time the decode path only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-extra", action="store_true", help="skip the variable-length / paged decode figures")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_env()
@@ -345,6 +388,9 @@ def main():
     torch.cuda.synchronize()
     alone_us = sorted(1e3 * a.elapsed_time(b_) for a, b_ in alone)[len(alone) // 2]
 
+    # ---------------- the step beside config 3: variable lengths, contiguous and paged
+    extra = None if args.no_extra else measure_varlen(ta, synth, accounting, peaks, dev)
+
     # ---------------- end to end through the public single call, host buffers
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
     hq = x["q"].pin_memory()
@@ -430,6 +476,7 @@ def main():
                      "traffic": profiled_traffic("decode"), "algorithmic_bytes_per_launch": kv_bytes,
                      "peak_source": peaks["source"] + " (copy bandwidth)",
                      "avg_launch_us": round(1e3 * dec_avg, 3), "launches_per_token": decode_launches},
+        "varlen_b16": extra,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "e2e": {"value": round(world * kv_bytes * e2e_steps / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
