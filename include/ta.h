@@ -169,6 +169,26 @@ ta_status ta_decode_noalloc(const void *q, const void *k, const void *v, void *o
 ta_status ta_decode_ex(const ta_decode_params *p);
 
 /*
+ * Split-KV decode over the key set of pi-Attention (pi-Attention explainer,
+ * gist.science/ja/paper/2511.10696, technical summary section 2A): the
+ * query of each sequence, the newest token i = L_b - 1, attends
+ *   the ring-local window  { j : max(0, i - window) <= j <= i }  and
+ *   the periodic skips     { j = i - m * period : m >= 1, 0 <= j < i - window },
+ * in one softmax (causal: past keys only).  The learned fusion gate of that
+ * page is not applied (it needs trained weights): every attended key has
+ * its plain score.  period = 1 attends every key (= ta_decode_ex).
+ *   Arguments as ta_decode_ex (K/V contiguous [B, Hkv, S, D]); window >= 0,
+ *   period >= 1.  The chunks cut the ascending list of attended keys: a
+ *   caller workspace needs ta_decode_pi_workspace_bytes(...) bytes.
+ */
+ta_status ta_decode_pi(const ta_decode_params *p, int window, int period);
+
+/* Workspace bytes of ta_decode_pi (0 on bad arguments); arguments as
+ * ta_decode_workspace_bytes plus window and period. */
+size_t ta_decode_pi_workspace_bytes(int B, int Hq, int Hkv, int S, int D, int chunk, int n_split, int varlen,
+                                    int window, int period);
+
+/*
  * Split-KV decode over a paged KV cache (block table).  The step beside the
  * variable-length batch: the KV cache is a pool of fixed-size pages and each
  * sequence lists its pages, so sequences grow without copying (Attention

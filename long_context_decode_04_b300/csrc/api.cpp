@@ -189,11 +189,15 @@ namespace {
 // The decode of ta_decode_ex, reading K/V through a block table when one is
 // given (block_table != nullptr; p->k, p->v are then the page pools).
 ta_status decode_impl(const ta_decode_params *p, const int32_t *block_table, int page_size, int pages_per_seq,
-                      int num_pages)
+                      int num_pages, int pi_window = 0, int pi_period = 0)
 {
     ta_status s;
     ta_decode_plan plan;
-    s = ta_decode_plan_for(p->B, p->Hq, p->Hkv, p->S, p->D, p->chunk, p->n_split, p->seqlens != nullptr, 0, &plan);
+    // the chunks cut the list of attended keys: all S of them, or the
+    // pi-Attention set's at most pi_max_keys
+    const int S_list = pi_period > 0 ? (int)ta::pi_max_keys(p->S, pi_window, pi_period) : p->S;
+    s = ta_decode_plan_for(p->B, p->Hq, p->Hkv, S_list, p->D, p->chunk, p->n_split, p->seqlens != nullptr, 0,
+                           &plan);
     if (s != TA_OK)
         return s;
     void *ws = p->workspace;
@@ -214,6 +218,8 @@ ta_status decode_impl(const ta_decode_params *p, const int32_t *block_table, int
     a.page_size = page_size;
     a.pages_per_seq = pages_per_seq;
     a.num_pages = num_pages;
+    a.pi_window = pi_window;
+    a.pi_period = pi_period;
     a.q = p->q;
     a.k = p->k;
     a.v = p->v;
@@ -269,6 +275,24 @@ ta_status ta_decode_ex(const ta_decode_params *p)
     if (s != TA_OK)
         return s;
     return decode_impl(p, nullptr, 0, 0, 0);
+}
+
+ta_status ta_decode_pi(const ta_decode_params *p, int window, int period)
+{
+    ta_status s = validate_decode(p);
+    if (s != TA_OK)
+        return s;
+    if (window < 0 || period < 1)
+        return fail(TA_ERR_INVALID_ARG, "pi-Attention needs window >= 0 and period >= 1");
+    return decode_impl(p, nullptr, 0, 0, 0, window, period);
+}
+
+size_t ta_decode_pi_workspace_bytes(int B, int Hq, int Hkv, int S, int D, int chunk, int n_split, int varlen,
+                                    int window, int period)
+{
+    if (S < 1 || window < 0 || period < 1)
+        return 0;
+    return ta_decode_workspace_bytes(B, Hq, Hkv, (int)ta::pi_max_keys(S, window, period), D, chunk, n_split, varlen);
 }
 
 ta_status ta_decode_paged(const ta_paged_decode_params *pp)
@@ -360,6 +384,7 @@ ta_status ta_decode_partials(const ta_decode_params *p, float *m, float *l, floa
     a.force_partials = true;
     a.block_table = nullptr;
     a.page_size = a.pages_per_seq = a.num_pages = 0;
+    a.pi_window = a.pi_period = 0;
     a.stream = static_cast<cudaStream_t>(p->stream);
     a.status = static_cast<int32_t *>(ws);
     a.counters = nullptr;

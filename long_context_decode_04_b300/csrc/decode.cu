@@ -94,6 +94,10 @@ struct DecodeParams {
     // block_table[b * pages_per_seq + j / page_size] at row j % page_size.
     const int32_t *block_table;
     int page_size, pages_per_seq, num_pages;
+    // pi-Attention key set (pi_period > 0): the query at i = L - 1 attends
+    // the window [max(0, i - pi_window), i] and the keys i - m * pi_period
+    // (m >= 1) before it; the chunks cut the ascending list of those keys.
+    int pi_window, pi_period;
 };
 
 template <typename T>
@@ -324,8 +328,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
                     L = L < 0 ? 0 : p.S;
                 }
             }
+            // the keys this sequence attends, as an ascending list of N
+            // positions: n_skip periodic keys r, r + pi, ... then the window
+            int N = L, w0 = 0, r0 = 0, n_skip = 0;
+            if (p.pi_period > 0 && L > 0) {
+                const int i = L - 1;
+                w0 = max(0, i - p.pi_window);
+                r0 = i % p.pi_period;
+                n_skip = w0 > r0 ? (w0 - 1 - r0) / p.pi_period + 1 : 0;
+                N = n_skip + (i - w0 + 1);
+            }
             const int c0 = split * p.chunk;
-            const int c1 = min(c0 + p.chunk, L);
+            const int c1 = min(c0 + p.chunk, N);
             const KV *kbase = static_cast<const KV *>(p.k) + (size_t)unit * kv_head_stride;
             const KV *vbase = static_cast<const KV *>(p.v) + (size_t)unit * kv_head_stride;
             int j0 = c0;
@@ -341,7 +355,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
                 }
                 desc[stage] = TileDesc{item, j0, n, flags};
                 unsigned char *dst = smem + stage * C::STAGE;
-                if (n > 0 && !p.block_table) {
+                if (n > 0 && p.pi_period > 0) {
+                    // periodic keys one row each (one run when the period is 1),
+                    // then the window as one contiguous run
+                    mbar_arrive_expect_tx(&full[stage], 2 * (uint32_t)n * C::RB);
+                    int pos = j0;
+                    const int skip_end = min(j0 + n, n_skip);
+                    if (p.pi_period == 1 && pos < skip_end) {
+                        const uint32_t bytes = (uint32_t)(skip_end - pos) * C::RB;
+                        bulk_copy_g2s_hint(dst, kbase + (size_t)(r0 + pos) * D, bytes, &full[stage], policy);
+                        bulk_copy_g2s_hint(dst + C::KV_OFF, vbase + (size_t)(r0 + pos) * D, bytes, &full[stage],
+                                           policy);
+                        pos = skip_end;
+                    }
+                    for (; pos < skip_end; ++pos) {
+                        const size_t key = (size_t)r0 + (size_t)pos * p.pi_period;
+                        const uint32_t so = (uint32_t)(pos - j0) * C::RB;
+                        bulk_copy_g2s_hint(dst + so, kbase + key * D, C::RB, &full[stage], policy);
+                        bulk_copy_g2s_hint(dst + C::KV_OFF + so, vbase + key * D, C::RB, &full[stage], policy);
+                    }
+                    if (pos < j0 + n) {
+                        const size_t key = (size_t)w0 + (size_t)(pos - n_skip);
+                        const uint32_t so = (uint32_t)(pos - j0) * C::RB;
+                        const uint32_t bytes = (uint32_t)(j0 + n - pos) * C::RB;
+                        bulk_copy_g2s_hint(dst + so, kbase + key * D, bytes, &full[stage], policy);
+                        bulk_copy_g2s_hint(dst + C::KV_OFF + so, vbase + key * D, bytes, &full[stage], policy);
+                    }
+                } else if (n > 0 && !p.block_table) {
                     const uint32_t bytes = (uint32_t)n * C::RB;
                     mbar_arrive_expect_tx(&full[stage], 2 * bytes);
                     bulk_copy_g2s_hint(dst, kbase + (size_t)j0 * D, bytes, &full[stage], policy);
@@ -790,6 +830,8 @@ cudaError_t launch_decode(const DecodeLaunch &a)
     p.page_size = a.page_size;
     p.pages_per_seq = a.pages_per_seq;
     p.num_pages = a.num_pages;
+    p.pi_window = a.pi_window;
+    p.pi_period = a.pi_period;
     const int G = a.Hq / a.Hkv;
     if (a.D == 128) {
         switch (G) {

@@ -38,6 +38,7 @@ struct DecodeLaunch {
     bool force_partials;               // write partials even when n_split == 1
     const int32_t *block_table;        // paged KV cache, or nullptr (contiguous [B, Hkv, S, D])
     int page_size, pages_per_seq, num_pages;
+    int pi_window, pi_period;          // pi-Attention key set (period 0: every key)
     cudaStream_t stream;
 };
 
@@ -53,6 +54,15 @@ ta_status check_decode_params(const ta_decode_params *p);
 inline bool decode_merges_itself(int n_split, int units)
 {
     return n_split > 1 && n_split <= kFusedMergeMaxSplits && units <= kMaxFusedUnits;
+}
+
+// Keys the pi-Attention decode attends at most for caches of up to S keys:
+// min(S, window + 1 + ceil(max(0, S - 1 - window) / period)).
+inline int64_t pi_max_keys(int64_t S, int64_t window, int64_t period)
+{
+    const int64_t far = S - 1 - window > 0 ? S - 1 - window : 0;
+    const int64_t n = (window + 1 < S ? window + 1 : S) + (far + period - 1) / period;
+    return n < S ? n : S;
 }
 
 // Scheduler (sched.cpp).

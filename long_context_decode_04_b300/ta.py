@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
         L.ta_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
         L.ta_decode_ex.argtypes = [ctypes.POINTER(DecodeParams)]
         L.ta_decode_paged.argtypes = [ctypes.POINTER(PagedDecodeParams)]
+        L.ta_decode_pi.argtypes = [ctypes.POINTER(DecodeParams), i, i]
+        L.ta_decode_pi_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i, i]
+        L.ta_decode_pi_workspace_bytes.restype = st
         L.ta_decode_partials.argtypes = [ctypes.POINTER(DecodeParams), vp, vp, vp]
         L.ta_decode_plan_for.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.POINTER(DecodePlan)]
         L.ta_decode_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
@@ -85,7 +88,7 @@ def lib() -> ctypes.CDLL:
         L.ta_prefill_causal.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         L.ta_last_error.argtypes = []
         L.ta_last_error.restype = ctypes.c_char_p
-        for fn in ("ta_decode", "ta_decode_noalloc", "ta_decode_ex", "ta_decode_paged", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
+        for fn in ("ta_decode", "ta_decode_noalloc", "ta_decode_ex", "ta_decode_paged", "ta_decode_pi", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
                    "ta_prefill_causal"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
@@ -157,6 +160,30 @@ def decode(q, k, v, *, seqlens=None, scale=None, out_dtype=None, chunk=0, n_spli
     p.stream = torch.cuda.current_stream(q.device).cuda_stream
     _check(lib().ta_decode_ex(ctypes.byref(p)))
     return out, lse
+
+
+def decode_pi(q, k, v, window, period, *, seqlens=None, scale=None, out_dtype=None, chunk=0, n_split=0,
+              workspace=None, out=None, lse=None):
+    """Decode over the pi-Attention key set: the window of the last ``window``
+    keys plus every ``period``-th key before it, counted back from the
+    newest.  Shapes as ``decode``; returns (out, lse)."""
+    B, Hq, D = q.shape
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    p = _params(q, k, v, seqlens, scale, chunk, n_split, workspace, out=out, lse=lse, out_dtype=out.dtype)
+    _check(lib().ta_decode_pi(ctypes.byref(p), int(window), int(period)))
+    return out, lse
+
+
+def decode_pi_workspace(B, Hq, Hkv, S, D, window, period, *, chunk=0, n_split=0, varlen=False, device="cuda"):
+    n = int(lib().ta_decode_pi_workspace_bytes(B, Hq, Hkv, S, D, chunk, n_split, int(bool(varlen)), window,
+                                               period))
+    if n == 0:
+        raise TAError(TA_ERR_INVALID_ARG, "bad pi-Attention workspace arguments")
+    return torch.zeros(max(256, n), dtype=torch.uint8, device=device)
 
 
 def decode_paged(q, k_pages, v_pages, block_table, seqlens, *, scale=None, out_dtype=None, chunk=0, n_split=0,

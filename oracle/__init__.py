@@ -168,3 +168,39 @@ def decode_paged(q, k_pages, v_pages, block_table, seqlens, scale, rows=None, th
             kc[b, :, pg * page:(pg + 1) * page] = kp[table[b, pg]]
             vc[b, :, pg * page:(pg + 1) * page] = vp[table[b, pg]]
     return decode(q, kc, vc, scale, seqlens=lens.astype(np.int32), rows=rows, threads=threads)
+
+
+def pi_key_set(L, window, period):
+    """The keys the newest query (position i = L - 1) attends under pi-Attention
+    (pi-Attention explainer, technical summary section 2A): the ring-local
+    window [i - window, i] and the periodic skips i - m * period (m >= 1)
+    before it; past keys only.  Ascending list."""
+    if L <= 0:
+        return []
+    i = L - 1
+    keys = set(range(max(0, i - window), i + 1))
+    j = i - period
+    while j >= 0:
+        keys.add(j)
+        j -= period
+    return sorted(keys)
+
+
+def decode_pi(q, k, v, scale, window, period, seqlens=None, rows=None, threads=None):
+    """Decode attention restricted to each sequence's pi-Attention key set: the
+    definition of ``decode`` over the gathered keys (a numpy gather); the fusion
+    gate of that page is not applied."""
+    ka, kt = _raw(k)
+    va, vt = _raw(v)
+    B, Hkv, S, D = ka.shape
+    lens = [S] * B if seqlens is None else [int(x) for x in seqlens]
+    sets = [pi_key_set(L, window, period) for L in lens]
+    n = max(1, max(len(x) for x in sets))
+    kg = np.zeros((B, Hkv, n, D), dtype=ka.dtype)
+    vg = np.zeros((B, Hkv, n, D), dtype=va.dtype)
+    for b, idx in enumerate(sets):
+        if idx:
+            kg[b, :, :len(idx)] = ka[b][:, idx]
+            vg[b, :, :len(idx)] = va[b][:, idx]
+    glens = np.array([len(x) for x in sets], dtype=np.int32)
+    return decode(q, kg, vg, scale, seqlens=glens, rows=rows, threads=threads)

@@ -463,4 +463,43 @@ def pin_paged_page_permutation():
     assert np.array_equal(a[0], b_[0]) and np.array_equal(a[1], b_[1])
 
 
+# ------------------------------------------------------------ pi-Attention key set
+
+def pin_pi_brute_force():
+    """pi-Attention decode against 50-digit attention over the keys chosen one by
+    one from the definition: j in the window [i - w, i], or i - j a positive
+    multiple of the period."""
+    rng = _rng(51)
+    B, Hkv, G, S, D = 2, 2, 2, 23, 4
+    q = _f32(rng, B, Hkv * G, D)
+    k = _f32(rng, B, Hkv, S, D, scale=1.4)
+    v = _f32(rng, B, Hkv, S, D)
+    for window, period in ((0, 1), (2, 3), (4, 5), (0, 7), (30, 2), (3, 50)):
+        lens = [23, 9]
+        out, lse = oracle.decode_pi(q, k, v, 0.6, window, period, seqlens=lens)
+        for b in range(B):
+            i = lens[b] - 1
+            chosen = [j for j in range(lens[b]) if i - window <= j <= i or (i - j) % period == 0]
+            for h in range(Hkv * G):
+                ref, ref_lse = _mp_attend(q[b, h], k[b, h // G, chosen], v[b, h // G, chosen], 0.6)
+                assert np.max(np.abs(out[b * Hkv * G + h] - np.array(ref))) < 1e-13, (window, period, b, h)
+                assert abs(lse[b * Hkv * G + h] - ref_lse) < 1e-13
+
+
+def pin_pi_special_cases():
+    """Period 1, or a window reaching key 0, attends every key (plain decode);
+    a period longer than the sequence leaves the window only."""
+    rng = _rng(52)
+    q = _f32(rng, 1, 4, 8)
+    k = _f32(rng, 1, 2, 40, 8)
+    v = _f32(rng, 1, 2, 40, 8)
+    dense = oracle.decode(q, k, v, 0.4)
+    for window, period in ((0, 1), (5, 1), (39, 9), (100, 3)):
+        got = oracle.decode_pi(q, k, v, 0.4, window, period)
+        assert np.array_equal(got[0], dense[0]) and np.array_equal(got[1], dense[1]), (window, period)
+    tail = oracle.decode(q, np.ascontiguousarray(k[:, :, 33:]), np.ascontiguousarray(v[:, :, 33:]), 0.4)
+    got = oracle.decode_pi(q, k, v, 0.4, 6, 41)
+    assert np.array_equal(got[0], tail[0]) and np.array_equal(got[1], tail[1])
+
+
 ALL_PINS = [f for name, f in sorted(globals().items()) if name.startswith("pin_") and callable(f)]

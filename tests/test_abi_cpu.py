@@ -156,3 +156,22 @@ def test_paged_decode_rejects_bad_arguments_before_launch(kw, status):
     p = ta.PagedDecodeParams(**base)
     assert ta.lib().ta_decode_paged(ctypes.byref(p)) == status
     assert len(ta.lib().ta_last_error()) > 0
+
+
+def test_pi_decode_rejects_bad_window_and_period():
+    p = ta.DecodeParams(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, B=1, Hq=8, Hkv=2, S=64, D=128,
+                        scale=0.1, in_dtype=ta.TA_BF16, out_dtype=ta.TA_BF16)
+    assert ta.lib().ta_decode_pi(ctypes.byref(p), -1, 4) == ta.TA_ERR_INVALID_ARG
+    assert ta.lib().ta_decode_pi(ctypes.byref(p), 4, 0) == ta.TA_ERR_INVALID_ARG
+    assert ta.lib().ta_decode_pi_workspace_bytes(1, 8, 2, 64, 128, 0, 0, 0, 4, 0) == 0
+
+
+@pytest.mark.parametrize("S,window,period", [(1, 0, 1), (100, 0, 1), (100, 5, 7), (131072, 4096, 64),
+                                             (1000, 2000, 3), (50, 3, 100)])
+def test_pi_key_bound_covers_every_length(S, window, period):
+    """The plan cuts the list of attended keys; its length bound must hold for
+    every sequence length up to S (checked against the oracle's key set)."""
+    import oracle
+    bound = min(S, min(window + 1, S) + -(-max(0, S - 1 - window) // period))
+    for L in sorted(x for x in {1, 2, S // 3, S // 2, S - 1, S} if 1 <= x <= S):
+        assert len(oracle.pi_key_set(L, window, period)) <= bound

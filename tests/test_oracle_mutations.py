@@ -114,3 +114,32 @@ def test_paged_mutation_is_caught(monkeypatch, name):
         except (AssertionError, ValueError, IndexError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught mutation {name}"
+
+
+PI_MUTATIONS = {
+    "window_excludes_newest": ("keys = set(range(max(0, i - window), i + 1))",
+                               "keys = set(range(max(0, i - window), i))"),
+    "window_one_short": ("keys = set(range(max(0, i - window), i + 1))",
+                         "keys = set(range(max(0, i - window + 1), i + 1))"),
+    "skips_from_window_start": ("j = i - period\n", "j = max(0, i - window) - period\n"),
+    "skip_step_doubled": ("        j -= period", "        j -= 2 * period"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PI_MUTATIONS))
+def test_pi_mutation_is_caught(monkeypatch, name):
+    import inspect
+    import textwrap
+    old, new = PI_MUTATIONS[name]
+    src = textwrap.dedent(inspect.getsource(oracle.pi_key_set))
+    assert src.count(old) >= 1, f"mutation {name}: pattern not found"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, "pi_key_set", ns["pi_key_set"])
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutation {name}"
