@@ -18,7 +18,8 @@
 // (about 4 FLOP per byte at G = 4) under it.
 //
 // Kernel layout (one persistent CTA per SM, 16 warps):
-//   * warp 15, lane 0 is the producer.  It pulls work items
+//   * warp 15 is the producer (lane 0 decides, the 32 lanes share the
+//     copies of a tile).  It pulls work items
 //     (sequence, KV head, chunk) from a device-wide queue and stages the
 //     chunk's K and V rows into shared memory, a tile at a time, with
 //     one-dimensional bulk async copies into a ring of stages guarded by
@@ -56,6 +57,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace ta {
 namespace {
@@ -98,6 +100,12 @@ struct DecodeParams {
     // the window [max(0, i - pi_window), i] and the keys i - m * pi_period
     // (m >= 1) before it; the chunks cut the ascending list of those keys.
     int pi_window, pi_period;
+    // pi_tma: K and V of each (sequence, KV head) seen as rows of
+    // pi_period keys, [B*Hkv, ceil(S / period), period * D] with a box of
+    // D x TILE: the box at x = r * D, y = m gathers keys r + (m + t) * period,
+    // t < TILE, in one copy.
+    int pi_tma;
+    CUtensorMap pi_kmap, pi_vmap;
 };
 
 template <typename T>
@@ -245,7 +253,7 @@ struct Cfg {
     static constexpr int PBUF_FLOATS = kConsumerWarps * KPW * G;
     static constexpr int FM_FLOATS = 2 * G * kFusedMergeMaxSplits;  // partial m, l of one unit
     static constexpr size_t SMEM = (size_t)STAGES * STAGE + (size_t)(MERGE_FLOATS + PBUF_FLOATS + FM_FLOATS) * 4 +
-                                   (2 * STAGES + 5) * 8 + STAGES * sizeof(TileDesc) + 16;
+                                   (2 * STAGES + 5) * 8 + STAGES * sizeof(TileDesc) + 16 + 1024;
     static_assert(NCH >= 1 && RB % 128 == 0, "row must be a multiple of 128 bytes");
     static_assert(STAGES >= 2, "need at least two stages");
     static_assert(kDecodeTileKeys % TILE == 0, "chunks must be whole tiles");
@@ -253,10 +261,13 @@ struct Cfg {
 };
 
 template <int D, int G, typename KV, typename OUT>
-__global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_constant__ DecodeParams p)
 {
     using C = Cfg<D, G, KV>;
-    extern __shared__ __align__(1024) unsigned char smem[];
+    // stage buffers start on a 1024-byte boundary (tensor copies need 128)
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    unsigned char *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     float *merge_o = reinterpret_cast<float *>(smem + C::STAGES * C::STAGE);  // [W][G][D]
     float *merge_m = merge_o + kConsumerWarps * G * D;                         // [W][G]
     float *merge_l = merge_m + kConsumerWarps * G;                             // [W][G]
@@ -296,8 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        if (lane != 0)
-            return;
+        // Lane 0 takes the decisions (work queue, ring waits, expected bytes,
+        // descriptors); every lane computes the same schedule and the 32
+        // lanes share the bulk copies of a tile (gathered rows of the
+        // pi-Attention set or a paged cache need one copy per run of rows).
+        const bool leader = lane == 0;
         const uint64_t policy = l2_policy_evict_first();
         int stage = 0;
         uint32_t phase = 0;
@@ -305,16 +319,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
         const size_t kv_head_stride = (size_t)p.S * D;
         bool ok = true;
         while (ok) {
-            const int item = atomicAdd(&p.status[16], 1);
+            int item = 0;
+            if (leader)
+                item = atomicAdd(&p.status[16], 1);
+            item = __shfl_sync(kFull, item, 0);
             if (item >= p.n_items) {
-                if (item == p.n_items + (int)gridDim.x - 1)
-                    atomicExch(&p.status[16], 0);  // last grab of the launch: reset the queue
-                if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag))
-                    break;
-                desc[stage] = TileDesc{item, 0, 0, kEnd};
-                mbar_arrive(&full[stage]);
-                used_mask |= 1u << stage;
-                parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
+                bool w = true;
+                if (leader) {
+                    if (item == p.n_items + (int)gridDim.x - 1)
+                        atomicExch(&p.status[16], 0);  // last grab of the launch: reset the queue
+                    w = mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag);
+                    if (w) {
+                        desc[stage] = TileDesc{item, 0, 0, kEnd};
+                        mbar_arrive(&full[stage]);
+                    }
+                }
+                if (__shfl_sync(kFull, w, 0)) {
+                    used_mask |= 1u << stage;
+                    parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
+                }
                 break;
             }
             const int unit = item / p.n_split;
@@ -324,7 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
             if (p.seqlens) {
                 L = p.seqlens[b];
                 if (L < 0 || L > p.S) {
-                    atomicOr(&p.status[0], TA_DEVERR_SEQLEN);
+                    if (leader)
+                        atomicOr(&p.status[0], TA_DEVERR_SEQLEN);
                     L = L < 0 ? 0 : p.S;
                 }
             }
@@ -349,32 +373,49 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
                 const bool last = j0 + n >= c1;
                 if (last)
                     flags |= kLast;
-                if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag)) {
+                bool w = true;
+                if (leader) {
+                    w = mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag);
+                    if (w) {
+                        desc[stage] = TileDesc{item, j0, n, flags};
+                        if (n > 0)
+                            mbar_arrive_expect_tx(&full[stage], 2 * (uint32_t)n * C::RB);
+                        else
+                            mbar_arrive(&full[stage]);
+                    }
+                }
+                if (!__shfl_sync(kFull, w, 0)) {
                     ok = false;
                     break;
                 }
-                desc[stage] = TileDesc{item, j0, n, flags};
                 unsigned char *dst = smem + stage * C::STAGE;
                 if (n > 0 && p.pi_period > 0) {
                     // periodic keys one row each (one run when the period is 1),
                     // then the window as one contiguous run
-                    mbar_arrive_expect_tx(&full[stage], 2 * (uint32_t)n * C::RB);
-                    int pos = j0;
                     const int skip_end = min(j0 + n, n_skip);
-                    if (p.pi_period == 1 && pos < skip_end) {
-                        const uint32_t bytes = (uint32_t)(skip_end - pos) * C::RB;
-                        bulk_copy_g2s_hint(dst, kbase + (size_t)(r0 + pos) * D, bytes, &full[stage], policy);
-                        bulk_copy_g2s_hint(dst + C::KV_OFF, vbase + (size_t)(r0 + pos) * D, bytes, &full[stage],
-                                           policy);
-                        pos = skip_end;
+                    if (p.pi_tma && n == C::TILE && skip_end == j0 + n) {
+                        // a whole tile of periodic keys: one strided box each
+                        if (leader) {
+                            tc::tma_load_3d(dst, &p.pi_kmap, r0 * D, j0, unit, &full[stage]);
+                            tc::tma_load_3d(dst + C::KV_OFF, &p.pi_vmap, r0 * D, j0, unit, &full[stage]);
+                        }
+                    } else if (p.pi_period == 1) {
+                        if (leader && j0 < skip_end) {
+                            const uint32_t bytes = (uint32_t)(skip_end - j0) * C::RB;
+                            bulk_copy_g2s_hint(dst, kbase + (size_t)(r0 + j0) * D, bytes, &full[stage], policy);
+                            bulk_copy_g2s_hint(dst + C::KV_OFF, vbase + (size_t)(r0 + j0) * D, bytes, &full[stage],
+                                               policy);
+                        }
+                    } else {
+                        for (int pos = j0 + lane; pos < skip_end; pos += 32) {  // one row per lane
+                            const size_t key = (size_t)r0 + (size_t)pos * p.pi_period;
+                            const uint32_t so = (uint32_t)(pos - j0) * C::RB;
+                            bulk_copy_g2s_hint(dst + so, kbase + key * D, C::RB, &full[stage], policy);
+                            bulk_copy_g2s_hint(dst + C::KV_OFF + so, vbase + key * D, C::RB, &full[stage], policy);
+                        }
                     }
-                    for (; pos < skip_end; ++pos) {
-                        const size_t key = (size_t)r0 + (size_t)pos * p.pi_period;
-                        const uint32_t so = (uint32_t)(pos - j0) * C::RB;
-                        bulk_copy_g2s_hint(dst + so, kbase + key * D, C::RB, &full[stage], policy);
-                        bulk_copy_g2s_hint(dst + C::KV_OFF + so, vbase + key * D, C::RB, &full[stage], policy);
-                    }
-                    if (pos < j0 + n) {
+                    const int pos = max(j0, skip_end);
+                    if (leader && pos < j0 + n) {
                         const size_t key = (size_t)w0 + (size_t)(pos - n_skip);
                         const uint32_t so = (uint32_t)(pos - j0) * C::RB;
                         const uint32_t bytes = (uint32_t)(j0 + n - pos) * C::RB;
@@ -382,17 +423,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
                         bulk_copy_g2s_hint(dst + C::KV_OFF + so, vbase + key * D, bytes, &full[stage], policy);
                     }
                 } else if (n > 0 && !p.block_table) {
-                    const uint32_t bytes = (uint32_t)n * C::RB;
-                    mbar_arrive_expect_tx(&full[stage], 2 * bytes);
-                    bulk_copy_g2s_hint(dst, kbase + (size_t)j0 * D, bytes, &full[stage], policy);
-                    bulk_copy_g2s_hint(dst + C::KV_OFF, vbase + (size_t)j0 * D, bytes, &full[stage], policy);
+                    if (leader) {
+                        const uint32_t bytes = (uint32_t)n * C::RB;
+                        bulk_copy_g2s_hint(dst, kbase + (size_t)j0 * D, bytes, &full[stage], policy);
+                        bulk_copy_g2s_hint(dst + C::KV_OFF, vbase + (size_t)j0 * D, bytes, &full[stage], policy);
+                    }
                 } else if (n > 0) {
-                    // paged: one copy per page segment of the tile
-                    mbar_arrive_expect_tx(&full[stage], 2 * (uint32_t)n * C::RB);
+                    // paged: one copy per page segment of the tile, segment s
+                    // issued by lane s % 32 (segment 0 starts at j0, the
+                    // others at page starts)
                     const int kvh = unit - b * p.Hkv;
                     const int32_t *bt = p.block_table + (size_t)b * p.pages_per_seq;
-                    for (int j = j0; j < j0 + n;) {
-                        const int pg = j / p.page_size;
+                    const int pg0 = j0 / p.page_size;
+                    const int n_seg = (j0 + n - 1) / p.page_size - pg0 + 1;
+                    for (int sg = lane; sg < n_seg; sg += 32) {
+                        const int pg = pg0 + sg;
+                        const int j = sg == 0 ? j0 : pg * p.page_size;
                         const int off = j - pg * p.page_size;
                         const int cnt = min(p.page_size - off, j0 + n - j);
                         int page = bt[pg];
@@ -407,10 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
                                            policy);
                         bulk_copy_g2s_hint(dst + C::KV_OFF + so, static_cast<const KV *>(p.v) + row * D, bytes,
                                            &full[stage], policy);
-                        j += cnt;
                     }
-                } else {
-                    mbar_arrive(&full[stage]);
                 }
                 used_mask |= 1u << stage;
                 parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
@@ -424,14 +467,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const DecodeP
                 flags = 0;
             }
         }
-        // Drain: every copy this thread issued has landed before the CTA exits
+        // Drain: every copy this warp issued has landed before the CTA exits
         // (immediate on the normal path; bounded after an abort).
-        int drain_abort = 0;
-        for (int s = 0; s < C::STAGES; ++s)
-            if (used_mask & (1u << s))
-                mbar_wait_bounded(&full[s], (parity_mask >> s) & 1u, &drain_abort);
-        if (*abort_flag)
-            atomicOr(&p.status[0], TA_DEVERR_TIMEOUT);
+        __syncwarp();
+        if (leader) {
+            int drain_abort = 0;
+            for (int s = 0; s < C::STAGES; ++s)
+                if (used_mask & (1u << s))
+                    mbar_wait_bounded(&full[s], (parity_mask >> s) & 1u, &drain_abort);
+            if (*abort_flag)
+                atomicOr(&p.status[0], TA_DEVERR_TIMEOUT);
+        }
         return;
     }
 
@@ -832,6 +878,18 @@ cudaError_t launch_decode(const DecodeLaunch &a)
     p.num_pages = a.num_pages;
     p.pi_window = a.pi_window;
     p.pi_period = a.pi_period;
+    p.pi_tma = 0;
+    if (a.pi_period > 1) {
+        const bool bf16 = a.in_dtype == TA_BF16;
+        const uint64_t es = bf16 ? 2 : 4;
+        const uint64_t dims[3] = {(uint64_t)a.pi_period * a.D, ((uint64_t)a.S + a.pi_period - 1) / a.pi_period,
+                                  (uint64_t)a.B * a.Hkv};
+        const uint64_t strides[2] = {(uint64_t)a.pi_period * a.D * es, (uint64_t)a.S * a.D * es};
+        const uint32_t box[3] = {(uint32_t)a.D, (uint32_t)(a.D * es > 256 ? 60 : 120), 1};
+        // the boxes only ever cover keys below S of one (sequence, KV head)
+        p.pi_tma = encode_tmap_3d(&p.pi_kmap, a.k, bf16, dims, strides, box, false) &&
+                   encode_tmap_3d(&p.pi_vmap, a.v, bf16, dims, strides, box, false);
+    }
     const int G = a.Hq / a.Hkv;
     if (a.D == 128) {
         switch (G) {

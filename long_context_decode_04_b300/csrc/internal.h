@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <string>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/ta.h"
@@ -64,6 +65,12 @@ inline int64_t pi_max_keys(int64_t S, int64_t window, int64_t period)
     const int64_t n = (window + 1 < S ? window + 1 : S) + (far + period - 1) / period;
     return n < S ? n : S;
 }
+
+// A 3-D TMA tensor map (tmap.cpp): dims innermost first, strides in bytes
+// of dims 1 and 2, box in elements; bf16 or fp32 elements; zero fill out of
+// range.  false if the driver entry point or the encoding fails.
+bool encode_tmap_3d(CUtensorMap *m, const void *base, bool bf16, const uint64_t dims[3], const uint64_t strides[2],
+                    const uint32_t box[3], bool swizzle128);
 
 // Scheduler (sched.cpp).
 ta_status plan_decode(int B, int Hq, int Hkv, int S, int D, int chunk, int n_split, int varlen,

@@ -446,38 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
 
 // ------------------------------------------------------------------ host
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return static_cast<EncodeTiledFn>(nullptr);
-        return reinterpret_cast<EncodeTiledFn>(f);
-    }();
-    return fn;
-}
-
 // 3-D map over a [rows3, S, D] bf16 tensor, box {64, 128, 1}, 128-byte
 // swizzle; out-of-range rows read as zero.
 bool make_map(CUtensorMap *m, const void *base, int S, int rows3)
 {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc)
-        return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)kHD, (cuuint64_t)S, (cuuint64_t)rows3};
-    const cuuint64_t strides[2] = {(cuuint64_t)kHD * 2, (cuuint64_t)S * kHD * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kBM, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const uint64_t dims[3] = {(uint64_t)kHD, (uint64_t)S, (uint64_t)rows3};
+    const uint64_t strides[2] = {(uint64_t)kHD * 2, (uint64_t)S * kHD * 2};
+    const uint32_t box[3] = {64, (uint32_t)kBM, 1};
+    return encode_tmap_3d(m, base, true, dims, strides, box, true);
 }
 
 }  // namespace
