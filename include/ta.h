@@ -302,6 +302,26 @@ size_t ta_combine_workspace_bytes(int R, int N, int D);
 ta_status ta_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse,
                             int B, int H, int Hkv, int S, int D, float scale, void *stream);
 
+/*
+ * Causal prefill of a packed batch of variable-length sequences: the
+ * prefill-side twin of the variable-length decode, same fused kernel.
+ * Sequence s is tokens [cu_seqlens[s], cu_seqlens[s+1]) of the packed
+ * tensors; within it query row i attends keys 0..i of the same sequence.
+ *   q, out [total_tokens, H, D] bf16; k, v [total_tokens, Hkv, D] bf16;
+ *   lse [H, total_tokens] fp32 (may be NULL);
+ *   cu_seqlens [num_seqs + 1] int32 on the device, non-decreasing, from 0 to
+ *     total_tokens; every sequence at most max_seqlen tokens long.  Offsets
+ *     that break this are not followed past the tensors:
+ *     TA_DEVERR_SEQLEN is recorded (read with ta_decode_status(NULL, ...))
+ *     and rows past max_seqlen are not written.
+ * Keys of a neighbouring sequence that share a 128-key tile with attended
+ * keys are masked (weight exactly 0), so they must be finite.
+ * Supported: D = 128; H % Hkv == 0; scale > 0; q, k, v, out 16-byte aligned.
+ */
+ta_status ta_prefill_causal_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                                   const int32_t *cu_seqlens, int num_seqs, int max_seqlen, int total_tokens,
+                                   int H, int Hkv, int D, float scale, void *stream);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char *ta_last_error(void);
 

@@ -530,4 +530,37 @@ ta_status ta_prefill_causal(const void *q, const void *k, const void *v, void *o
     return TA_OK;
 }
 
+ta_status ta_prefill_causal_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                                   const int32_t *cu_seqlens, int num_seqs, int max_seqlen, int total_tokens, int H,
+                                   int Hkv, int D, float scale, void *stream)
+{
+    if (!q || !k || !v || !out || !cu_seqlens)
+        return fail(TA_ERR_INVALID_ARG, "q, k, v, out and cu_seqlens must be non-NULL");
+    if (num_seqs < 1 || max_seqlen < 1 || total_tokens < 1 || H < 1 || Hkv < 1 || D < 1)
+        return fail(TA_ERR_INVALID_ARG, "num_seqs, max_seqlen, total_tokens, H, Hkv and D must all be >= 1");
+    if (H % Hkv != 0)
+        return fail(TA_ERR_INVALID_ARG, "H must be a multiple of Hkv");
+    if (!std::isfinite(scale))
+        return fail(TA_ERR_INVALID_ARG, "scale must be finite");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4)) ||
+        !aligned(cu_seqlens, 4))
+        return fail(TA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned, lse and cu_seqlens 4-byte aligned");
+    if (D != 128)
+        return fail(TA_ERR_UNSUPPORTED, "prefill supports head dim D = 128");
+    if (!(scale > 0.f))
+        return fail(TA_ERR_UNSUPPORTED, "prefill supports scale > 0");
+    if ((double)total_tokens * H * D > 9.0e18 / 4 || (double)num_seqs * H * ((max_seqlen + 255) / 256) > 2.0e9)
+        return fail(TA_ERR_INVALID_ARG, "problem size overflows");
+    void *ws = nullptr;
+    ta_status s = library_workspace(256, &ws);
+    if (s != TA_OK)
+        return s;
+    cudaError_t e = ta::launch_prefill_causal_varlen(q, k, v, out, lse, cu_seqlens, num_seqs, max_seqlen,
+                                                     total_tokens, H, Hkv, D, scale, static_cast<int32_t *>(ws),
+                                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "prefill kernel launch");
+    return TA_OK;
+}
+
 }  // extern "C"

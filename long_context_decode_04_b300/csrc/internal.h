@@ -86,5 +86,8 @@ cudaError_t launch_combine(const float *m, const float *l, const float *o, int R
 cudaError_t launch_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse, int B,
                                   int H, int Hkv, int S, int D, float scale, int32_t *status,
                                   cudaStream_t stream);
+cudaError_t launch_prefill_causal_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                                         const int32_t *cu_seqlens, int num_seqs, int max_seqlen, int T, int H,
+                                         int Hkv, int D, float scale, int32_t *status, cudaStream_t stream);
 
 }  // namespace ta

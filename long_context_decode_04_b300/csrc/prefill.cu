@@ -75,14 +75,19 @@ constexpr size_t kSmemBytes = kBarOff + 256 + 1024;  // + alignment slack
 constexpr float kRescaleLog2 = 8.0f;
 
 struct PrefillParams {
-    CUtensorMap qmap;  // [B*H, S, D] bf16, box {64, 128, 1}
-    CUtensorMap kmap;  // [B*Hkv, S, D]
+    // batched: q [B*H, S, D], k/v [B*Hkv, S, D] (z = (b, head), y = token);
+    // packed variable lengths: q [T, H, D], k/v [T, Hkv, D] seen as
+    // {D, T, heads} (z = head, y = token).  bf16, box {64, 128, 1}.
+    CUtensorMap qmap;
+    CUtensorMap kmap;
     CUtensorMap vmap;
     __nv_bfloat16 *out;
     float *lse;
-    int S, H, G, n_qt, BH;
-    float c;  // scale * log2(e)
+    int S, H, G, n_qt, BH;  // S: keys per sequence (batched) or max_seqlen (packed)
+    float c;                // scale * log2(e)
     int32_t *status;
+    const int32_t *cu_seqlens;  // packed: [BH / H + 1] token offsets; nullptr: batched
+    int T;                      // packed: total tokens
 };
 
 struct Bars {
@@ -116,7 +121,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
     const int bh = (int)(blockIdx.x % p.BH);
     const int q0 = qt * 2 * kBM;
     const int bh_kv = (bh / p.H) * (p.H / p.G) + (bh % p.H) / p.G;
-    const bool active1 = q0 + kBM < p.S;
+    // This CTA's sequence: L tokens starting at token y0 of the maps' y axis,
+    // at z = zq (queries) and zkv (keys, values).
+    int L = p.S, y0 = 0, zq = bh, zkv = bh_kv;
+    if (p.cu_seqlens) {
+        const int seq = bh / p.H, h = bh - seq * p.H;
+        const int a = p.cu_seqlens[seq], e = p.cu_seqlens[seq + 1];
+        if (threadIdx.x == 0 && qt == 0 && (a < 0 || e < a || e > p.T || e - a > p.S))
+            atomicOr(p.status, TA_DEVERR_SEQLEN);
+        y0 = max(0, min(a, p.T));
+        L = max(0, min(e, p.T) - y0);
+        zq = h;
+        zkv = h / p.G;
+        if (q0 >= L)
+            return;  // past this sequence's end: the whole CTA leaves before any set-up
+    }
+    const bool active1 = q0 + kBM < L;
     const int diag0 = 2 * qt, diag1 = 2 * qt + 1;
     const int nk = (active1 ? diag1 : diag0) + 1;  // K/V tiles this CTA walks
 
@@ -159,8 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
             mbar_arrive_expect_tx(&bars->q_full, n_q * kTileBytes);
             for (int t = 0; t < n_q; ++t) {
                 unsigned char *dst = smem + kQOff + t * kTileBytes;
-                tc::tma_load_3d(dst, &p.qmap, 0, q0 + t * kBM, bh, &bars->q_full);
-                tc::tma_load_3d(dst + kHalfBytes, &p.qmap, 64, q0 + t * kBM, bh, &bars->q_full);
+                tc::tma_load_3d(dst, &p.qmap, 0, y0 + q0 + t * kBM, zq, &bars->q_full);
+                tc::tma_load_3d(dst + kHalfBytes, &p.qmap, 64, y0 + q0 + t * kBM, zq, &bars->q_full);
             }
             // Issue order K0, K1, V0, K2, V1, ...: K runs one tile ahead of
             // V, since S of a tile needs K while its PV comes a softmax later.
@@ -175,8 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                     }
                     unsigned char *kd = smem + kKOff + st * kTileBytes;
                     mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-                    tc::tma_load_3d(kd, &p.kmap, 0, i * kBN, bh_kv, &bars->k_full[st]);
-                    tc::tma_load_3d(kd + kHalfBytes, &p.kmap, 64, i * kBN, bh_kv, &bars->k_full[st]);
+                    tc::tma_load_3d(kd, &p.kmap, 0, y0 + i * kBN, zkv, &bars->k_full[st]);
+                    tc::tma_load_3d(kd + kHalfBytes, &p.kmap, 64, y0 + i * kBN, zkv, &bars->k_full[st]);
                     ++k_armed[st];
                 }
                 if (i > 0) {  // V tile i - 1
@@ -188,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                     }
                     unsigned char *vd = smem + kVOff + st * kTileBytes;
                     mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-                    tc::tma_load_3d(vd, &p.vmap, 0, j * kBN, bh_kv, &bars->v_full[st]);
-                    tc::tma_load_3d(vd + kHalfBytes, &p.vmap, 64, j * kBN, bh_kv, &bars->v_full[st]);
+                    tc::tma_load_3d(vd, &p.vmap, 0, y0 + j * kBN, zkv, &bars->v_full[st]);
+                    tc::tma_load_3d(vd + kHalfBytes, &p.vmap, 64, y0 + j * kBN, zkv, &bars->v_full[st]);
                     ++v_armed[st];
                 }
             }
@@ -312,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
         const int t = warp >> 2;  // query tile
         const int r = threadIdx.x & (kBM - 1);
         const int qrow0 = q0 + t * kBM;
-        if (qrow0 < p.S) {
+        if (qrow0 < L) {
             const int diag = qrow0 / kBN;
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
             const uint32_t s_tmem = tmem + lane_base + t * kBN;
@@ -409,7 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                 tc::fence_after_sync();
                 const int row = qrow0 + r;
                 const float inv = 1.0f / l;
-                __nv_bfloat16 *orow = p.out + ((size_t)bh * p.S + row) * kHD;
+                // output row: [b*H + h][S][D] batched, [T][H][D] packed; lse
+                // [b*H + h][S] batched, [H][T] packed
+                __nv_bfloat16 *orow = p.cu_seqlens ? p.out + ((size_t)(y0 + row) * p.H + zq) * kHD
+                                                   : p.out + ((size_t)bh * p.S + row) * kHD;
+                const size_t lse_at = p.cu_seqlens ? (size_t)zq * p.T + y0 + row : (size_t)bh * p.S + row;
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t u[32];
@@ -419,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         pk[i] = tc::pack_bf16x2(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
-                    if (row < p.S) {
+                    if (row < L) {
                         // streaming stores: the output is not read again here,
                         // so its lines leave L2 first instead of lingering dirty
                         uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
@@ -428,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                             __stcs(dst + i, make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]));
                     }
                 }
-                if (row < p.S && p.lse)
-                    __stcs(p.lse + (size_t)bh * p.S + row, (m_used + fast_log2(l)) * kLn2);
+                if (row < L && p.lse)
+                    __stcs(p.lse + lse_at, (m_used + fast_log2(l)) * kLn2);
             }
         }
     }
@@ -475,6 +499,45 @@ cudaError_t launch_prefill_causal(const void *q, const void *k, const void *v, v
     p.BH = B * H;
     p.c = scale * kLog2e;
     p.status = status;
+    p.cu_seqlens = nullptr;
+    p.T = 0;
+    cudaError_t e = cudaFuncSetAttribute(prefill_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    const long long grid = (long long)p.n_qt * p.BH;
+    prefill_causal_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_causal_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                                         const int32_t *cu_seqlens, int num_seqs, int max_seqlen, int T, int H,
+                                         int Hkv, int D, float scale, int32_t *status, cudaStream_t stream)
+{
+    if (D != kHD)
+        return cudaErrorNotSupported;
+    PrefillParams p;
+    // the packed tensors as {D, T, heads}: token stride heads * D, head stride D
+    const uint64_t qdims[3] = {(uint64_t)kHD, (uint64_t)T, (uint64_t)H};
+    const uint64_t qstr[2] = {(uint64_t)H * kHD * 2, (uint64_t)kHD * 2};
+    const uint64_t kdims[3] = {(uint64_t)kHD, (uint64_t)T, (uint64_t)Hkv};
+    const uint64_t kstr[2] = {(uint64_t)Hkv * kHD * 2, (uint64_t)kHD * 2};
+    const uint32_t box[3] = {64, (uint32_t)kBM, 1};
+    if (!encode_tmap_3d(&p.qmap, q, true, qdims, qstr, box, true) ||
+        !encode_tmap_3d(&p.kmap, k, true, kdims, kstr, box, true) ||
+        !encode_tmap_3d(&p.vmap, v, true, kdims, kstr, box, true))
+        return cudaErrorInvalidValue;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.S = max_seqlen;
+    p.H = H;
+    p.G = H / Hkv;
+    p.n_qt = (max_seqlen + 2 * kBM - 1) / (2 * kBM);
+    p.BH = num_seqs * H;
+    p.c = scale * kLog2e;
+    p.status = status;
+    p.cu_seqlens = cu_seqlens;
+    p.T = T;
     cudaError_t e = cudaFuncSetAttribute(prefill_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess)

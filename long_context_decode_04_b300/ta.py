@@ -86,9 +86,11 @@ def lib() -> ctypes.CDLL:
         L.ta_combine_workspace_bytes.argtypes = [i, i, i]
         L.ta_combine_workspace_bytes.restype = st
         L.ta_prefill_causal.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        L.ta_prefill_causal_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
         L.ta_last_error.argtypes = []
         L.ta_last_error.restype = ctypes.c_char_p
-        for fn in ("ta_decode", "ta_decode_noalloc", "ta_decode_ex", "ta_decode_paged", "ta_decode_pi", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
+        for fn in ("ta_decode", "ta_decode_noalloc", "ta_decode_ex", "ta_decode_paged", "ta_decode_pi",
+                   "ta_prefill_causal_varlen", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
                    "ta_prefill_causal"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
@@ -309,4 +311,21 @@ def prefill_causal(q, k, v, *, scale=None, out=None, lse=None):
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
     _check(lib().ta_prefill_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, S, D, scale,
                                    _stream(q.device)))
+    return out, lse
+
+
+def prefill_causal_varlen(q, k, v, cu_seqlens, max_seqlen, *, scale=None, out=None, lse=None):
+    """Causal prefill of packed variable-length sequences.  q [T,H,D], k/v
+    [T,Hkv,D] bf16, cu_seqlens [num_seqs+1] int32 (CUDA) -> (out [T,H,D] bf16,
+    lse [H,T] fp32)."""
+    T, H, D = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    _check(lib().ta_prefill_causal_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
+                                          cu_seqlens.numel() - 1, int(max_seqlen), T, H, Hkv, D, scale,
+                                          _stream(q.device)))
     return out, lse

@@ -204,3 +204,29 @@ def decode_pi(q, k, v, scale, window, period, seqlens=None, rows=None, threads=N
             vg[b, :, :len(idx)] = va[b][:, idx]
     glens = np.array([len(x) for x in sets], dtype=np.int32)
     return decode(q, kg, vg, scale, seqlens=glens, rows=rows, threads=threads)
+
+
+def prefill_causal_varlen(q, k, v, cu_seqlens, scale, threads=None):
+    """Causal prefill of packed variable-length sequences: q [T,H,D], k/v
+    [T,Hkv,D]; sequence s is tokens [cu[s], cu[s+1]), and its row i attends
+    keys 0..i of the same sequence.  Each sequence is sliced out (numpy) and
+    given to ``prefill_causal``.  Returns (out [T,H,D], lse [H,T])."""
+    qa, qt = _raw(q)
+    ka, kt = _raw(k)
+    va, vt = _raw(v)
+    T, H, D = qa.shape
+    Hkv = ka.shape[1]
+    cu = [int(x) for x in cu_seqlens]
+    out = np.zeros((T, H, D))
+    lse = np.zeros((H, T))
+    for s in range(len(cu) - 1):
+        a, e = cu[s], cu[s + 1]
+        if e <= a:
+            continue
+        qs = np.ascontiguousarray(qa[a:e].transpose(1, 0, 2))[None]
+        ks = np.ascontiguousarray(ka[a:e].transpose(1, 0, 2))[None]
+        vs = np.ascontiguousarray(va[a:e].transpose(1, 0, 2))[None]
+        o, l = prefill_causal(qs, ks, vs, scale, threads=threads)
+        out[a:e] = o.reshape(H, e - a, D).transpose(1, 0, 2)
+        lse[:, a:e] = l.reshape(H, e - a)
+    return out, lse

@@ -502,4 +502,41 @@ def pin_pi_special_cases():
     assert np.array_equal(got[0], tail[0]) and np.array_equal(got[1], tail[1])
 
 
+# ------------------------------------------------------------ packed variable-length prefill
+
+def pin_varlen_prefill_brute_force():
+    """Packed causal prefill against 50-digit attention of each token over the
+    earlier tokens of its own sequence, looped token by token."""
+    rng = _rng(61)
+    cu = [0, 3, 3, 8, 9]
+    T, H, Hkv, D = cu[-1], 4, 2, 4
+    q = _f32(rng, T, H, D)
+    k = _f32(rng, T, Hkv, D, scale=1.3)
+    v = _f32(rng, T, Hkv, D)
+    out, lse = oracle.prefill_causal_varlen(q, k, v, cu, 0.8)
+    for s in range(len(cu) - 1):
+        for t in range(cu[s], cu[s + 1]):
+            for h in range(H):
+                ref, ref_lse = _mp_attend(q[t, h], k[cu[s]:t + 1, h // 2], v[cu[s]:t + 1, h // 2], 0.8)
+                assert np.max(np.abs(out[t, h] - np.array(ref))) < 1e-13, (s, t, h)
+                assert abs(lse[h, t] - ref_lse) < 1e-13
+
+
+def pin_varlen_prefill_sequences_independent():
+    """A sequence's output depends on its own tokens only."""
+    rng = _rng(62)
+    cu = [0, 6, 13]
+    q = _f32(rng, 13, 2, 4)
+    k = _f32(rng, 13, 1, 4)
+    v = _f32(rng, 13, 1, 4)
+    a = oracle.prefill_causal_varlen(q, k, v, cu, 0.5)
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    q2[6:] += 3.0
+    k2[6:] *= -2.0
+    v2[6:] += 1.0
+    b = oracle.prefill_causal_varlen(q2, k2, v2, cu, 0.5)
+    assert np.array_equal(a[0][:6], b[0][:6]) and np.array_equal(a[1][:, :6], b[1][:, :6])
+    assert not np.array_equal(a[0][6:], b[0][6:])
+
+
 ALL_PINS = [f for name, f in sorted(globals().items()) if name.startswith("pin_") and callable(f)]

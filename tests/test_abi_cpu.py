@@ -175,3 +175,22 @@ def test_pi_key_bound_covers_every_length(S, window, period):
     bound = min(S, min(window + 1, S) + -(-max(0, S - 1 - window) // period))
     for L in sorted(x for x in {1, 2, S // 3, S // 2, S - 1, S} if 1 <= x <= S):
         assert len(oracle.pi_key_set(L, window, period)) <= bound
+
+
+def test_varlen_prefill_rejects_bad_arguments():
+    L = ta.lib()
+    vp = ctypes.c_void_p
+    f = ctypes.c_float(0.1)
+    ok = dict(q=vp(0x1000), k=vp(0x2000), v=vp(0x3000), out=vp(0x4000), lse=None, cu=vp(0x5000))
+    def call(**kw):
+        a = dict(ok, **{k2: v2 for k2, v2 in kw.items() if k2 in ok})
+        n = dict(num_seqs=2, max_seqlen=128, total=256, H=8, Hkv=2, D=128)
+        n.update({k2: v2 for k2, v2 in kw.items() if k2 in n})
+        return L.ta_prefill_causal_varlen(a["q"], a["k"], a["v"], a["out"], a["lse"], a["cu"], n["num_seqs"],
+                                          n["max_seqlen"], n["total"], n["H"], n["Hkv"], n["D"], f, None)
+    assert call(cu=None) == ta.TA_ERR_INVALID_ARG
+    assert call(num_seqs=0) == ta.TA_ERR_INVALID_ARG
+    assert call(H=6, Hkv=4) == ta.TA_ERR_INVALID_ARG
+    assert call(D=64) == ta.TA_ERR_UNSUPPORTED
+    assert call(q=vp(0x1008)) == ta.TA_ERR_INVALID_ARG
+    assert call(cu=vp(0x5002)) == ta.TA_ERR_INVALID_ARG

@@ -143,3 +143,32 @@ def test_pi_mutation_is_caught(monkeypatch, name):
         except (AssertionError, ValueError, IndexError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught mutation {name}"
+
+
+VARLEN_MUTATIONS = {
+    "starts_one_token_early": ("a, e = cu[s], cu[s + 1]", "a, e = max(cu[s] - 1, 0), cu[s + 1]"),
+    "kv_heads_not_transposed": ("ks = np.ascontiguousarray(ka[a:e].transpose(1, 0, 2))[None]",
+                                "ks = np.ascontiguousarray(ka[a:e].reshape(Hkv, e - a, D))[None]"),
+    "lse_rows_swapped": ("lse[:, a:e] = l.reshape(H, e - a)", "lse[:, a:e] = l.reshape(e - a, H).T"),
+    "output_not_transposed_back": ("out[a:e] = o.reshape(H, e - a, D).transpose(1, 0, 2)",
+                                   "out[a:e] = o.reshape(e - a, H, D)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(VARLEN_MUTATIONS))
+def test_varlen_prefill_mutation_is_caught(monkeypatch, name):
+    import inspect
+    import textwrap
+    old, new = VARLEN_MUTATIONS[name]
+    src = textwrap.dedent(inspect.getsource(oracle.prefill_causal_varlen))
+    assert src.count(old) >= 1, f"mutation {name}: pattern not found"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, "prefill_causal_varlen", ns["prefill_causal_varlen"])
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutation {name}"
