@@ -198,6 +198,76 @@ def measure_varlen(ta, synth, accounting, peaks, dev, reps=20):
     return res
 
 
+def measure_pi(ta, accounting, peaks, dev, w, q, k, v, window=4096, period=64, reps=20):
+    """Decode of the 128K-token workload over the pi-Attention key set (the last
+    `window` keys plus every `period`-th key before them): median of `reps`
+    graph replays, KV bytes of the attended keys only."""
+    import torch
+    i = w.S - 1
+    w0 = max(0, i - window)
+    n_keys = (i - w0 + 1) + sum(1 for j in range(i - period, -1, -period) if j < w0)
+    kv_bytes = accounting.decode_kv_bytes(w.B, w.Hkv, w.D, n_keys, 2)
+    ws = ta.decode_pi_workspace(w.B, w.Hq, w.Hkv, w.S, w.D, window, period, device=dev)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    fn = lambda: ta.decode_pi(q, k, v, window, period, scale=w.scale, workspace=ws, out=out, lse=lse)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = sorted(1e3 * a.elapsed_time(b) for a, b in ev)[reps // 2]
+    gbs = kv_bytes / (us / 1e6) / 1e9
+    return {"workload": f"B=1, Hq=32, Hkv=8, D=128, S={w.S}, window={window}, period={period}",
+            "attended_keys": n_keys, "attended_kv_bytes": kv_bytes, "us": round(us, 2), "gbs": round(gbs, 1),
+            "frac": round(gbs / peaks["hbm_gbs"], 4)}
+
+
+def measure_prefill_varlen(ta, synth, peaks, dev, reps=5):
+    """Causal prefill of 8 packed sequences with lengths uniform in [1024, 16384]
+    (seeded), 32 heads / 8 KV heads: median of `reps` graph replays."""
+    import numpy as np
+    import torch
+    rng = np.random.Generator(np.random.PCG64(1005))
+    lens = [int(x) for x in rng.integers(1024, 16384, size=8, endpoint=True)]
+    T, H, Hkv, D = sum(lens), 32, 8, 128
+    w = synth.Workload("packed_prefill", 5, "prefill", 1, H, Hkv, T, D, "bf16")
+    x = synth.make_inputs(w)
+    q = x["q"][0].transpose(0, 1).contiguous().to(dev)
+    k = x["k"][0].transpose(0, 1).contiguous().to(dev)
+    v = x["v"][0].transpose(0, 1).contiguous().to(dev)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    flops = sum(4 * D * H * (L * (L + 1) // 2) for L in lens)
+    fn = lambda: ta.prefill_causal_varlen(q, k, v, cu, max(lens), scale=w.scale, out=out, lse=lse)
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in ev)[reps // 2]
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": f"8 packed sequences, lengths {lens}, H=32, Hkv=8, D=128, causal, bf16",
+            "flops": flops, "ms": round(ms, 3), "tflops": round(tf, 1),
+            "frac_sustained": round(tf / peaks["bf16_tflops_sustained"], 4)}
+
+
 def cpu_oracle_decode(x, rows, threads):
     import oracle
     t = time.perf_counter()
@@ -390,6 +460,8 @@ def main():
 
     # ---------------- the step beside config 3: variable lengths, contiguous and paged
     extra = None if args.no_extra else measure_varlen(ta, synth, accounting, peaks, dev)
+    pi_fig = None if args.no_extra else measure_pi(ta, accounting, peaks, dev, w, q, k, v)
+    pvar_fig = None if (args.no_extra or not do_prefill) else measure_prefill_varlen(ta, synth, peaks, dev)
 
     # ---------------- end to end through the public single call, host buffers
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
@@ -477,6 +549,8 @@ def main():
                      "peak_source": peaks["source"] + " (copy bandwidth)",
                      "avg_launch_us": round(1e3 * dec_avg, 3), "launches_per_token": decode_launches},
         "varlen_b16": extra,
+        "pi_attention": pi_fig,
+        "prefill_varlen": pvar_fig,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "e2e": {"value": round(world * kv_bytes * e2e_steps / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
