@@ -169,6 +169,21 @@ ta_status ta_decode_noalloc(const void *q, const void *k, const void *v, void *o
 ta_status ta_decode_ex(const ta_decode_params *p);
 
 /*
+ * Split-KV decode over an FP8 (E4M3) KV cache: half the bytes of a bf16
+ * cache (the ThriftAttention page, hyperion-consulting.io, "the rise of
+ * FP4" and the COMPUTE layer: low-precision KV-cache compression with
+ * higher-precision arithmetic).
+ *   k, v [B, Hkv, S, D] E4M3 bytes (sign, 4 exponent bits with bias 7, 3
+ *   mantissa bits; 0x7f / 0xff are NaN); the cache value of (b, kv head) is
+ *   e4m3 * k_scale[b * Hkv + kvh] (resp. v_scale), fp32 on the device, or
+ *   1 when the pointer is NULL.  q bf16 (p->in_dtype = TA_BF16), output
+ *   bf16 or fp32, fp32 accumulation.  Everything else as ta_decode_ex.
+ *   Supported: D = 128, G in {1, 2, 4}.  Queries are used as f16 values
+ *   (exact for bf16 values of magnitude in [2^-14, 65504]).
+ */
+ta_status ta_decode_fp8(const ta_decode_params *p, const float *k_scale, const float *v_scale);
+
+/*
  * Split-KV decode over the key set of pi-Attention (pi-Attention explainer,
  * gist.science/ja/paper/2511.10696, technical summary section 2A): the
  * query of each sequence, the newest token i = L_b - 1, attends

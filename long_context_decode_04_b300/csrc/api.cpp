@@ -189,7 +189,8 @@ namespace {
 // The decode of ta_decode_ex, reading K/V through a block table when one is
 // given (block_table != nullptr; p->k, p->v are then the page pools).
 ta_status decode_impl(const ta_decode_params *p, const int32_t *block_table, int page_size, int pages_per_seq,
-                      int num_pages, int pi_window = 0, int pi_period = 0)
+                      int num_pages, int pi_window = 0, int pi_period = 0, bool kv_fp8 = false,
+                      const float *k_scale = nullptr, const float *v_scale = nullptr)
 {
     ta_status s;
     ta_decode_plan plan;
@@ -220,6 +221,9 @@ ta_status decode_impl(const ta_decode_params *p, const int32_t *block_table, int
     a.num_pages = num_pages;
     a.pi_window = pi_window;
     a.pi_period = pi_period;
+    a.kv_fp8 = kv_fp8;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.q = p->q;
     a.k = p->k;
     a.v = p->v;
@@ -275,6 +279,20 @@ ta_status ta_decode_ex(const ta_decode_params *p)
     if (s != TA_OK)
         return s;
     return decode_impl(p, nullptr, 0, 0, 0);
+}
+
+ta_status ta_decode_fp8(const ta_decode_params *p, const float *k_scale, const float *v_scale)
+{
+    ta_status s = validate_decode(p);
+    if (s != TA_OK)
+        return s;
+    if (p->in_dtype != TA_BF16)
+        return fail(TA_ERR_INVALID_ARG, "fp8 decode takes bf16 queries (in_dtype = TA_BF16)");
+    if (p->D != 128)
+        return fail(TA_ERR_UNSUPPORTED, "fp8 decode supports head dim D = 128");
+    if ((k_scale && !aligned(k_scale, 4)) || (v_scale && !aligned(v_scale, 4)))
+        return fail(TA_ERR_INVALID_ARG, "k_scale and v_scale must be 4-byte aligned");
+    return decode_impl(p, nullptr, 0, 0, 0, 0, 0, true, k_scale, v_scale);
 }
 
 ta_status ta_decode_pi(const ta_decode_params *p, int window, int period)
@@ -385,6 +403,8 @@ ta_status ta_decode_partials(const ta_decode_params *p, float *m, float *l, floa
     a.block_table = nullptr;
     a.page_size = a.pages_per_seq = a.num_pages = 0;
     a.pi_window = a.pi_period = 0;
+    a.kv_fp8 = false;
+    a.k_scale = a.v_scale = nullptr;
     a.stream = static_cast<cudaStream_t>(p->stream);
     a.status = static_cast<int32_t *>(ws);
     a.counters = nullptr;

@@ -52,6 +52,7 @@
 //   * Every wait is bounded (kWaitLimitNs); on expiry the kernel records
 //     TA_DEVERR_TIMEOUT, stops, and drains its own outstanding copies.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include <type_traits>
 
@@ -100,6 +101,8 @@ struct DecodeParams {
     // the window [max(0, i - pi_window), i] and the keys i - m * pi_period
     // (m >= 1) before it; the chunks cut the ascending list of those keys.
     int pi_window, pi_period;
+    // fp8 K/V: per (sequence, KV head) dequantisation factors, or nullptr (1)
+    const float *k_scale, *v_scale;
     // pi_tma: K and V of each (sequence, KV head) seen as rows of
     // pi_period keys, [B*Hkv, ceil(S / period), period * D] with a box of
     // D x TILE: the box at x = r * D, y = m gathers keys r + (m + t) * period,
@@ -117,6 +120,10 @@ struct Elem<float> {
 template <>
 struct Elem<__nv_bfloat16> {
     static constexpr int kPerChunk = 8;
+};
+template <>
+struct Elem<__nv_fp8_e4m3> {
+    static constexpr int kPerChunk = 16;
 };
 
 __device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
@@ -181,6 +188,39 @@ struct Lay {
     }
 };
 
+// acc += sum of the 4 products of two packed f16 pairs a, b (fp32 accumulator).
+__device__ __forceinline__ void fma_f16(float &acc, uint32_t a, uint32_t b)
+{
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+}
+
+// Two e4m3 values (low byte first) to a packed f16 pair (exact: e4m3 is a
+// subset of f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(x));
+    return r;
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t w)
+{
+    float2 r;
+    asm("{\n\t.reg .f16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.f32.f16 %0, lo;\n\t"
+        "cvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(w));
+    return r;
+}
+
 // The G weights of one key from shared memory (one vector load).
 template <int G>
 __device__ __forceinline__ void load_weights(const float *src, float (&pk)[G])
@@ -220,6 +260,18 @@ __device__ __forceinline__ void load_v_slice(const unsigned char *src, float (&v
     }
 }
 template <int DPL>
+__device__ __forceinline__ void load_v_slice(const unsigned char *src, float (&vf)[DPL], __nv_fp8_e4m3 *)
+{
+    static_assert(DPL == 4, "fp8 rows are 128 bytes: 4 dims a lane");
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
+    const float2 a = f16x2_to_float2(e4m3x2_to_f16x2((uint16_t)(w & 0xffffu)));
+    const float2 b = f16x2_to_float2(e4m3x2_to_f16x2((uint16_t)(w >> 16)));
+    vf[0] = a.x;
+    vf[1] = a.y;
+    vf[2] = b.x;
+    vf[3] = b.y;
+}
+template <int DPL>
 __device__ __forceinline__ void load_v_slice(const unsigned char *src, float (&vf)[DPL], float *)
 {
     if constexpr (DPL == 4) {
@@ -240,7 +292,9 @@ struct Cfg {
     static constexpr int RB = D * (int)sizeof(KV);  // bytes per K or V row
     static constexpr int NCH = RB / 128;            // 16-byte chunks per lane per row (8 lanes per key)
     static constexpr int EPC = Elem<KV>::kPerChunk; // elements per chunk
-    static constexpr int QPL_W = NCH * 4;           // 32-bit q words held by a lane per head
+    // 32-bit q words a lane holds per head: bf16 pairs or fp32 values as
+    // loaded; for fp8 K/V, f16 pairs (16 dims per chunk)
+    static constexpr int QPL_W = NCH * (sizeof(KV) == 1 ? 8 : 4);
     static constexpr int DPL = D / 32;              // output dims owned by a lane (PV)
     static constexpr int VB = DPL * (int)sizeof(KV);// V bytes read by a lane per key
     static constexpr int PB = (G * (DPL + 1) > 24) ? 2 : 4;  // keys per PV load batch (register budget)
@@ -500,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     uint32_t phase = 0;
     uint32_t merge_phase = 0, ticket_phase = 0, fm_phase = 0;
     int b = 0, kvh = 0, split = 0, unit = 0;
+    float qs = p.qscale;  // scale * log2(e), times the key dequantisation factor
     float *slot = pbuf + warp * (C::KPW * G);  // this warp's weights [KPW][G]
     int my_kidx[L::NVL], my_h[L::NVL];          // key (within the warp's KPW) and head of value j
 #pragma unroll
@@ -520,16 +575,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
             split = d.item - unit * p.n_split;
             b = unit / p.Hkv;
             kvh = unit - b * p.Hkv;
+            qs = p.k_scale ? p.qscale * p.k_scale[unit] : p.qscale;
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const KV *qrow = static_cast<const KV *>(p.q) + ((size_t)b * p.Hq + (size_t)kvh * G + h) * D;
+                if constexpr (sizeof(KV) == 1) {
+                    // bf16 q, as f16 pairs for the mixed-precision products
+                    // with f16-widened e4m3 keys
+                    const __nv_bfloat16 *qrow =
+                        static_cast<const __nv_bfloat16 *>(p.q) + ((size_t)b * p.Hq + (size_t)kvh * G + h) * D;
 #pragma unroll
-                for (int i = 0; i < C::NCH; ++i) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(qrow + (t + 8 * i) * C::EPC);
-                    qw[h][4 * i + 0] = raw.x;
-                    qw[h][4 * i + 1] = raw.y;
-                    qw[h][4 * i + 2] = raw.z;
-                    qw[h][4 * i + 3] = raw.w;
+                    for (int i = 0; i < C::NCH; ++i) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(qrow + (t + 8 * i) * C::EPC);
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const uint4 raw = src[u];
+                            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                uint32_t hv;
+                                asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hv) : "f"(bf16_hi(wv[w])), "f"(bf16_lo(wv[w])));
+                                qw[h][8 * i + 4 * u + w] = hv;
+                            }
+                        }
+                    }
+                } else {
+                    const KV *qrow = static_cast<const KV *>(p.q) + ((size_t)b * p.Hq + (size_t)kvh * G + h) * D;
+#pragma unroll
+                    for (int i = 0; i < C::NCH; ++i) {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(qrow + (t + 8 * i) * C::EPC);
+                        qw[h][4 * i + 0] = raw.x;
+                        qw[h][4 * i + 1] = raw.y;
+                        qw[h][4 * i + 2] = raw.z;
+                        qw[h][4 * i + 3] = raw.w;
+                    }
                 }
 #pragma unroll
                 for (int e = 0; e < C::DPL; ++e)
@@ -564,16 +642,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
                         const uint4 kr =
                             *reinterpret_cast<const uint4 *>(Ks + (kbeg + kidx) * C::RB + (t + 8 * i) * 16);
                         const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
-#pragma unroll
-                        for (int h = 0; h < G; ++h)
+                        if constexpr (sizeof(KV) == 1) {
+                            // 16 e4m3 keys -> 8 f16 pairs, once for all heads
+                            uint32_t kh[8];
 #pragma unroll
                             for (int w = 0; w < 4; ++w) {
-                                if constexpr (sizeof(KV) == 2)
-                                    fma_bf16(v[kk * G + h], qw[h][4 * i + w], kw[w]);
-                                else
-                                    v[kk * G + h] = fmaf(__uint_as_float(qw[h][4 * i + w]), __uint_as_float(kw[w]),
-                                                         v[kk * G + h]);
+                                kh[2 * w] = e4m3x2_to_f16x2((uint16_t)(kw[w] & 0xffffu));
+                                kh[2 * w + 1] = e4m3x2_to_f16x2((uint16_t)(kw[w] >> 16));
                             }
+#pragma unroll
+                            for (int h = 0; h < G; ++h)
+#pragma unroll
+                                for (int w = 0; w < 8; ++w)
+                                    fma_f16(v[kk * G + h], qw[h][8 * i + w], kh[w]);
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < G; ++h)
+#pragma unroll
+                                for (int w = 0; w < 4; ++w) {
+                                    if constexpr (sizeof(KV) == 2)
+                                        fma_bf16(v[kk * G + h], qw[h][4 * i + w], kw[w]);
+                                    else
+                                        v[kk * G + h] = fmaf(__uint_as_float(qw[h][4 * i + w]),
+                                                             __uint_as_float(kw[w]), v[kk * G + h]);
+                                }
+                        }
                     }
                 }
             }
@@ -599,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
             bool need = false;
 #pragma unroll
             for (int j = 0; j < L::NVL; ++j) {
-                sc[j] = (FULL || my_kidx[j] < nvalid) ? v[j] * p.qscale : -INFINITY;  // log2 units
+                sc[j] = (FULL || my_kidx[j] < nvalid) ? v[j] * qs : -INFINITY;  // log2 units
                 need |= sc[j] > m_run[j] + kRescaleLog2;
             }
             // ---- lazy rescale of the running references (warp vote)
@@ -684,6 +777,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
             for (int mask = 1; mask < 32; mask <<= 1)
                 if (L::preserves_head(mask))
                     l_run[j] += __shfl_xor_sync(kFull, l_run[j], mask);
+        }
+        if (p.v_scale) {
+            const float vs = p.v_scale[unit];  // value dequantisation factor
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < C::DPL; ++e)
+                    o[h][e] *= vs;
         }
         ok = mbar_wait_bounded(merge_out, merge_phase ^ 1, abort_flag);
         if (!__all_sync(kFull, ok))
@@ -834,6 +935,14 @@ cudaError_t launch_typed(const DecodeLaunch &a, const DecodeParams &p)
 template <int D, int G>
 cudaError_t dispatch_types(const DecodeLaunch &a, const DecodeParams &p)
 {
+    if (a.kv_fp8) {
+        if constexpr (D == 128 && G <= 4) {
+            if (a.out_dtype == TA_BF16)
+                return launch_typed<D, G, __nv_fp8_e4m3, __nv_bfloat16>(a, p);
+            return launch_typed<D, G, __nv_fp8_e4m3, float>(a, p);
+        }
+        return cudaErrorInvalidValue;
+    }
     if (a.in_dtype == TA_BF16) {
         if (a.out_dtype == TA_BF16)
             return launch_typed<D, G, __nv_bfloat16, __nv_bfloat16>(a, p);
@@ -876,6 +985,8 @@ cudaError_t launch_decode(const DecodeLaunch &a)
     p.page_size = a.page_size;
     p.pages_per_seq = a.pages_per_seq;
     p.num_pages = a.num_pages;
+    p.k_scale = a.k_scale;
+    p.v_scale = a.v_scale;
     p.pi_window = a.pi_window;
     p.pi_period = a.pi_period;
     p.pi_tma = 0;

@@ -40,6 +40,8 @@ struct DecodeLaunch {
     const int32_t *block_table;        // paged KV cache, or nullptr (contiguous [B, Hkv, S, D])
     int page_size, pages_per_seq, num_pages;
     int pi_window, pi_period;          // pi-Attention key set (period 0: every key)
+    bool kv_fp8;                       // K/V are e4m3 bytes (q bf16), dequantised by
+    const float *k_scale, *v_scale;    //   per (sequence, KV head) factors
     cudaStream_t stream;
 };
 

@@ -199,3 +199,16 @@ def to_pages(k: torch.Tensor, v: torch.Tensor, seqlens, page_size: int, *, seed:
                 phys = spare[pg % len(spare)]
             table[b, pg] = phys
     return kp, vp, table
+
+
+def to_e4m3(x: torch.Tensor):
+    """Quantise K or V [B, Hkv, S, D] to FP8 E4M3 with one scale per (sequence,
+    KV head): scale = max|x| / 448 (the largest finite E4M3), bits = RNE of
+    x / scale (torch's float8_e4m3fn cast).  Returns (uint8 bit patterns,
+    float32 scales [B*Hkv]).  Input generation only."""
+    B, Hkv = x.shape[:2]
+    xf = x.float()
+    amax = xf.abs().amax(dim=(2, 3)).clamp_min(1e-30)
+    sc = (amax / 448.0).to(torch.float32)
+    bits = (xf / sc.view(B, Hkv, 1, 1)).to(torch.float8_e4m3fn).view(torch.uint8)
+    return bits.contiguous(), sc.reshape(-1).contiguous()

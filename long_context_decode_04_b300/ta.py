@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
         L.ta_decode_ex.argtypes = [ctypes.POINTER(DecodeParams)]
         L.ta_decode_paged.argtypes = [ctypes.POINTER(PagedDecodeParams)]
         L.ta_decode_pi.argtypes = [ctypes.POINTER(DecodeParams), i, i]
+        L.ta_decode_fp8.argtypes = [ctypes.POINTER(DecodeParams), vp, vp]
         L.ta_decode_pi_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i, i]
         L.ta_decode_pi_workspace_bytes.restype = st
         L.ta_decode_partials.argtypes = [ctypes.POINTER(DecodeParams), vp, vp, vp]
@@ -89,7 +90,7 @@ def lib() -> ctypes.CDLL:
         L.ta_prefill_causal_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
         L.ta_last_error.argtypes = []
         L.ta_last_error.restype = ctypes.c_char_p
-        for fn in ("ta_decode", "ta_decode_noalloc", "ta_decode_ex", "ta_decode_paged", "ta_decode_pi",
+        for fn in ("ta_decode", "ta_decode_noalloc", "ta_decode_ex", "ta_decode_paged", "ta_decode_pi", "ta_decode_fp8",
                    "ta_prefill_causal_varlen", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
                    "ta_prefill_causal"):
             getattr(L, fn).restype = ctypes.c_int
@@ -177,6 +178,22 @@ def decode_pi(q, k, v, window, period, *, seqlens=None, scale=None, out_dtype=No
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     p = _params(q, k, v, seqlens, scale, chunk, n_split, workspace, out=out, lse=lse, out_dtype=out.dtype)
     _check(lib().ta_decode_pi(ctypes.byref(p), int(window), int(period)))
+    return out, lse
+
+
+def decode_fp8(q, k8, v8, *, k_scale=None, v_scale=None, seqlens=None, scale=None, out_dtype=None, chunk=0,
+               n_split=0, workspace=None, out=None, lse=None):
+    """Decode over an E4M3 KV cache.  q [B,Hq,D] bf16; k8/v8 [B,Hkv,S,D] uint8
+    (E4M3 bit patterns); k_scale/v_scale [B*Hkv] fp32 or None.  Returns
+    (out, lse)."""
+    B, Hq, D = q.shape
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    p = _params(q, k8, v8, seqlens, scale, chunk, n_split, workspace, out=out, lse=lse, out_dtype=out.dtype)
+    _check(lib().ta_decode_fp8(ctypes.byref(p), _ptr(k_scale), _ptr(v_scale)))
     return out, lse
 
 

@@ -16,7 +16,7 @@ import numpy as np
 
 from . import build as _build
 
-F32, BF16 = 0, 1
+F32, BF16, F64 = 0, 1, 2
 
 _lib = None
 
@@ -59,6 +59,8 @@ def _raw(t):
     a = np.ascontiguousarray(t)
     if a.dtype == np.float32:
         return a, F32
+    if a.dtype == np.float64:
+        return a, F64
     if a.dtype == np.uint16:  # raw bf16 bits
         return a, BF16
     raise TypeError(f"oracle takes float32 or raw-bf16 uint16 arrays, got {a.dtype}")
@@ -230,3 +232,32 @@ def prefill_causal_varlen(q, k, v, cu_seqlens, scale, threads=None):
         out[a:e] = o.reshape(H, e - a, D).transpose(1, 0, 2)
         lse[:, a:e] = l.reshape(H, e - a)
     return out, lse
+
+
+def e4m3_to_float(bits):
+    """Values of FP8 E4M3 bit patterns (uint8): sign, 4 exponent bits with
+    bias 7, 3 mantissa bits; exponent 0 is subnormal (m/8 * 2^-6); S.1111.111
+    is NaN and there is no infinity.  Written from the format definition."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    s = (b >> 7) & 1
+    e = (b >> 3) & 15
+    m = b & 7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(s == 1, -mag, mag)
+
+
+def decode_fp8(q, k8, v8, k_scale, v_scale, scale, seqlens=None, rows=None, threads=None):
+    """Decode over an E4M3 KV cache: the cache is dequantised first (value =
+    e4m3 * scale of its (sequence, KV head), in float64, exact) and ``decode``
+    does the rest.  k8/v8 [B,Hkv,S,D] uint8 bit patterns; k_scale/v_scale
+    [B*Hkv] or None (1)."""
+    kb = np.asarray(k8.cpu().numpy() if hasattr(k8, "cpu") else k8, dtype=np.uint8)
+    vb = np.asarray(v8.cpu().numpy() if hasattr(v8, "cpu") else v8, dtype=np.uint8)
+    B, Hkv = kb.shape[:2]
+    ks = np.ones(B * Hkv) if k_scale is None else np.asarray(k_scale, dtype=np.float64).reshape(-1)
+    vs = np.ones(B * Hkv) if v_scale is None else np.asarray(v_scale, dtype=np.float64).reshape(-1)
+    kd = e4m3_to_float(kb) * ks.reshape(B, Hkv, 1, 1)
+    vd = e4m3_to_float(vb) * vs.reshape(B, Hkv, 1, 1)
+    return decode(q, np.ascontiguousarray(kd), np.ascontiguousarray(vd), scale, seqlens=seqlens, rows=rows,
+                  threads=threads)

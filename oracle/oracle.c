@@ -52,12 +52,15 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F64 = 2 };
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = 1, ORACLE_NO_MEMORY = 2 };
 
-/* Widen element i of a bf16 (raw bits) or fp32 array to double. */
+/* Widen element i of a bf16 (raw bits), fp32 or fp64 array to double
+ * (fp64 carries already-widened values, e.g. a dequantised cache). */
 static double widen(const void *base, int dtype, size_t i)
 {
+    if (dtype == ORACLE_F64)
+        return ((const double *)base)[i];
     if (dtype == ORACLE_F32)
         return (double)((const float *)base)[i];
     uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;

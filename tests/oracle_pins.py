@@ -539,4 +539,59 @@ def pin_varlen_prefill_sequences_independent():
     assert not np.array_equal(a[0][6:], b[0][6:])
 
 
+# ------------------------------------------------------------ FP8 (E4M3) KV cache
+
+def pin_e4m3_values_match_the_library():
+    """All 256 E4M3 bit patterns decode as torch's float8_e4m3fn does."""
+    import torch
+    bits = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_to_float(bits)
+    ref = torch.from_numpy(bits).view(torch.float8_e4m3fn).float().double().numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert np.array_equal(mine[~np.isnan(mine)], ref[~np.isnan(ref)])
+
+
+def pin_fp8_brute_force():
+    """FP8 decode against 50-digit attention over keys and values dequantised
+    element by element (sign * 2^(e-7) * (1 + m/8), or 2^-6 * m/8) times the
+    (sequence, KV head) scale."""
+    rng = _rng(71)
+    B, Hkv, G, S, D = 2, 2, 2, 9, 4
+    k8 = rng.integers(0, 256, size=(B, Hkv, S, D)).astype(np.uint8)
+    v8 = rng.integers(0, 256, size=(B, Hkv, S, D)).astype(np.uint8)
+    k8[(k8 & 0x7f) == 0x7f] = 0x38  # no NaN patterns
+    v8[(v8 & 0x7f) == 0x7f] = 0x40
+    k8 = np.where((k8 >> 3) & 15 >= 13, k8 & 0x87, k8).astype(np.uint8)  # keep logits moderate
+    ks = rng.uniform(0.01, 0.05, B * Hkv)
+    vs = rng.uniform(0.5, 2.0, B * Hkv)
+    q = _f32(rng, B, Hkv * G, D)
+
+    def val(bt):
+        bt = int(bt)
+        sgn = -1 if bt >> 7 else 1
+        e, m = (bt >> 3) & 15, bt & 7
+        return sgn * (mpmath.mpf(m) / 8 * mpmath.mpf(2) ** -6 if e == 0 else (1 + mpmath.mpf(m) / 8) * mpmath.mpf(2) ** (e - 7))
+
+    out, lse = oracle.decode_fp8(q, k8, v8, ks, vs, 0.7)
+    for b in range(B):
+        for h in range(Hkv * G):
+            u = b * Hkv + h // G
+            kk = np.array([[float(val(x) * ks[u]) for x in row] for row in k8[b, h // G]])
+            vv = np.array([[float(val(x) * vs[u]) for x in row] for row in v8[b, h // G]])
+            ref, ref_lse = _mp_attend(q[b, h], kk, vv, 0.7)
+            assert np.max(np.abs(out[b * Hkv * G + h] - np.array(ref))) < 1e-12 * max(1.0, float(np.max(np.abs(vv))))
+            assert abs(lse[b * Hkv * G + h] - ref_lse) < 1e-12
+
+
+def pin_fp8_scales_are_linear():
+    """A key scale multiplies the logits, a value scale the output."""
+    rng = _rng(72)
+    k8 = rng.integers(0, 0x60, size=(1, 1, 12, 8)).astype(np.uint8)
+    v8 = rng.integers(0, 0x70, size=(1, 1, 12, 8)).astype(np.uint8)
+    q = _f32(rng, 1, 2, 8)
+    a = oracle.decode_fp8(q, k8, v8, [0.02], [1.0], 0.5)
+    b_ = oracle.decode_fp8(q, k8, v8, [0.01], [3.0], 1.0)
+    assert np.max(np.abs(3.0 * a[0] - b_[0])) < 1e-12 and np.max(np.abs(a[1] - b_[1])) < 1e-12
+
+
 ALL_PINS = [f for name, f in sorted(globals().items()) if name.startswith("pin_") and callable(f)]

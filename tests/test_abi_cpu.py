@@ -194,3 +194,15 @@ def test_varlen_prefill_rejects_bad_arguments():
     assert call(D=64) == ta.TA_ERR_UNSUPPORTED
     assert call(q=vp(0x1008)) == ta.TA_ERR_INVALID_ARG
     assert call(cu=vp(0x5002)) == ta.TA_ERR_INVALID_ARG
+
+
+def test_fp8_decode_rejects_unsupported_shapes():
+    base = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, B=1, Hq=8, Hkv=2, S=64, D=128,
+                scale=0.1, in_dtype=ta.TA_BF16, out_dtype=ta.TA_BF16)
+    L = ta.lib()
+    p = ta.DecodeParams(**dict(base, D=64))
+    assert L.ta_decode_fp8(ctypes.byref(p), None, None) == ta.TA_ERR_UNSUPPORTED
+    p = ta.DecodeParams(**dict(base, in_dtype=ta.TA_F32, out_dtype=ta.TA_F32))
+    assert L.ta_decode_fp8(ctypes.byref(p), None, None) == ta.TA_ERR_INVALID_ARG
+    p = ta.DecodeParams(**base)
+    assert L.ta_decode_fp8(ctypes.byref(p), ctypes.c_void_p(0x6002), None) == ta.TA_ERR_INVALID_ARG

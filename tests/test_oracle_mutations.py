@@ -172,3 +172,33 @@ def test_varlen_prefill_mutation_is_caught(monkeypatch, name):
         except (AssertionError, ValueError, IndexError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught mutation {name}"
+
+
+FP8_MUTATIONS = {
+    ("e4m3_to_float", "bias_8"): ("np.exp2(e - 7.0)", "np.exp2(e - 8.0)"),
+    ("e4m3_to_float", "subnormal_as_normal"): ("m / 8.0 * 2.0 ** -6", "(1.0 + m / 8.0) * 2.0 ** -7"),
+    ("e4m3_to_float", "sign_ignored"): ("return np.where(s == 1, -mag, mag)", "return mag"),
+    ("decode_fp8", "v_scale_dropped"): ("vd = e4m3_to_float(vb) * vs.reshape(B, Hkv, 1, 1)", "vd = e4m3_to_float(vb)"),
+    ("decode_fp8", "k_scale_per_wrong_unit"): ("kd = e4m3_to_float(kb) * ks.reshape(B, Hkv, 1, 1)",
+                                               "kd = e4m3_to_float(kb) * ks[::-1].reshape(B, Hkv, 1, 1)"),
+}
+
+
+@pytest.mark.parametrize("key", sorted(FP8_MUTATIONS), ids=lambda k: "-".join(k))
+def test_fp8_mutation_is_caught(monkeypatch, key):
+    import inspect
+    import textwrap
+    fn_name, _ = key
+    old, new = FP8_MUTATIONS[key]
+    src = textwrap.dedent(inspect.getsource(getattr(oracle, fn_name)))
+    assert src.count(old) >= 1, f"mutation {key}: pattern not found"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant {key}>", "exec"), ns)
+    monkeypatch.setattr(oracle, fn_name, ns[fn_name])
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutation {key}"
