@@ -231,6 +231,39 @@ def measure_pi(ta, accounting, peaks, dev, w, q, k, v, window=4096, period=64, r
             "frac": round(gbs / peaks["hbm_gbs"], 4)}
 
 
+def measure_fp8(ta, synth, accounting, peaks, dev, w, x, reps=20):
+    """Decode of the 128K-token workload with its K/V quantised to E4M3 (one
+    factor per KV head): median of `reps` graph replays, KV bytes read (1 byte
+    an element)."""
+    import torch
+    k8, ks = synth.to_e4m3(x["k"])
+    v8, vs = synth.to_e4m3(x["v"])
+    q = x["q"].to(dev)
+    k8, v8, ks, vs = k8.to(dev), v8.to(dev), ks.to(dev), vs.to(dev)
+    kv_bytes = accounting.decode_kv_bytes(w.B, w.Hkv, w.D, w.S, 1)
+    ws = ta.decode_workspace(w.B, w.Hq, w.Hkv, w.S, w.D, device=dev)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    fn = lambda: ta.decode_fp8(q, k8, v8, k_scale=ks, v_scale=vs, scale=w.scale, workspace=ws, out=out, lse=lse)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = sorted(1e3 * a.elapsed_time(b) for a, b in ev)[reps // 2]
+    gbs = kv_bytes / (us / 1e6) / 1e9
+    return {"workload": "B=1, Hq=32, Hkv=8, D=128, S=131072, K/V E4M3 with per-KV-head factors, bf16 q",
+            "kv_bytes": kv_bytes, "us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
+
+
 def measure_prefill_varlen(ta, synth, peaks, dev, reps=5):
     """Causal prefill of 8 packed sequences with lengths uniform in [1024, 16384]
     (seeded), 32 heads / 8 KV heads: median of `reps` graph replays."""
@@ -461,6 +494,7 @@ def main():
     # ---------------- the step beside config 3: variable lengths, contiguous and paged
     extra = None if args.no_extra else measure_varlen(ta, synth, accounting, peaks, dev)
     pi_fig = None if args.no_extra else measure_pi(ta, accounting, peaks, dev, w, q, k, v)
+    fp8_fig = None if args.no_extra else measure_fp8(ta, synth, accounting, peaks, dev, w, x)
     pvar_fig = None if (args.no_extra or not do_prefill) else measure_prefill_varlen(ta, synth, peaks, dev)
 
     # ---------------- end to end through the public single call, host buffers
@@ -550,6 +584,7 @@ def main():
                      "avg_launch_us": round(1e3 * dec_avg, 3), "launches_per_token": decode_launches},
         "varlen_b16": extra,
         "pi_attention": pi_fig,
+        "fp8_kv": fp8_fig,
         "prefill_varlen": pvar_fig,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
