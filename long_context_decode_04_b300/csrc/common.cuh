@@ -61,6 +61,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the same (for a thread that polls several barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity.  Gives up (returns
 // false) when *abort is set by another thread or after kWaitLimitNs, in
 // which case it sets *abort itself.
@@ -110,6 +124,16 @@ __device__ __forceinline__ void bulk_copy_g2s_hint(void *smem_dst, const void *g
         "%4;" ::"r"(smem_u32(smem_dst)),
         "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// Atomic add at GPU scope with acquire-release semantics; returns the old
+// value.  After a CTA-wide rendezvous it publishes the CTA's earlier global
+// stores (release) and makes other CTAs' published stores visible (acquire).
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *ptr, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
 }
 
 // Named barrier over `count` threads (a multiple of 32), id 1..15.

@@ -955,6 +955,8 @@ cudaError_t dispatch_types(const DecodeLaunch &a, const DecodeParams &p)
 
 cudaError_t launch_decode(const DecodeLaunch &a)
 {
+    if (decode_tc_eligible(a))
+        return launch_decode_tc(a);
     DecodeParams p;
     p.q = a.q;
     p.k = a.k;

@@ -1,0 +1,954 @@
+// decode_tc.cu -- split-KV exact decode for grouped-query attention with
+// both contractions on the tensor cores (tcgen05, accumulators in TMEM).
+//
+// What is computed is the same as the CUDA-core decode (decode.cu): for
+// each query head, scores s_j = scale * <q, k_j>, softmax weights and the
+// weighted mean of the values (Attention glossary, jisaku.com/glossary/
+// attention, "basic concepts and operating principle"), one partial
+// (m, l, o) per KV chunk and the log-sum-exp merge of a sequence's
+// partials (Tree Attention explainer, aibr.jp/archives/143699, sections 1
+// and 3).  The chunks are the same whole 120-key tiles, so the plan and the
+// partials' layout do not depend on which of the two kernels runs.
+//
+// Why tensor cores in a bandwidth-bound step.  The G query heads of a KV
+// head (grouped-query attention) share its keys, so per KV head the scores
+// are the product [keys x D] . [D x G] and the output [D x keys] . [keys x G]:
+// dense contractions of the streamed tile with a small matrix.  On the CUDA
+// cores they cost about 57 issued warp instructions per key row at G = 4,
+// which keeps that kernel issue-bound a little under the HBM roofline.
+// Here each contraction is a handful of tcgen05.mma per tile and the
+// remaining per-key work is a few instructions of softmax, so the kernel
+// streams K and V at the bandwidth of HBM.
+//
+// Per 120-key tile (M = 128 rows; rows 120-127 of every staged tile are
+// zero and masked):
+//   S^T [128 keys x 16] = K [128 x D] . Q^T [D x 16]     (A = K, K-major;
+//                                                        B = Q, heads padded to 16)
+//   O_t^T [D x 16]      = V^T [D x 128] . P^T [128 x 16] (A = V, MN-major;
+//                                                        B = P, K-major)
+// with P = exp2(s - m) of the running maximum m, written to shared memory
+// as bf16 hi + lo parts (p = hi + lo to about 2^-17 relative; two MMAs add
+// both), so the weights keep fp32-like precision against bf16 V.
+//
+// Kernel layout (one persistent CTA per SM, 8 warps):
+//   * warp 0, lane 0: producer.  Takes work items (sequence, KV head, chunk)
+//     from the device-wide queue, loads the item's G query rows (TMA, 128-
+//     byte swizzle) into one of two Q buffers and the chunk's K/V tiles
+//     (TMA boxes of 120 rows x 64 dims) into a 3-stage ring.
+//   * warp 1: allocates 64 TMEM columns (S double buffer, O double
+//     buffer); lane 0 issues the MMAs: S of tile t, then O of tile t - 1,
+//     so the score product of a tile overlaps the softmax of the previous.
+//   * warps 4-7 (one warpgroup, TMEM lane quadrants 0-3): thread r owns key
+//     row r of every tile for the softmax and output dimension r for the
+//     accumulation.  Per tile: load the G scores of its key, tile maximum
+//     (warp shuffles, then four warps through shared memory), new running
+//     maximum, weights, P to shared memory; then add the previous tile's
+//     O_t (rescaled by the ratio of the running maxima) to its registers.
+//     At the end of an item: weight sums, then the partial (or the final
+//     output and lse), and in fused mode the ticket and the merge.
+//   * Every wait is bounded (kWaitLimitNs); on expiry the kernel records
+//     TA_DEVERR_TIMEOUT, stops, lets its copies and MMAs land and frees its
+//     TMEM.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace ta {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTile = kDecodeTileKeys;  // 120 keys a tile
+constexpr int kRows = 128;              // MMA rows: staged rows 120-127 stay zero
+constexpr int kN = 16;                  // MMA N: the group's heads, zero-padded
+constexpr int kStages = 3;
+constexpr int kHalf = kRows * 128;          // one 64-dim half of a staged K or V tile
+constexpr int kTileBytes = 2 * kHalf;       // 32 KiB
+constexpr int kStageBytes = 2 * kTileBytes; // K then V
+constexpr int kQHalf = kN * 128;            // 16 rows x 128 bytes
+constexpr int kQBytes = 2 * kQHalf;
+constexpr int kON = 2 * kN;                 // value-product N: (warp, head) columns, hi then lo
+constexpr int kPHalf = kON * 128;           // P rows x 64 keys of 128 bytes
+constexpr int kPBytes = 2 * kPHalf;         // one P operand: 32 rows x 128 keys, bf16
+constexpr int kQOff = kStages * kStageBytes;
+constexpr int kPOff = kQOff + 2 * kQBytes;
+constexpr int kMiscOff = kPOff + 2 * kPBytes;
+constexpr uint32_t kTxBytes = 4u * kTile * 128u;  // K and V, two halves each
+constexpr int kSoftWarp0 = 4;
+constexpr int kSoftThreads = 128;
+constexpr int kThreads = 256;
+constexpr uint32_t kOCol = 2 * kN;   // S at TMEM columns 0 and 16, O at 32 and 64
+constexpr uint32_t kTmemCols = 128;
+constexpr unsigned kFull = 0xffffffffu;
+
+enum : int { kFirst = 1, kLast = 2, kEnd = 4 };
+enum : int { kModeFinal = 0, kModePartials = 1, kModeFused = 2 };
+
+struct TileDesc {
+    int item;
+    int j0;
+    int n;
+    int flags;
+};
+
+struct Misc {
+    uint64_t full[kStages];      // K/V tile landed (TMA bytes) and its descriptor written
+    uint64_t kv_empty[kStages];  // both products of the tile done (MMA commit)
+    uint64_t s_full[2];          // S of a tile in TMEM (MMA commit)
+    uint64_t p_full[2];          // P of a tile in shared memory (128 softmax threads)
+    uint64_t o_full[2];          // O_t in TMEM (MMA commit)
+    uint64_t o_empty[2];         // O_t added to the registers (128 threads)
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
+    uint64_t grp_bar;            // softmax warpgroup rendezvous (end of item)
+    uint64_t mma_done;
+    TileDesc desc[kStages];
+    float alpha[4][4][4];        // [tile % 4][warp][head] factor by which a warp's maximum rose
+    float lred[4][4];            // [warp][head] weight sums at the item end
+    float mred[4][4];            // [warp][head] running maxima at the item end
+    uint32_t tmem_base;
+    int abort;
+    int ticket;
+};
+
+constexpr size_t kSmem = (size_t)kMiscOff + sizeof(Misc) + 1024;  // + alignment slack
+static_assert(kSmem <= 232448, "shared memory per CTA");
+static_assert(kTile <= kRows && kTile % 8 == 0, "tile rows");
+
+struct TcParams {
+    // q rows (box 64 x G); K/V tiles of 120 rows (contiguous cache); K/V
+    // groups of 8 rows (contiguous cache, or the page pool of a paged one);
+    // pi-Attention periodic keys as rows (tiles of 120 and groups of 8)
+    CUtensorMap qmap, kmap, vmap, k8map, v8map, kpimap, vpimap, kpi8map, vpi8map;
+    // a page pool with boxes of 8, 16, 32 and 64 rows
+    CUtensorMap kpg[4], vpg[4];
+    const void *k, *v;
+    void *out;
+    float *lse;
+    int B, Hq, Hkv, S;
+    float qscale;  // scale * log2(e)
+    const int32_t *seqlens;
+    int n_split, chunk, n_items;
+    int mode;
+    int32_t *status;    // [0] flags, [16] work-queue counter
+    int32_t *counters;  // [B * Hkv] finished chunks per unit (fused mode)
+    float *part_m, *part_l, *part_o;
+    // Paged KV cache (block_table != nullptr): k, v are [num_pages, Hkv,
+    // page_size, D] and key j of sequence b lives in page
+    // block_table[b * pages_per_seq + j / page_size] at row j % page_size.
+    const int32_t *block_table;
+    int page_size, pages_per_seq, num_pages;
+    // pi-Attention key set (pi_period > 0): the query at i = L - 1 attends
+    // the window [max(0, i - pi_window), i] and the keys i - m * pi_period
+    // (m >= 1) before it; the chunks cut the ascending list of those keys.
+    int pi_window, pi_period;
+};
+
+__device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+template <int G, typename OUT>
+__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ TcParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    Misc *ms = reinterpret_cast<Misc *>(smem + kMiscOff);
+    volatile int *abort_flag = &ms->abort;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Zero what no copy writes: rows 120-127 of every staged half, the Q
+    // buffers (rows G..15 stay zero) and the P buffers.
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < kStages * 4 * 8 * 8; i += kThreads) {
+        const int c = i & 7, r = kTile + ((i >> 3) & 7), hh = (i >> 6) & 3, s = i >> 8;
+        *reinterpret_cast<uint4 *>(smem + s * kStageBytes + hh * kHalf + r * 128 + c * 16) = z4;
+    }
+    for (int i = threadIdx.x; i < (kMiscOff - kQOff) / 16; i += kThreads)
+        *reinterpret_cast<uint4 *>(smem + kQOff + i * 16) = z4;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ms->full[s], 2);  // the producer arrives before and after its copies
+            mbar_init(&ms->kv_empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ms->s_full[i], 1);
+            mbar_init(&ms->p_full[i], kSoftThreads);
+            mbar_init(&ms->o_full[i], 1);
+            mbar_init(&ms->o_empty[i], kSoftThreads);
+            mbar_init(&ms->q_full[i], 1);
+            mbar_init(&ms->q_empty[i], 1);
+        }
+        mbar_init(&ms->grp_bar, 4);
+        mbar_init(&ms->mma_done, 1);
+        ms->abort = 0;
+        ms->ticket = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&ms->tmem_base, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = ms->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        // Lane 0 takes the decisions (work queue, ring waits, expected
+        // bytes, descriptors); the 32 lanes share the copies of a tile.  A
+        // tile is one TMA box of 120 rows when its keys are contiguous in
+        // memory, else 15 groups of 8 rows: a box of 8 rows for a group whose
+        // keys are contiguous (one page; all periodic or all window keys),
+        // plain loads and swizzled stores for the others.  The full barrier
+        // takes two arrivals from lane 0, with the expected TMA bytes before
+        // the copies and once the plain stores are done.
+        const bool leader = lane == 0;
+        if (leader) {
+            tc::prefetch_tensormap(&p.qmap);
+            tc::prefetch_tensormap(&p.kmap);
+            tc::prefetch_tensormap(&p.vmap);
+        }
+        const uint64_t policy = l2_policy_evict_first();
+        const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.k);
+        const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(p.v);
+        int stage = 0;
+        uint32_t uses[kStages] = {0u, 0u, 0u};  // times each stage was armed
+        uint32_t q_uses[2] = {0u, 0u};
+        int ic = 0;  // items taken
+        bool ok = true;
+        while (ok) {
+            int item = 0;
+            if (leader)
+                item = atomicAdd(&p.status[16], 1);
+            item = __shfl_sync(kFull, item, 0);
+            if (item >= p.n_items) {
+                int w = 1;
+                if (leader) {
+                    if (item == p.n_items + (int)gridDim.x - 1)
+                        atomicExch(&p.status[16], 0);  // last grab of the launch: reset the queue
+                    if (uses[stage] > 0)
+                        w = mbar_wait_bounded(&ms->kv_empty[stage], (uses[stage] - 1) & 1, abort_flag);
+                    if (w) {
+                        ms->desc[stage] = TileDesc{item, 0, 0, kEnd};
+                        mbar_arrive(&ms->full[stage]);
+                        mbar_arrive(&ms->full[stage]);
+                    }
+                }
+                if (__shfl_sync(kFull, w, 0))
+                    ++uses[stage];
+                break;
+            }
+            const int unit = item / p.n_split;
+            const int split = item - unit * p.n_split;
+            const int b = unit / p.Hkv;
+            const int kvh = unit - b * p.Hkv;
+            int L = p.S;
+            if (p.seqlens) {
+                L = p.seqlens[b];
+                if (L < 0 || L > p.S) {
+                    if (leader)
+                        atomicOr(&p.status[0], TA_DEVERR_SEQLEN);
+                    L = L < 0 ? 0 : p.S;
+                }
+            }
+            // the keys this sequence attends, as an ascending list of N
+            // positions: n_skip periodic keys r0, r0 + pi, ... then the window
+            int N = L, w0 = 0, r0 = 0, n_skip = 0;
+            if (p.pi_period > 0 && L > 0) {
+                const int i = L - 1;
+                w0 = max(0, i - p.pi_window);
+                r0 = i % p.pi_period;
+                n_skip = w0 > r0 ? (w0 - 1 - r0) / p.pi_period + 1 : 0;
+                N = n_skip + (i - w0 + 1);
+            }
+            const int c0 = split * p.chunk;
+            const int c1 = min(c0 + p.chunk, N);
+            const int32_t *bt = p.block_table ? p.block_table + (size_t)b * p.pages_per_seq : nullptr;
+            // element offset of the K/V row of list position pos (a paged
+            // cache's bad page entries are flagged and read page 0)
+            auto row_of = [&](int pos) -> size_t {
+                if (bt) {
+                    const int pg = pos / p.page_size;
+                    int page = bt[pg];
+                    if (page < 0 || page >= p.num_pages) {
+                        atomicOr(&p.status[0], TA_DEVERR_PAGE);
+                        page = 0;
+                    }
+                    return (((size_t)page * p.Hkv + kvh) * p.page_size + (pos - pg * p.page_size)) * kD;
+                }
+                const int key = pos < n_skip ? r0 + pos * p.pi_period : w0 + (pos - n_skip);
+                return ((size_t)unit * p.S + key) * kD;
+            };
+            // the item's G query rows
+            const int qb = ic & 1;
+            int w = 1;
+            if (leader) {
+                if (q_uses[qb] > 0)
+                    w = mbar_wait_bounded(&ms->q_empty[qb], (q_uses[qb] - 1) & 1, abort_flag);
+                if (w) {
+                    unsigned char *qd = smem + kQOff + qb * kQBytes;
+                    mbar_arrive_expect_tx(&ms->q_full[qb], 2u * G * 128u);
+                    tc::tma_load_3d(qd, &p.qmap, 0, 0, unit, &ms->q_full[qb]);
+                    tc::tma_load_3d(qd + kQHalf, &p.qmap, 64, 0, unit, &ms->q_full[qb]);
+                }
+            }
+            if (!__shfl_sync(kFull, w, 0))
+                break;
+            ++q_uses[qb];
+            ++ic;
+            int j0 = c0, flags = kFirst;
+            for (;;) {
+                const int n = max(0, min(kTile, c1 - j0));
+                const bool last = j0 + n >= c1;
+                if (last)
+                    flags |= kLast;
+                // whole-tile boxes: contiguous keys (y = ya of kmap), or 120
+                // periodic keys (y = j0 of kpimap)
+                const bool whole = n > 0 && !bt && (p.pi_period == 0 || j0 >= n_skip);
+                const bool whole_pi = n > 0 && !bt && p.pi_period > 0 && j0 + kTile <= n_skip;
+                const int ya = p.pi_period > 0 ? w0 + (j0 - n_skip) : j0;
+                // a paged tile on the 8-row grid: lane sg copies the tile's
+                // rows in page pg0 + sg, [sg_r, sg_r + sg_len) of the tile
+                // from row sg_off of the page, in boxes of 64/32/16/8 rows
+                const bool segs = n > 0 && bt && (p.page_size & 7) == 0 && (j0 & 7) == 0;
+                int sg_len = 0, sg_r = 0, sg_off = 0, sg_z = 0;
+                if (segs) {
+                    const int P = p.page_size;
+                    const int pg0 = j0 / P;
+                    const int n_seg = (j0 + n - 1) / P - pg0 + 1;
+                    if (lane < n_seg) {
+                        const int pg = pg0 + lane;
+                        const int a = max(j0, pg * P);
+                        const int e = min(j0 + n, (pg + 1) * P);
+                        const int e8 = min(j0 + ((e - j0 + 7) & ~7), (pg + 1) * P);  // whole groups of 8
+                        int page = bt[pg];
+                        if (page < 0 || page >= p.num_pages) {
+                            atomicOr(&p.status[0], TA_DEVERR_PAGE);
+                            page = 0;
+                        }
+                        sg_len = e8 - a;
+                        sg_r = a - j0;
+                        sg_off = a - pg * P;
+                        sg_z = page * p.Hkv + kvh;
+                    }
+                }
+                const int ng = (whole || whole_pi || segs) ? 0 : (n + 7) >> 3;  // groups of 8 rows
+                bool g8 = false;
+                const CUtensorMap *gk = &p.k8map, *gv = &p.v8map;
+                int gx = 0, gy = 0, gz = unit;
+                if (lane < ng) {
+                    const int pos = j0 + 8 * lane;
+                    if (bt) {
+                        const int pg = pos / p.page_size, off = pos - pg * p.page_size;
+                        if (off + 8 <= p.page_size) {
+                            int page = bt[pg];
+                            if (page < 0 || page >= p.num_pages) {
+                                atomicOr(&p.status[0], TA_DEVERR_PAGE);
+                                page = 0;
+                            }
+                            g8 = true;
+                            gy = off;
+                            gz = page * p.Hkv + kvh;
+                        }
+                    } else if (pos + 8 <= n_skip) {
+                        g8 = true;
+                        gk = &p.kpi8map;
+                        gv = &p.vpi8map;
+                        gx = r0 * kD;
+                        gy = pos;
+                    } else if (pos >= n_skip) {
+                        g8 = true;
+                        gy = w0 + (pos - n_skip);
+                    }
+                }
+                const unsigned g8_mask = __ballot_sync(kFull, g8);
+                const unsigned man_mask = __ballot_sync(kFull, lane < ng && !g8);
+                int seg_rows = sg_len;
+#pragma unroll
+                for (int mask = 16; mask >= 1; mask >>= 1)
+                    seg_rows += __shfl_xor_sync(kFull, seg_rows, mask);
+                const uint32_t bytes = (whole || whole_pi) ? kTxBytes
+                                       : segs            ? (uint32_t)seg_rows * 512u
+                                                         : (uint32_t)__popc(g8_mask) * 4096u;
+                w = 1;
+                if (leader) {
+                    if (uses[stage] > 0)
+                        w = mbar_wait_bounded(&ms->kv_empty[stage], (uses[stage] - 1) & 1, abort_flag);
+                    if (w) {
+                        ms->desc[stage] = TileDesc{item, j0, n, flags};
+                        if (bytes)
+                            mbar_arrive_expect_tx(&ms->full[stage], bytes);
+                        else
+                            mbar_arrive(&ms->full[stage]);
+                    }
+                }
+                if (!__shfl_sync(kFull, w, 0)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char *kd = smem + stage * kStageBytes;
+                unsigned char *vd = kd + kTileBytes;
+                uint64_t *fb = &ms->full[stage];
+                if (leader && (whole || whole_pi)) {
+                    // rows past S read as zero; rows in [n, 120) are zeroed by
+                    // the softmax threads before the value product
+                    const CUtensorMap *mk = whole ? &p.kmap : &p.kpimap;
+                    const CUtensorMap *mv = whole ? &p.vmap : &p.vpimap;
+                    const int x0 = whole ? 0 : r0 * kD, y = whole ? ya : j0;
+                    tc::tma_load_3d_hint(kd, mk, x0, y, unit, fb, policy);
+                    tc::tma_load_3d_hint(kd + kHalf, mk, x0 + 64, y, unit, fb, policy);
+                    tc::tma_load_3d_hint(vd, mv, x0, y, unit, fb, policy);
+                    tc::tma_load_3d_hint(vd + kHalf, mv, x0 + 64, y, unit, fb, policy);
+                }
+                if (sg_len > 0) {
+                    int r = sg_r, off = sg_off;
+#pragma unroll
+                    for (int i = 3; i >= 0; --i) {
+                        const int h = 8 << i;
+                        if (sg_len & h) {
+                            tc::tma_load_3d_hint(kd + r * 128, &p.kpg[i], 0, off, sg_z, fb, policy);
+                            tc::tma_load_3d_hint(kd + kHalf + r * 128, &p.kpg[i], 64, off, sg_z, fb, policy);
+                            tc::tma_load_3d_hint(vd + r * 128, &p.vpg[i], 0, off, sg_z, fb, policy);
+                            tc::tma_load_3d_hint(vd + kHalf + r * 128, &p.vpg[i], 64, off, sg_z, fb, policy);
+                            r += h;
+                            off += h;
+                        }
+                    }
+                }
+                if (g8) {
+                    const int r = 8 * lane * 128;
+                    tc::tma_load_3d_hint(kd + r, gk, gx, gy, gz, fb, policy);
+                    tc::tma_load_3d_hint(kd + kHalf + r, gk, gx + 64, gy, gz, fb, policy);
+                    tc::tma_load_3d_hint(vd + r, gv, gx, gy, gz, fb, policy);
+                    tc::tma_load_3d_hint(vd + kHalf + r, gv, gx + 64, gy, gz, fb, policy);
+                }
+                // the other groups: lane = 4 * row + part, part = K or V x half
+                for (unsigned mm = man_mask; mm; mm &= mm - 1) {
+                    const int r = 8 * (__ffs(mm) - 1) + (lane >> 2);
+                    const int part = lane & 3;
+                    if (r < n) {
+                        const __nv_bfloat16 *src = (part < 2 ? kg : vg) + row_of(j0 + r) + (part & 1) * 64;
+                        uint4 x[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            x[c] = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+                        unsigned char *dst = (part < 2 ? kd : vd) + (part & 1) * kHalf + r * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) = x[c];
+                    }
+                }
+                if (man_mask)
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (leader)
+                    mbar_arrive(fb);
+                ++uses[stage];
+                if (++stage == kStages)
+                    stage = 0;
+                if (last)
+                    break;
+                j0 += n;
+                flags = 0;
+            }
+        }
+        // Every copy issued lands before the CTA exits (immediate on the
+        // normal path; bounded after an abort).
+        __syncwarp();
+        if (leader) {
+            int drain_abort = 0;
+            for (int s = 0; s < kStages; ++s)
+                if (uses[s] > 0)
+                    mbar_wait_bounded(&ms->full[s], (uses[s] - 1) & 1, &drain_abort);
+            for (int i = 0; i < 2; ++i)
+                if (q_uses[i] > 0)
+                    mbar_wait_bounded(&ms->q_full[i], (q_uses[i] - 1) & 1, &drain_abort);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = tc::idesc_bf16_f32_major(kRows, kN, false, false);
+            constexpr uint32_t kIdPV = tc::idesc_bf16_f32_major(kRows, kON, true, false);
+            const uint32_t sbase = smem_u32(smem);
+            // O_x^T = V^T P^T: A = V (MN-major: the two 64-dim halves 16 KiB
+            // apart, 8-key groups 1 KiB apart), B = P hi then P lo (K-major).
+            auto issue_pv = [&](int x, int st) {
+                const uint32_t o_tm = tmem + kOCol + (x & 1) * kON;
+                const uint32_t vb = sbase + st * kStageBytes + kTileBytes;
+                const uint32_t pb = sbase + kPOff + (x & 1) * kPBytes;
+#pragma unroll
+                for (int kk = 0; kk < kRows / 16; ++kk) {
+                    const uint64_t a = tc::sw128_desc(vb + kk * 2048, kHalf, 1024);
+                    const uint32_t po = (kk >> 2) * kPHalf + (kk & 3) * 32;
+                    tc::mma_ss(o_tm, a, tc::sw128_desc(pb + po, 16, 1024), kIdPV, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(&ms->o_full[x & 1]);
+                tc::commit(&ms->kv_empty[st]);
+            };
+            // The two products are issued as soon as their inputs are ready,
+            // polling both: S of tile qt (its K/V landed, S buffer free: the
+            // softmax of qt - 2 is done) and O of tile vt (its P written, its
+            // O buffer added up).  So a tile's value product never waits for
+            // the next tile's copy, and a stage is released early.
+            int qt = 0, vt = 0;            // next tile for S, for O
+            int q_stage = 0, v_stage = 0;  // their ring stages
+            uint32_t q_sph = 0;
+            int ic = 0;
+            bool end = false;
+            uint64_t t_idle = 0;
+            for (uint32_t spin = 0;; ++spin) {
+                bool progress = false;
+                if (!end && qt <= vt + 1 && mbar_test_wait(&ms->full[q_stage], q_sph)) {
+                    const TileDesc d = ms->desc[q_stage];
+                    const int qb = ic & 1;
+                    if (d.flags & kEnd) {
+                        end = true;
+                        progress = true;
+                    } else if (!(d.flags & kFirst) || mbar_test_wait(&ms->q_full[qb], (ic >> 1) & 1)) {
+                        tc::fence_after_sync();
+                        // S_t^T = K Q^T over D in 8 steps of 16
+                        const uint32_t s_tm = tmem + (qt & 1) * kN;
+                        const uint32_t kb = sbase + q_stage * kStageBytes;
+                        const uint32_t qa = sbase + kQOff + qb * kQBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kD / 16; ++kk) {
+                            const uint32_t ko = (kk >> 2) * kHalf + (kk & 3) * 32;
+                            const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
+                            tc::mma_ss(s_tm, tc::sw128_desc(kb + ko, 16, 1024), tc::sw128_desc(qa + qo, 16, 1024),
+                                       kIdS, kk > 0 ? 1u : 0u);
+                        }
+                        tc::commit(&ms->s_full[qt & 1]);
+                        if (d.flags & kLast) {
+                            tc::commit(&ms->q_empty[qb]);
+                            ++ic;
+                        }
+                        ++qt;
+                        if (++q_stage == kStages) {
+                            q_stage = 0;
+                            q_sph ^= 1;
+                        }
+                        progress = true;
+                    }
+                }
+                if (vt < qt && mbar_test_wait(&ms->p_full[vt & 1], (vt >> 1) & 1) &&
+                    mbar_test_wait(&ms->o_empty[vt & 1], ((vt >> 1) & 1) ^ 1)) {
+                    tc::fence_after_sync();
+                    issue_pv(vt, v_stage);
+                    ++vt;
+                    if (++v_stage == kStages)
+                        v_stage = 0;
+                    progress = true;
+                }
+                if (end && vt == qt) {
+                    // every S was read: tell the softmax warps to stop
+                    mbar_arrive(&ms->s_full[qt & 1]);
+                    break;
+                }
+                if (progress) {
+                    t_idle = 0;
+                } else if ((spin & 15u) == 0) {
+                    if (*abort_flag)
+                        break;
+                    const uint64_t now = globaltimer_ns();
+                    if (t_idle == 0) {
+                        t_idle = now;
+                    } else if (now - t_idle > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
+            }
+            // Every MMA issued completes before the TMEM is freed.
+            tc::commit(&ms->mma_done);
+            int drain_abort = 0;
+            mbar_wait_bounded(&ms->mma_done, 0, &drain_abort);
+        }
+        __syncwarp();
+    } else if (warp >= kSoftWarp0) {
+        // ------------------------------------------------------------ softmax + accumulation
+        // Each warp w runs its own online softmax over its 32 key rows of
+        // every tile (running maximum mw, weight sums), so no tile needs an
+        // exchange between warps: its weights go to the P rows of (w, head),
+        // and the value product keeps one column per (w, head), hi and lo.
+        // Thread (w, lane) accumulates output dimension 32 w + lane of all
+        // four warps' columns, each against that warp's maximum (the factors
+        // come through shared memory); the four are merged at the item end.
+        const int q4 = warp - kSoftWarp0;  // TMEM lane quadrant (warp % 4)
+        const int row = q4 * 32 + lane;    // key row of a tile; output dimension
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        int stage = 0;
+        uint32_t sph = 0, gph = 0;
+        int t = 0;
+        float mw[G], l_run[G], o[4][G];
+        int unit = 0, split = 0, b = 0, kvh = 0;
+        auto group_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ms->grp_bar);
+            const bool w = mbar_wait_bounded(&ms->grp_bar, gph, abort_flag);
+            gph ^= 1;
+            return __all_sync(kFull, w);
+        };
+        // o[w] = o[w] * alpha_w + O_x[w] for the four warps' columns of tile x
+        auto accumulate = [&](int x) -> bool {
+            bool w = mbar_wait_bounded(&ms->o_full[x & 1], (x >> 1) & 1, abort_flag);
+            w = w && mbar_wait_bounded(&ms->p_full[x & 1], (x >> 1) & 1, abort_flag);  // the factors
+            if (!__all_sync(kFull, w))
+                return false;
+            tc::fence_after_sync();
+            uint32_t r[32];
+            tc::tmem_ld32(tmem + lane_base + kOCol + (x & 1) * kON, r);
+            tc::tmem_wait_ld(r);
+#pragma unroll
+            for (int w2 = 0; w2 < 4; ++w2)
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const int c = w2 * G + g;
+                    const float ov = __uint_as_float(r[c]) + __uint_as_float(r[kN + c]);
+                    o[w2][g] = fmaf(o[w2][g], ms->alpha[x & 3][w2][g], ov);
+                }
+            tc::fence_before_sync();
+            mbar_arrive(&ms->o_empty[x & 1]);
+            return true;
+        };
+        for (;;) {
+            bool w = mbar_wait_bounded(&ms->s_full[t & 1], (t >> 1) & 1, abort_flag);
+            w = w && mbar_wait_bounded(&ms->full[stage], sph, abort_flag);  // descriptor and V visible
+            if (!__all_sync(kFull, w))
+                break;
+            const TileDesc d = ms->desc[stage];
+            if (d.flags & kEnd)
+                break;
+            if (d.flags & kFirst) {
+                unit = d.item / p.n_split;
+                split = d.item - unit * p.n_split;
+                b = unit / p.Hkv;
+                kvh = unit - b * p.Hkv;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    mw[g] = -INFINITY;
+                    l_run[g] = 0.f;
+#pragma unroll
+                    for (int w2 = 0; w2 < 4; ++w2)
+                        o[w2][g] = 0.f;
+                }
+            }
+            tc::fence_after_sync();
+            uint32_t sr[G];
+            tc::tmem_ld_small<G>(tmem + lane_base + (t & 1) * kN, sr);
+            const bool valid = row < d.n;
+            float s[G], mx[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                s[g] = valid ? __uint_as_float(sr[g]) * p.qscale : -INFINITY;  // log2 units
+                mx[g] = s[g];
+            }
+#pragma unroll
+            for (int mask = 16; mask >= 1; mask >>= 1)
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    mx[g] = fmaxf(mx[g], __shfl_xor_sync(kFull, mx[g], mask));
+            float alpha[G], pw[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float mn = fmaxf(mw[g], mx[g]);
+                alpha[g] = mn == -INFINITY ? 1.f : fast_exp2(mw[g] - mn);
+                pw[g] = mn == -INFINITY ? 0.f : fast_exp2(s[g] - mn);
+                l_run[g] = fmaf(l_run[g], alpha[g], pw[g]);
+                mw[g] = mn;
+            }
+            if (lane < G) {
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    if (lane == g)
+                        ms->alpha[t & 3][q4][g] = alpha[g];
+            }
+            // P^T: rows w*G + g (hi) and 16 + w*G + g (lo), column `row`
+            // (key), 128-byte swizzle: the 16-byte chunk index within a
+            // 128-byte row is xor-ed with row % 8
+            unsigned char *pbase = smem + kPOff + (t & 1) * kPBytes;
+            const int cb = (row & 63) * 2;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const int rh = q4 * G + g, rl = kN + rh;
+                const int base = (row >> 6) * kPHalf + (cb & 15);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(pw[g]);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(pw[g] - __bfloat162float(hi));
+                *reinterpret_cast<__nv_bfloat16 *>(pbase + base + rh * 128 + ((((cb >> 4) ^ rh) & 7) << 4)) = hi;
+                *reinterpret_cast<__nv_bfloat16 *>(pbase + base + rl * 128 + ((((cb >> 4) ^ rl) & 7) << 4)) = lo;
+            }
+            // V rows of keys past the tile's end may hold anything (padding
+            // past a sequence's length): zero them so that 0 * V stays 0
+            if (d.n < kTile && row >= d.n && row < kTile) {
+                unsigned char *vr = smem + stage * kStageBytes + kTileBytes + row * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    *reinterpret_cast<uint4 *>(vr + c * 16) = z4;
+                    *reinterpret_cast<uint4 *>(vr + kHalf + c * 16) = z4;
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc::fence_before_sync();
+            mbar_arrive(&ms->p_full[t & 1]);
+            if (!(d.flags & kFirst) && !accumulate(t - 1))
+                break;
+            const int tt = t;
+            ++t;
+            if (++stage == kStages) {
+                stage = 0;
+                sph ^= 1;
+            }
+            if (!(d.flags & kLast))
+                continue;
+            if (!accumulate(tt))
+                break;
+
+            // ---- end of item: merge the four warps' states
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float v = l_run[g];
+#pragma unroll
+                for (int mask = 16; mask >= 1; mask >>= 1)
+                    v += __shfl_xor_sync(kFull, v, mask);
+                if (lane == g) {
+                    ms->lred[q4][g] = v;
+                    ms->mred[q4][g] = mw[g];
+                }
+            }
+            if (!group_sync())
+                break;
+            float ls[G], mt[G], of[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                mt[g] = fmax3(ms->mred[0][g], ms->mred[1][g], fmaxf(ms->mred[2][g], ms->mred[3][g]));
+                ls[g] = 0.f;
+                of[g] = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < 4; ++w2) {
+                    const float m2 = ms->mred[w2][g];
+                    const float be = m2 == -INFINITY ? 0.f : fast_exp2(m2 - mt[g]);
+                    ls[g] = fmaf(ms->lred[w2][g], be, ls[g]);
+                    of[g] = fmaf(o[w2][g], be, of[g]);
+                }
+            }
+            const size_t row0 = (size_t)b * p.Hq + (size_t)kvh * G;
+            if (p.mode == kModeFinal) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float inv = ls[g] > 0.f ? 1.0f / ls[g] : 0.f;
+                    store_out(static_cast<OUT *>(p.out) + (row0 + g) * kD + row, of[g] * inv);
+                    if (row == g && p.lse)
+                        p.lse[row0 + g] = ls[g] > 0.f ? (mt[g] + fast_log2(ls[g])) * kLn2 : -INFINITY;
+                }
+                continue;
+            }
+            const int ns = p.n_split;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const size_t pi = (row0 + g) * ns + split;
+                p.part_o[pi * kD + row] = of[g];
+                if (row == g) {
+                    p.part_m[pi] = mt[g] == -INFINITY ? -INFINITY : mt[g] * kLn2;
+                    p.part_l[pi] = ls[g];
+                }
+            }
+            if (p.mode != kModeFused)
+                continue;
+
+            // ---- fused merge: the CTA that writes a unit's last partial merges it.
+            // The rendezvous orders the warpgroup's partial stores before
+            // thread 0's GPU-scope acquire-release ticket, which publishes
+            // them to the merging CTA (and, for that CTA, acquires the others').
+            if (!group_sync())
+                break;
+            if (row == 0) {
+                int last = 0;
+                if (atomic_add_acq_rel_gpu(&p.counters[unit], 1) == ns - 1) {
+                    last = 1;
+                    p.counters[unit] = 0;  // ready for the next launch
+                }
+                *reinterpret_cast<volatile int *>(&ms->ticket) = last;
+            }
+            if (!group_sync())
+                break;
+            if (!*reinterpret_cast<volatile int *>(&ms->ticket))
+                continue;
+            // Thread (h, d4) folds head h's ns partials in order with a running
+            // maximum (log-sum-exp rule, natural-log m), loading 16 at a time.
+            for (int idx = row; idx < G * kD / 4; idx += kSoftThreads) {
+                const int h = idx / (kD / 4);
+                const int d4 = (idx - h * (kD / 4)) * 4;
+                const size_t pr = (row0 + h) * ns;
+                const float4 *po = reinterpret_cast<const float4 *>(p.part_o + pr * kD + d4);
+                float mx2 = -INFINITY, lsum = 0.f;
+                float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int n0 = 0; n0 < ns; n0 += 16) {
+                    float mb[16], lb[16];
+                    float4 ob[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        mb[i] = -INFINITY;
+                        if (n0 + i < ns) {
+                            mb[i] = __ldcg(p.part_m + pr + n0 + i);
+                            lb[i] = __ldcg(p.part_l + pr + n0 + i);
+                            ob[i] = __ldcg(po + (size_t)(n0 + i) * (kD / 4));
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (mb[i] != -INFINITY) {
+                            const float mn = fmaxf(mx2, mb[i]);
+                            const float sc = fast_exp2((mx2 - mn) * kLog2e);
+                            const float a = fast_exp2((mb[i] - mn) * kLog2e);
+                            lsum = fmaf(lsum, sc, a * lb[i]);
+                            os.x = fmaf(os.x, sc, a * ob[i].x);
+                            os.y = fmaf(os.y, sc, a * ob[i].y);
+                            os.z = fmaf(os.z, sc, a * ob[i].z);
+                            os.w = fmaf(os.w, sc, a * ob[i].w);
+                            mx2 = mn;
+                        }
+                    }
+                }
+                const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+                OUT *dst = static_cast<OUT *>(p.out) + (row0 + h) * kD + d4;
+                store_out(dst + 0, os.x * inv);
+                store_out(dst + 1, os.y * inv);
+                store_out(dst + 2, os.z * inv);
+                store_out(dst + 3, os.w * inv);
+                if (d4 == 0 && p.lse)
+                    p.lse[row0 + h] = lsum > 0.f ? mx2 + fast_log2(lsum) * kLn2 : -INFINITY;
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag)
+        atomicOr(&p.status[0], TA_DEVERR_TIMEOUT);
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int G, typename OUT>
+cudaError_t launch_typed(const DecodeLaunch &a, const TcParams &p)
+{
+    auto kern = decode_tc_kernel<G, OUT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess)
+        return e;
+    kern<<<a.plan.grid, kThreads, kSmem, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_tc_eligible(const DecodeLaunch &a)
+{
+    const int G = a.Hq / a.Hkv;
+    return a.D == kD && (G == 2 || G == 4) && a.in_dtype == TA_BF16 && !a.kv_fp8;
+}
+
+cudaError_t launch_decode_tc(const DecodeLaunch &a)
+{
+    const int G = a.Hq / a.Hkv;
+    TcParams p;
+    p.out = a.out;
+    p.lse = a.lse;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.S = a.S;
+    p.qscale = a.scale * kLog2e;
+    p.seqlens = a.seqlens;
+    p.n_split = a.plan.n_split;
+    p.chunk = a.plan.chunk;
+    p.n_items = a.B * a.Hkv * a.plan.n_split;
+    if (a.force_partials)
+        p.mode = kModePartials;
+    else if (a.plan.n_split == 1)
+        p.mode = kModeFinal;
+    else
+        p.mode = decode_merges_itself(a.plan.n_split, a.B * a.Hkv) ? kModeFused : kModePartials;
+    p.status = a.status;
+    p.counters = a.counters;
+    p.part_m = a.part_m;
+    p.part_l = a.part_l;
+    p.part_o = a.part_o;
+    p.k = a.k;
+    p.v = a.v;
+    p.block_table = a.block_table;
+    p.page_size = a.page_size;
+    p.pages_per_seq = a.pages_per_seq;
+    p.num_pages = a.num_pages;
+    p.pi_window = a.pi_window;
+    p.pi_period = a.pi_period;
+    // Tensor maps, boxes of 64 dims (128 bytes, the swizzle span):
+    //   q [B, Hq, D] as (D, G, B*Hkv), box G rows;
+    //   K, V [B, Hkv, S, D] as (D, S, B*Hkv), boxes of 120 and 8 rows;
+    //   a page pool [num_pages, Hkv, page_size, D] as (D, page_size,
+    //     num_pages*Hkv), box 8 rows (only pages of at least 8 rows use it);
+    //   pi-Attention: each (sequence, KV head) as rows of pi_period keys,
+    //     (pi*D, ceil(S/pi), B*Hkv): the box at x = r*D, y = m holds keys
+    //     r + (m + t) * pi; it is only used where all its rows are keys of
+    //     the periodic part, so below S of that (sequence, KV head).
+    const uint64_t units = (uint64_t)a.B * a.Hkv;
+    const uint64_t qd[3] = {(uint64_t)kD, (uint64_t)G, units};
+    const uint64_t qs[2] = {(uint64_t)kD * 2, (uint64_t)G * kD * 2};
+    const uint32_t qbox[3] = {64, (uint32_t)G, 1};
+    const uint32_t box120[3] = {64, (uint32_t)kTile, 1};
+    const uint32_t box8[3] = {64, 8, 1};
+    bool ok = encode_tmap_3d(&p.qmap, a.q, true, qd, qs, qbox, true);
+    if (a.block_table) {
+        const uint64_t pd[3] = {(uint64_t)kD, (uint64_t)a.page_size, (uint64_t)a.num_pages * a.Hkv};
+        const uint64_t ps[2] = {(uint64_t)kD * 2, (uint64_t)a.page_size * kD * 2};
+        p.kmap = p.vmap = p.kpimap = p.vpimap = p.kpi8map = p.vpi8map = p.qmap;  // unused
+        p.k8map = p.v8map = p.qmap;
+        for (int i = 0; i < 4; ++i)
+            p.kpg[i] = p.vpg[i] = p.qmap;
+        if (a.page_size >= 8) {
+            ok = ok && encode_tmap_3d(&p.k8map, a.k, true, pd, ps, box8, true) &&
+                 encode_tmap_3d(&p.v8map, a.v, true, pd, ps, box8, true);
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t bx[3] = {64, (uint32_t)(8 << i), 1};
+                ok = ok && encode_tmap_3d(&p.kpg[i], a.k, true, pd, ps, bx, true) &&
+                     encode_tmap_3d(&p.vpg[i], a.v, true, pd, ps, bx, true);
+            }
+        }
+    } else {
+        const uint64_t kd[3] = {(uint64_t)kD, (uint64_t)a.S, units};
+        const uint64_t ks[2] = {(uint64_t)kD * 2, (uint64_t)a.S * kD * 2};
+        ok = ok && encode_tmap_3d(&p.kmap, a.k, true, kd, ks, box120, true) &&
+             encode_tmap_3d(&p.vmap, a.v, true, kd, ks, box120, true) &&
+             encode_tmap_3d(&p.k8map, a.k, true, kd, ks, box8, true) &&
+             encode_tmap_3d(&p.v8map, a.v, true, kd, ks, box8, true);
+        p.kpimap = p.vpimap = p.kpi8map = p.vpi8map = p.qmap;  // unused
+        for (int i = 0; i < 4; ++i)
+            p.kpg[i] = p.vpg[i] = p.qmap;
+        if (a.pi_period > 0) {
+            const uint64_t per = (uint64_t)a.pi_period;
+            const uint64_t pd[3] = {per * kD, ((uint64_t)a.S + per - 1) / per, units};
+            const uint64_t ps[2] = {per * kD * 2, (uint64_t)a.S * kD * 2};
+            ok = ok && encode_tmap_3d(&p.kpimap, a.k, true, pd, ps, box120, true) &&
+                 encode_tmap_3d(&p.vpimap, a.v, true, pd, ps, box120, true) &&
+                 encode_tmap_3d(&p.kpi8map, a.k, true, pd, ps, box8, true) &&
+                 encode_tmap_3d(&p.vpi8map, a.v, true, pd, ps, box8, true);
+        }
+    }
+    if (!ok)
+        return cudaErrorInvalidValue;
+    const bool bf16_out = a.out_dtype == TA_BF16;
+    if (G == 2)
+        return bf16_out ? launch_typed<2, __nv_bfloat16>(a, p) : launch_typed<2, float>(a, p);
+    return bf16_out ? launch_typed<4, __nv_bfloat16>(a, p) : launch_typed<4, float>(a, p);
+}
+
+}  // namespace ta

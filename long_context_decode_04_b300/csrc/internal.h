@@ -83,6 +83,10 @@ int decode_ctas_per_sm();
 
 // Launchers (decode.cu, combine.cu, prefill.cu).  Return cudaGetLastError().
 cudaError_t launch_decode(const DecodeLaunch &a);
+// The tensor-core decode (decode_tc.cu): bf16 q/K/V in a contiguous cache,
+// D = 128, G = 2 or 4; launch_decode hands such launches to it.
+bool decode_tc_eligible(const DecodeLaunch &a);
+cudaError_t launch_decode_tc(const DecodeLaunch &a);
 cudaError_t launch_combine(const float *m, const float *l, const float *o, int R, int N, int D, void *out,
                            ta_dtype out_dtype, float *lse, void *scratch, cudaStream_t stream);
 cudaError_t launch_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse, int B,
