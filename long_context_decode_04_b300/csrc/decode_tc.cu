@@ -31,21 +31,24 @@
 // both), so the weights keep fp32-like precision against bf16 V.
 //
 // Kernel layout (one persistent CTA per SM, 8 warps):
-//   * warp 0, lane 0: producer.  Takes work items (sequence, KV head, chunk)
-//     from the device-wide queue, loads the item's G query rows (TMA, 128-
-//     byte swizzle) into one of two Q buffers and the chunk's K/V tiles
-//     (TMA boxes of 120 rows x 64 dims) into a 3-stage ring.
-//   * warp 1: allocates 64 TMEM columns (S double buffer, O double
-//     buffer); lane 0 issues the MMAs: S of tile t, then O of tile t - 1,
-//     so the score product of a tile overlaps the softmax of the previous.
+//   * warp 0: producer.  Takes work items (sequence, KV head, chunk) from
+//     the device-wide queue, loads the item's G query rows (TMA, 128-byte
+//     swizzle) into one of two Q buffers and the chunk's K/V tiles into a
+//     3-stage ring (TMA boxes of 120 rows x 64 dims; boxes of 8-64 rows
+//     over page segments and pi-Attention boundaries).
+//   * warp 1: allocates 128 TMEM columns (S double buffer, O double
+//     buffer) and issues the score products; warp 2 issues the value
+//     products.  Each blocks on the one barrier it needs next, so a tile's
+//     value product never waits for the next tile's copy.
 //   * warps 4-7 (one warpgroup, TMEM lane quadrants 0-3): thread r owns key
 //     row r of every tile for the softmax and output dimension r for the
-//     accumulation.  Per tile: load the G scores of its key, tile maximum
-//     (warp shuffles, then four warps through shared memory), new running
-//     maximum, weights, P to shared memory; then add the previous tile's
-//     O_t (rescaled by the ratio of the running maxima) to its registers.
-//     At the end of an item: weight sums, then the partial (or the final
-//     output and lse), and in fused mode the ticket and the merge.
+//     accumulation.  Each warp runs its own online softmax over its 32 key
+//     rows (running maximum, weights to the P rows of (warp, head)); per
+//     tile a thread then adds the four warps' columns of the previous
+//     tile's O_t to its registers, each rescaled by its warp's factor.  At
+//     the end of an item the four warps' states are merged and the partial
+//     (or the final output and lse) is written; in fused mode the ticket
+//     and the merge follow.
 //   * Every wait is bounded (kWaitLimitNs); on expiry the kernel records
 //     TA_DEVERR_TIMEOUT, stops, lets its copies and MMAs land and frees its
 //     TMEM.
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             mbar_init(&ms->q_empty[i], 1);
         }
         mbar_init(&ms->grp_bar, 4);
-        mbar_init(&ms->mma_done, 1);
+        mbar_init(&ms->mma_done, 2);  // both MMA issuers commit
         ms->abort = 0;
         ms->ticket = 0;
         fence_barrier_init();
@@ -471,101 +474,90 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     mbar_wait_bounded(&ms->q_full[i], (q_uses[i] - 1) & 1, &drain_abort);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 1 issues the score products, warp 2 the value products, each
+        // blocking on the one barrier it needs next, so that neither product
+        // waits on the other's inputs.  Each thread's commits track its own
+        // MMAs: the value product of a tile comes after its softmax, hence
+        // after its score product, so its commit releases the stage.
         if (lane == 0) {
-            constexpr uint32_t kIdS = tc::idesc_bf16_f32_major(kRows, kN, false, false);
-            constexpr uint32_t kIdPV = tc::idesc_bf16_f32_major(kRows, kON, true, false);
             const uint32_t sbase = smem_u32(smem);
-            // O_x^T = V^T P^T: A = V (MN-major: the two 64-dim halves 16 KiB
-            // apart, 8-key groups 1 KiB apart), B = P hi then P lo (K-major).
-            auto issue_pv = [&](int x, int st) {
-                const uint32_t o_tm = tmem + kOCol + (x & 1) * kON;
-                const uint32_t vb = sbase + st * kStageBytes + kTileBytes;
-                const uint32_t pb = sbase + kPOff + (x & 1) * kPBytes;
-#pragma unroll
-                for (int kk = 0; kk < kRows / 16; ++kk) {
-                    const uint64_t a = tc::sw128_desc(vb + kk * 2048, kHalf, 1024);
-                    const uint32_t po = (kk >> 2) * kPHalf + (kk & 3) * 32;
-                    tc::mma_ss(o_tm, a, tc::sw128_desc(pb + po, 16, 1024), kIdPV, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(&ms->o_full[x & 1]);
-                tc::commit(&ms->kv_empty[st]);
-            };
-            // The two products are issued as soon as their inputs are ready,
-            // polling both: S of tile qt (its K/V landed, S buffer free: the
-            // softmax of qt - 2 is done) and O of tile vt (its P written, its
-            // O buffer added up).  So a tile's value product never waits for
-            // the next tile's copy, and a stage is released early.
-            int qt = 0, vt = 0;            // next tile for S, for O
-            int q_stage = 0, v_stage = 0;  // their ring stages
-            uint32_t q_sph = 0;
-            int ic = 0;
-            bool end = false;
-            uint64_t t_idle = 0;
-            for (uint32_t spin = 0;; ++spin) {
-                bool progress = false;
-                if (!end && qt <= vt + 1 && mbar_test_wait(&ms->full[q_stage], q_sph)) {
-                    const TileDesc d = ms->desc[q_stage];
-                    const int qb = ic & 1;
+            int t = 0, stage = 0;
+            uint32_t sph = 0;
+            if (warp == 1) {
+                constexpr uint32_t kIdS = tc::idesc_bf16_f32_major(kRows, kN, false, false);
+                int ic = 0;
+                for (;;) {
+                    if (!mbar_wait_bounded(&ms->full[stage], sph, abort_flag))
+                        break;
+                    const TileDesc d = ms->desc[stage];
+                    // S and P buffers of this parity are free once the value
+                    // product of tile t - 2 is done (its softmax read S, it read P)
+                    if (t >= 2 && !mbar_wait_bounded(&ms->o_full[t & 1], ((t - 2) >> 1) & 1, abort_flag))
+                        break;
                     if (d.flags & kEnd) {
-                        end = true;
-                        progress = true;
-                    } else if (!(d.flags & kFirst) || mbar_test_wait(&ms->q_full[qb], (ic >> 1) & 1)) {
-                        tc::fence_after_sync();
-                        // S_t^T = K Q^T over D in 8 steps of 16
-                        const uint32_t s_tm = tmem + (qt & 1) * kN;
-                        const uint32_t kb = sbase + q_stage * kStageBytes;
-                        const uint32_t qa = sbase + kQOff + qb * kQBytes;
+                        mbar_arrive(&ms->s_full[t & 1]);  // tells the softmax warps to stop
+                        break;
+                    }
+                    const int qb = ic & 1;
+                    if ((d.flags & kFirst) && !mbar_wait_bounded(&ms->q_full[qb], (ic >> 1) & 1, abort_flag))
+                        break;
+                    tc::fence_after_sync();
+                    // S_t^T = K Q^T over D in 8 steps of 16
+                    const uint32_t s_tm = tmem + (t & 1) * kN;
+                    const uint32_t kb = sbase + stage * kStageBytes;
+                    const uint32_t qa = sbase + kQOff + qb * kQBytes;
 #pragma unroll
-                        for (int kk = 0; kk < kD / 16; ++kk) {
-                            const uint32_t ko = (kk >> 2) * kHalf + (kk & 3) * 32;
-                            const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
-                            tc::mma_ss(s_tm, tc::sw128_desc(kb + ko, 16, 1024), tc::sw128_desc(qa + qo, 16, 1024),
-                                       kIdS, kk > 0 ? 1u : 0u);
-                        }
-                        tc::commit(&ms->s_full[qt & 1]);
-                        if (d.flags & kLast) {
-                            tc::commit(&ms->q_empty[qb]);
-                            ++ic;
-                        }
-                        ++qt;
-                        if (++q_stage == kStages) {
-                            q_stage = 0;
-                            q_sph ^= 1;
-                        }
-                        progress = true;
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t ko = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
+                        tc::mma_ss(s_tm, tc::sw128_desc(kb + ko, 16, 1024), tc::sw128_desc(qa + qo, 16, 1024), kIdS,
+                                   kk > 0 ? 1u : 0u);
+                    }
+                    tc::commit(&ms->s_full[t & 1]);
+                    if (d.flags & kLast) {
+                        tc::commit(&ms->q_empty[qb]);
+                        ++ic;
+                    }
+                    ++t;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        sph ^= 1;
                     }
                 }
-                if (vt < qt && mbar_test_wait(&ms->p_full[vt & 1], (vt >> 1) & 1) &&
-                    mbar_test_wait(&ms->o_empty[vt & 1], ((vt >> 1) & 1) ^ 1)) {
+            } else {
+                constexpr uint32_t kIdPV = tc::idesc_bf16_f32_major(kRows, kON, true, false);
+                for (;;) {
+                    if (!mbar_wait_bounded(&ms->full[stage], sph, abort_flag))
+                        break;
+                    if (ms->desc[stage].flags & kEnd)
+                        break;
+                    if (!mbar_wait_bounded(&ms->p_full[t & 1], (t >> 1) & 1, abort_flag) ||
+                        !mbar_wait_bounded(&ms->o_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag))
+                        break;
                     tc::fence_after_sync();
-                    issue_pv(vt, v_stage);
-                    ++vt;
-                    if (++v_stage == kStages)
-                        v_stage = 0;
-                    progress = true;
-                }
-                if (end && vt == qt) {
-                    // every S was read: tell the softmax warps to stop
-                    mbar_arrive(&ms->s_full[qt & 1]);
-                    break;
-                }
-                if (progress) {
-                    t_idle = 0;
-                } else if ((spin & 15u) == 0) {
-                    if (*abort_flag)
-                        break;
-                    const uint64_t now = globaltimer_ns();
-                    if (t_idle == 0) {
-                        t_idle = now;
-                    } else if (now - t_idle > kWaitLimitNs) {
-                        *abort_flag = 1;
-                        break;
+                    // O_t^T = V^T P^T: A = V (MN-major: the two 64-dim halves
+                    // 16 KiB apart, 8-key groups 1 KiB apart), B = P (K-major)
+                    const uint32_t o_tm = tmem + kOCol + (t & 1) * kON;
+                    const uint32_t vb = sbase + stage * kStageBytes + kTileBytes;
+                    const uint32_t pb = sbase + kPOff + (t & 1) * kPBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kRows / 16; ++kk) {
+                        const uint64_t a = tc::sw128_desc(vb + kk * 2048, kHalf, 1024);
+                        const uint32_t po = (kk >> 2) * kPHalf + (kk & 3) * 32;
+                        tc::mma_ss(o_tm, a, tc::sw128_desc(pb + po, 16, 1024), kIdPV, kk > 0 ? 1u : 0u);
+                    }
+                    tc::commit(&ms->o_full[t & 1]);
+                    tc::commit(&ms->kv_empty[stage]);
+                    ++t;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        sph ^= 1;
                     }
                 }
             }
-            // Every MMA issued completes before the TMEM is freed.
+            // Every MMA this thread issued completes before the TMEM is freed.
             tc::commit(&ms->mma_done);
             int drain_abort = 0;
             mbar_wait_bounded(&ms->mma_done, 0, &drain_abort);
