@@ -38,7 +38,7 @@ if ROOT not in sys.path:
 DECODE_WORKLOAD = "gqa_32x8_d128_s131072"
 PREFILL_WORKLOAD = "causal_prefill_32x8_d128_s16384"
 PROFILES = {  # committed ncu summaries: (file, kernel source they were taken on)
-    "decode": ("decode_split_kernel_gqa_32x8_d128_s131072.md", "decode.cu"),
+    "decode": ("decode_tc_kernel_gqa_32x8_d128_s131072.md", "decode_tc.cu"),
     "prefill": ("prefill_causal_kernel_causal_prefill_32x8_d128_s16384.md", "prefill.cu"),
 }
 
@@ -577,7 +577,7 @@ def main():
                          "frac": round(kv_bytes / (alone_us / 1e6) / 1e9 / peaks["hbm_gbs"], 4),
                          "note": "median of 50 decode replays back to back, after the timed region"},
         "decode_hbm_frac": round(value / world / peaks["hbm_gbs"], 4),
-        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_tc_kernel", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": profiled_traffic("decode"), "algorithmic_bytes_per_launch": kv_bytes,
                      "peak_source": peaks["source"] + " (copy bandwidth)",

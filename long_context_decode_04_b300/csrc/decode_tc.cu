@@ -34,8 +34,8 @@
 //   * warp 0: producer.  Takes work items (sequence, KV head, chunk) from
 //     the device-wide queue, loads the item's G query rows (TMA, 128-byte
 //     swizzle) into one of two Q buffers and the chunk's K/V tiles into a
-//     3-stage ring (TMA boxes of 120 rows x 64 dims; boxes of 8-64 rows
-//     over page segments and pi-Attention boundaries).
+//     3-stage ring (TMA boxes of 120 rows x 64 dims; boxes of 8 rows at a
+//     pi-Attention sequence's boundary between periodic and window keys).
 //   * warp 1: allocates 128 TMEM columns (S double buffer, O double
 //     buffer) and issues the score products; warp 2 issues the value
 //     products.  Each blocks on the one barrier it needs next, so a tile's
@@ -84,6 +84,7 @@ constexpr int kThreads = 256;
 constexpr uint32_t kOCol = 2 * kN;   // S at TMEM columns 0 and 16, O at 32 and 64
 constexpr uint32_t kTmemCols = 128;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr float kRescaleLog2 = 8.0f;
 
 enum : int { kFirst = 1, kLast = 2, kEnd = 4 };
 enum : int { kModeFinal = 0, kModePartials = 1, kModeFused = 2 };
@@ -99,7 +100,9 @@ struct Misc {
     uint64_t full[kStages];      // K/V tile landed (TMA bytes) and its descriptor written
     uint64_t kv_empty[kStages];  // both products of the tile done (MMA commit)
     uint64_t s_full[2];          // S of a tile in TMEM (MMA commit)
-    uint64_t p_full[2];          // P of a tile in shared memory (128 softmax threads)
+    uint64_t p_full[2][4];       // a warp's P of a tile in shared memory (32 threads)
+    uint64_t p_all[2];           // all four warps' P and factors (128 threads): a fast
+                                 // warp cannot complete it alone, unlike its own p_full
     uint64_t o_full[2];          // O_t in TMEM (MMA commit)
     uint64_t o_empty[2];         // O_t added to the registers (128 threads)
     uint64_t q_full[2];
@@ -120,12 +123,9 @@ static_assert(kSmem <= 232448, "shared memory per CTA");
 static_assert(kTile <= kRows && kTile % 8 == 0, "tile rows");
 
 struct TcParams {
-    // q rows (box 64 x G); K/V tiles of 120 rows (contiguous cache); K/V
-    // groups of 8 rows (contiguous cache, or the page pool of a paged one);
+    // q rows (box 64 x G); K/V tiles of 120 rows and groups of 8 rows;
     // pi-Attention periodic keys as rows (tiles of 120 and groups of 8)
     CUtensorMap qmap, kmap, vmap, k8map, v8map, kpimap, vpimap, kpi8map, vpi8map;
-    // a page pool with boxes of 8, 16, 32 and 64 rows
-    CUtensorMap kpg[4], vpg[4];
     const void *k, *v;
     void *out;
     float *lse;
@@ -137,11 +137,6 @@ struct TcParams {
     int32_t *status;    // [0] flags, [16] work-queue counter
     int32_t *counters;  // [B * Hkv] finished chunks per unit (fused mode)
     float *part_m, *part_l, *part_o;
-    // Paged KV cache (block_table != nullptr): k, v are [num_pages, Hkv,
-    // page_size, D] and key j of sequence b lives in page
-    // block_table[b * pages_per_seq + j / page_size] at row j % page_size.
-    const int32_t *block_table;
-    int page_size, pages_per_seq, num_pages;
     // pi-Attention key set (pi_period > 0): the query at i = L - 1 attends
     // the window [max(0, i - pi_window), i] and the keys i - m * pi_period
     // (m >= 1) before it; the chunks cut the ascending list of those keys.
@@ -180,7 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms->s_full[i], 1);
-            mbar_init(&ms->p_full[i], kSoftThreads);
+            for (int w = 0; w < 4; ++w)
+                mbar_init(&ms->p_full[i][w], 32);
+            mbar_init(&ms->p_all[i], kSoftThreads);
             mbar_init(&ms->o_full[i], 1);
             mbar_init(&ms->o_empty[i], kSoftThreads);
             mbar_init(&ms->q_full[i], 1);
@@ -207,8 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         // bytes, descriptors); the 32 lanes share the copies of a tile.  A
         // tile is one TMA box of 120 rows when its keys are contiguous in
         // memory, else 15 groups of 8 rows: a box of 8 rows for a group whose
-        // keys are contiguous (one page; all periodic or all window keys),
-        // plain loads and swizzled stores for the others.  The full barrier
+        // keys are contiguous (all periodic or all window keys), plain loads
+        // and swizzled stores for the one group that straddles the two.  The full barrier
         // takes two arrivals from lane 0, with the expected TMA bytes before
         // the copies and once the plain stores are done.
         const bool leader = lane == 0;
@@ -250,7 +247,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             const int unit = item / p.n_split;
             const int split = item - unit * p.n_split;
             const int b = unit / p.Hkv;
-            const int kvh = unit - b * p.Hkv;
             int L = p.S;
             if (p.seqlens) {
                 L = p.seqlens[b];
@@ -272,19 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             }
             const int c0 = split * p.chunk;
             const int c1 = min(c0 + p.chunk, N);
-            const int32_t *bt = p.block_table ? p.block_table + (size_t)b * p.pages_per_seq : nullptr;
-            // element offset of the K/V row of list position pos (a paged
-            // cache's bad page entries are flagged and read page 0)
+            // element offset of the K/V row of list position pos
             auto row_of = [&](int pos) -> size_t {
-                if (bt) {
-                    const int pg = pos / p.page_size;
-                    int page = bt[pg];
-                    if (page < 0 || page >= p.num_pages) {
-                        atomicOr(&p.status[0], TA_DEVERR_PAGE);
-                        page = 0;
-                    }
-                    return (((size_t)page * p.Hkv + kvh) * p.page_size + (pos - pg * p.page_size)) * kD;
-                }
                 const int key = pos < n_skip ? r0 + pos * p.pi_period : w0 + (pos - n_skip);
                 return ((size_t)unit * p.S + key) * kD;
             };
@@ -313,53 +298,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     flags |= kLast;
                 // whole-tile boxes: contiguous keys (y = ya of kmap), or 120
                 // periodic keys (y = j0 of kpimap)
-                const bool whole = n > 0 && !bt && (p.pi_period == 0 || j0 >= n_skip);
-                const bool whole_pi = n > 0 && !bt && p.pi_period > 0 && j0 + kTile <= n_skip;
+                const bool whole = n > 0 && (p.pi_period == 0 || j0 >= n_skip);
+                const bool whole_pi = n > 0 && p.pi_period > 0 && j0 + kTile <= n_skip;
                 const int ya = p.pi_period > 0 ? w0 + (j0 - n_skip) : j0;
-                // a paged tile on the 8-row grid: lane sg copies the tile's
-                // rows in page pg0 + sg, [sg_r, sg_r + sg_len) of the tile
-                // from row sg_off of the page, in boxes of 64/32/16/8 rows
-                const bool segs = n > 0 && bt && (p.page_size & 7) == 0 && (j0 & 7) == 0;
-                int sg_len = 0, sg_r = 0, sg_off = 0, sg_z = 0;
-                if (segs) {
-                    const int P = p.page_size;
-                    const int pg0 = j0 / P;
-                    const int n_seg = (j0 + n - 1) / P - pg0 + 1;
-                    if (lane < n_seg) {
-                        const int pg = pg0 + lane;
-                        const int a = max(j0, pg * P);
-                        const int e = min(j0 + n, (pg + 1) * P);
-                        const int e8 = min(j0 + ((e - j0 + 7) & ~7), (pg + 1) * P);  // whole groups of 8
-                        int page = bt[pg];
-                        if (page < 0 || page >= p.num_pages) {
-                            atomicOr(&p.status[0], TA_DEVERR_PAGE);
-                            page = 0;
-                        }
-                        sg_len = e8 - a;
-                        sg_r = a - j0;
-                        sg_off = a - pg * P;
-                        sg_z = page * p.Hkv + kvh;
-                    }
-                }
-                const int ng = (whole || whole_pi || segs) ? 0 : (n + 7) >> 3;  // groups of 8 rows
+                const int ng = (whole || whole_pi) ? 0 : (n + 7) >> 3;  // groups of 8 rows
                 bool g8 = false;
                 const CUtensorMap *gk = &p.k8map, *gv = &p.v8map;
-                int gx = 0, gy = 0, gz = unit;
+                int gx = 0, gy = 0;
                 if (lane < ng) {
                     const int pos = j0 + 8 * lane;
-                    if (bt) {
-                        const int pg = pos / p.page_size, off = pos - pg * p.page_size;
-                        if (off + 8 <= p.page_size) {
-                            int page = bt[pg];
-                            if (page < 0 || page >= p.num_pages) {
-                                atomicOr(&p.status[0], TA_DEVERR_PAGE);
-                                page = 0;
-                            }
-                            g8 = true;
-                            gy = off;
-                            gz = page * p.Hkv + kvh;
-                        }
-                    } else if (pos + 8 <= n_skip) {
+                    if (pos + 8 <= n_skip) {
                         g8 = true;
                         gk = &p.kpi8map;
                         gv = &p.vpi8map;
@@ -372,13 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 }
                 const unsigned g8_mask = __ballot_sync(kFull, g8);
                 const unsigned man_mask = __ballot_sync(kFull, lane < ng && !g8);
-                int seg_rows = sg_len;
-#pragma unroll
-                for (int mask = 16; mask >= 1; mask >>= 1)
-                    seg_rows += __shfl_xor_sync(kFull, seg_rows, mask);
-                const uint32_t bytes = (whole || whole_pi) ? kTxBytes
-                                       : segs            ? (uint32_t)seg_rows * 512u
-                                                         : (uint32_t)__popc(g8_mask) * 4096u;
+                const uint32_t bytes = (whole || whole_pi) ? kTxBytes : (uint32_t)__popc(g8_mask) * 4096u;
                 w = 1;
                 if (leader) {
                     if (uses[stage] > 0)
@@ -409,27 +351,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     tc::tma_load_3d_hint(vd, mv, x0, y, unit, fb, policy);
                     tc::tma_load_3d_hint(vd + kHalf, mv, x0 + 64, y, unit, fb, policy);
                 }
-                if (sg_len > 0) {
-                    int r = sg_r, off = sg_off;
-#pragma unroll
-                    for (int i = 3; i >= 0; --i) {
-                        const int h = 8 << i;
-                        if (sg_len & h) {
-                            tc::tma_load_3d_hint(kd + r * 128, &p.kpg[i], 0, off, sg_z, fb, policy);
-                            tc::tma_load_3d_hint(kd + kHalf + r * 128, &p.kpg[i], 64, off, sg_z, fb, policy);
-                            tc::tma_load_3d_hint(vd + r * 128, &p.vpg[i], 0, off, sg_z, fb, policy);
-                            tc::tma_load_3d_hint(vd + kHalf + r * 128, &p.vpg[i], 64, off, sg_z, fb, policy);
-                            r += h;
-                            off += h;
-                        }
-                    }
-                }
                 if (g8) {
                     const int r = 8 * lane * 128;
-                    tc::tma_load_3d_hint(kd + r, gk, gx, gy, gz, fb, policy);
-                    tc::tma_load_3d_hint(kd + kHalf + r, gk, gx + 64, gy, gz, fb, policy);
-                    tc::tma_load_3d_hint(vd + r, gv, gx, gy, gz, fb, policy);
-                    tc::tma_load_3d_hint(vd + kHalf + r, gv, gx + 64, gy, gz, fb, policy);
+                    tc::tma_load_3d_hint(kd + r, gk, gx, gy, unit, fb, policy);
+                    tc::tma_load_3d_hint(kd + kHalf + r, gk, gx + 64, gy, unit, fb, policy);
+                    tc::tma_load_3d_hint(vd + r, gv, gx, gy, unit, fb, policy);
+                    tc::tma_load_3d_hint(vd + kHalf + r, gv, gx + 64, gy, unit, fb, policy);
                 }
                 // the other groups: lane = 4 * row + part, part = K or V x half
                 for (unsigned mm = man_mask; mm; mm &= mm - 1) {
@@ -533,21 +460,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                         break;
                     if (ms->desc[stage].flags & kEnd)
                         break;
-                    if (!mbar_wait_bounded(&ms->p_full[t & 1], (t >> 1) & 1, abort_flag) ||
-                        !mbar_wait_bounded(&ms->o_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag))
+                    if (!mbar_wait_bounded(&ms->o_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag))
                         break;
-                    tc::fence_after_sync();
                     // O_t^T = V^T P^T: A = V (MN-major: the two 64-dim halves
-                    // 16 KiB apart, 8-key groups 1 KiB apart), B = P (K-major)
+                    // 16 KiB apart, 8-key groups 1 KiB apart), B = P (K-major).
+                    // Warp w's keys 32w .. 32w + 31 (K steps 2w, 2w + 1) go as
+                    // soon as that warp has written its weights.
                     const uint32_t o_tm = tmem + kOCol + (t & 1) * kON;
                     const uint32_t vb = sbase + stage * kStageBytes + kTileBytes;
                     const uint32_t pb = sbase + kPOff + (t & 1) * kPBytes;
+                    bool ok = true;
 #pragma unroll
-                    for (int kk = 0; kk < kRows / 16; ++kk) {
-                        const uint64_t a = tc::sw128_desc(vb + kk * 2048, kHalf, 1024);
-                        const uint32_t po = (kk >> 2) * kPHalf + (kk & 3) * 32;
-                        tc::mma_ss(o_tm, a, tc::sw128_desc(pb + po, 16, 1024), kIdPV, kk > 0 ? 1u : 0u);
+                    for (int w = 0; w < 4 && ok; ++w) {
+                        ok = mbar_wait_bounded(&ms->p_full[t & 1][w], (t >> 1) & 1, abort_flag);
+                        if (!ok)
+                            break;
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const int kk = 2 * w + i;
+                            const uint64_t a = tc::sw128_desc(vb + kk * 2048, kHalf, 1024);
+                            const uint32_t po = (kk >> 2) * kPHalf + (kk & 3) * 32;
+                            tc::mma_ss(o_tm, a, tc::sw128_desc(pb + po, 16, 1024), kIdPV, kk > 0 ? 1u : 0u);
+                        }
                     }
+                    if (!ok)
+                        break;
                     tc::commit(&ms->o_full[t & 1]);
                     tc::commit(&ms->kv_empty[stage]);
                     ++t;
@@ -591,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         // o[w] = o[w] * alpha_w + O_x[w] for the four warps' columns of tile x
         auto accumulate = [&](int x) -> bool {
             bool w = mbar_wait_bounded(&ms->o_full[x & 1], (x >> 1) & 1, abort_flag);
-            w = w && mbar_wait_bounded(&ms->p_full[x & 1], (x >> 1) & 1, abort_flag);  // the factors
+            w = w && mbar_wait_bounded(&ms->p_all[x & 1], (x >> 1) & 1, abort_flag);  // the factors
             if (!__all_sync(kFull, w))
                 return false;
             tc::fence_after_sync();
@@ -642,19 +580,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 s[g] = valid ? __uint_as_float(sr[g]) * p.qscale : -INFINITY;  // log2 units
                 mx[g] = s[g];
             }
-#pragma unroll
-            for (int mask = 16; mask >= 1; mask >>= 1)
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    mx[g] = fmaxf(mx[g], __shfl_xor_sync(kFull, mx[g], mask));
+            // The warp's reference mw is raised only when a score exceeds it
+            // by more than 2^8 (a warp vote), so the weights stay below 2^8;
+            // then to the warp's maximum, with the factor alpha for the sums.
             float alpha[G], pw[G];
+            bool need = false;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float mn = fmaxf(mw[g], mx[g]);
-                alpha[g] = mn == -INFINITY ? 1.f : fast_exp2(mw[g] - mn);
-                pw[g] = mn == -INFINITY ? 0.f : fast_exp2(s[g] - mn);
-                l_run[g] = fmaf(l_run[g], alpha[g], pw[g]);
-                mw[g] = mn;
+                alpha[g] = 1.f;
+                need |= s[g] > mw[g] + kRescaleLog2;
+            }
+            if (__any_sync(kFull, need)) {
+#pragma unroll
+                for (int mask = 16; mask >= 1; mask >>= 1)
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        mx[g] = fmaxf(mx[g], __shfl_xor_sync(kFull, mx[g], mask));
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (mx[g] > mw[g] + kRescaleLog2) {
+                        alpha[g] = mw[g] == -INFINITY ? 0.f : fast_exp2(mw[g] - mx[g]);
+                        l_run[g] *= alpha[g];
+                        mw[g] = mx[g];
+                    }
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                pw[g] = mw[g] == -INFINITY ? 0.f : fast_exp2(s[g] - mw[g]);
+                l_run[g] += pw[g];
             }
             if (lane < G) {
 #pragma unroll
@@ -688,7 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc::fence_before_sync();
-            mbar_arrive(&ms->p_full[t & 1]);
+            mbar_arrive(&ms->p_full[t & 1][q4]);
+            mbar_arrive(&ms->p_all[t & 1]);
             if (!(d.flags & kFirst) && !accumulate(t - 1))
                 break;
             const int tt = t;
@@ -846,7 +801,9 @@ cudaError_t launch_typed(const DecodeLaunch &a, const TcParams &p)
 bool decode_tc_eligible(const DecodeLaunch &a)
 {
     const int G = a.Hq / a.Hkv;
-    return a.D == kD && (G == 2 || G == 4) && a.in_dtype == TA_BF16 && !a.kv_fp8;
+    // (a paged cache stays on the CUDA-core kernel: its 120-key tiles cut
+    // pages into pieces that would each need a TMA box of their own)
+    return a.D == kD && (G == 2 || G == 4) && a.in_dtype == TA_BF16 && !a.kv_fp8 && !a.block_table;
 }
 
 cudaError_t launch_decode_tc(const DecodeLaunch &a)
@@ -877,17 +834,11 @@ cudaError_t launch_decode_tc(const DecodeLaunch &a)
     p.part_o = a.part_o;
     p.k = a.k;
     p.v = a.v;
-    p.block_table = a.block_table;
-    p.page_size = a.page_size;
-    p.pages_per_seq = a.pages_per_seq;
-    p.num_pages = a.num_pages;
     p.pi_window = a.pi_window;
     p.pi_period = a.pi_period;
     // Tensor maps, boxes of 64 dims (128 bytes, the swizzle span):
     //   q [B, Hq, D] as (D, G, B*Hkv), box G rows;
     //   K, V [B, Hkv, S, D] as (D, S, B*Hkv), boxes of 120 and 8 rows;
-    //   a page pool [num_pages, Hkv, page_size, D] as (D, page_size,
-    //     num_pages*Hkv), box 8 rows (only pages of at least 8 rows use it);
     //   pi-Attention: each (sequence, KV head) as rows of pi_period keys,
     //     (pi*D, ceil(S/pi), B*Hkv): the box at x = r*D, y = m holds keys
     //     r + (m + t) * pi; it is only used where all its rows are keys of
@@ -898,42 +849,22 @@ cudaError_t launch_decode_tc(const DecodeLaunch &a)
     const uint32_t qbox[3] = {64, (uint32_t)G, 1};
     const uint32_t box120[3] = {64, (uint32_t)kTile, 1};
     const uint32_t box8[3] = {64, 8, 1};
-    bool ok = encode_tmap_3d(&p.qmap, a.q, true, qd, qs, qbox, true);
-    if (a.block_table) {
-        const uint64_t pd[3] = {(uint64_t)kD, (uint64_t)a.page_size, (uint64_t)a.num_pages * a.Hkv};
-        const uint64_t ps[2] = {(uint64_t)kD * 2, (uint64_t)a.page_size * kD * 2};
-        p.kmap = p.vmap = p.kpimap = p.vpimap = p.kpi8map = p.vpi8map = p.qmap;  // unused
-        p.k8map = p.v8map = p.qmap;
-        for (int i = 0; i < 4; ++i)
-            p.kpg[i] = p.vpg[i] = p.qmap;
-        if (a.page_size >= 8) {
-            ok = ok && encode_tmap_3d(&p.k8map, a.k, true, pd, ps, box8, true) &&
-                 encode_tmap_3d(&p.v8map, a.v, true, pd, ps, box8, true);
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t bx[3] = {64, (uint32_t)(8 << i), 1};
-                ok = ok && encode_tmap_3d(&p.kpg[i], a.k, true, pd, ps, bx, true) &&
-                     encode_tmap_3d(&p.vpg[i], a.v, true, pd, ps, bx, true);
-            }
-        }
-    } else {
-        const uint64_t kd[3] = {(uint64_t)kD, (uint64_t)a.S, units};
-        const uint64_t ks[2] = {(uint64_t)kD * 2, (uint64_t)a.S * kD * 2};
-        ok = ok && encode_tmap_3d(&p.kmap, a.k, true, kd, ks, box120, true) &&
-             encode_tmap_3d(&p.vmap, a.v, true, kd, ks, box120, true) &&
-             encode_tmap_3d(&p.k8map, a.k, true, kd, ks, box8, true) &&
-             encode_tmap_3d(&p.v8map, a.v, true, kd, ks, box8, true);
-        p.kpimap = p.vpimap = p.kpi8map = p.vpi8map = p.qmap;  // unused
-        for (int i = 0; i < 4; ++i)
-            p.kpg[i] = p.vpg[i] = p.qmap;
-        if (a.pi_period > 0) {
-            const uint64_t per = (uint64_t)a.pi_period;
-            const uint64_t pd[3] = {per * kD, ((uint64_t)a.S + per - 1) / per, units};
-            const uint64_t ps[2] = {per * kD * 2, (uint64_t)a.S * kD * 2};
-            ok = ok && encode_tmap_3d(&p.kpimap, a.k, true, pd, ps, box120, true) &&
-                 encode_tmap_3d(&p.vpimap, a.v, true, pd, ps, box120, true) &&
-                 encode_tmap_3d(&p.kpi8map, a.k, true, pd, ps, box8, true) &&
-                 encode_tmap_3d(&p.vpi8map, a.v, true, pd, ps, box8, true);
-        }
+    const uint64_t kd[3] = {(uint64_t)kD, (uint64_t)a.S, units};
+    const uint64_t ks[2] = {(uint64_t)kD * 2, (uint64_t)a.S * kD * 2};
+    bool ok = encode_tmap_3d(&p.qmap, a.q, true, qd, qs, qbox, true) &&
+              encode_tmap_3d(&p.kmap, a.k, true, kd, ks, box120, true) &&
+              encode_tmap_3d(&p.vmap, a.v, true, kd, ks, box120, true) &&
+              encode_tmap_3d(&p.k8map, a.k, true, kd, ks, box8, true) &&
+              encode_tmap_3d(&p.v8map, a.v, true, kd, ks, box8, true);
+    p.kpimap = p.vpimap = p.kpi8map = p.vpi8map = p.qmap;  // unused without pi-Attention
+    if (a.pi_period > 0) {
+        const uint64_t per = (uint64_t)a.pi_period;
+        const uint64_t pd[3] = {per * kD, ((uint64_t)a.S + per - 1) / per, units};
+        const uint64_t ps[2] = {per * kD * 2, (uint64_t)a.S * kD * 2};
+        ok = ok && encode_tmap_3d(&p.kpimap, a.k, true, pd, ps, box120, true) &&
+             encode_tmap_3d(&p.vpimap, a.v, true, pd, ps, box120, true) &&
+             encode_tmap_3d(&p.kpi8map, a.k, true, pd, ps, box8, true) &&
+             encode_tmap_3d(&p.vpi8map, a.v, true, pd, ps, box8, true);
     }
     if (!ok)
         return cudaErrorInvalidValue;

@@ -39,12 +39,15 @@ def test_paged_matches_oracle_and_contiguous(page):
     ro, rl = oracle.decode_paged(x["q"], kp, vp, bt.numpy(), lens, x["scale"])
     check_out(out.cpu().numpy().reshape(-1, 128), ro, bf16=False)
     check_lse(lse.cpu().numpy().reshape(-1), rl)
-    # the contiguous decode of the same cache (padded to the same S) is identical
+    # the contiguous decode of the same cache (padded to the same S) agrees:
+    # for this shape it runs on the tensor cores and the paged one on the CUDA
+    # cores, so the two agree to rounding, within the oracle tolerances
     sl = torch.tensor(lens, dtype=torch.int32, device=DEV)
     o2, l2 = ta.decode(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), seqlens=sl, scale=x["scale"],
                        out_dtype=torch.float32)
     torch.cuda.synchronize()
-    assert torch.equal(out, o2) and torch.equal(lse, l2)
+    check_out(out.cpu().numpy().reshape(-1, 128), o2.cpu().numpy().reshape(-1, 128).astype(np.float64), bf16=False)
+    check_lse(lse.cpu().numpy().reshape(-1), l2.cpu().numpy().reshape(-1).astype(np.float64))
     assert ta.decode_status() == 0
 
 
