@@ -957,6 +957,8 @@ cudaError_t launch_decode(const DecodeLaunch &a)
 {
     if (decode_tc_eligible(a))
         return launch_decode_tc(a);
+    if (decode_fp8_tc_eligible(a))
+        return launch_decode_fp8_tc(a);
     DecodeParams p;
     p.q = a.q;
     p.k = a.k;

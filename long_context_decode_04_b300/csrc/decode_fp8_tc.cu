@@ -1,0 +1,819 @@
+// decode_fp8_tc.cu -- split-KV exact decode over an FP8 (E4M3) KV cache for
+// grouped-query attention, with both contractions on the tensor cores.
+//
+// What is computed is the decode of decode_tc.cu (Attention glossary,
+// jisaku.com/glossary/attention, "basic concepts and operating principle";
+// partials merged by the log-sum-exp rule of the Tree Attention explainer,
+// aibr.jp/archives/143699, sections 1 and 3) over a cache stored in low
+// precision and computed in higher precision (the ThriftAttention page,
+// hyperion-consulting.io, "the rise of FP4" and the COMPUTE layer): K and V
+// are E4M3 codes with one fp32 dequantisation factor per (sequence, KV
+// head) each, q is bf16.  The K factor scales the scores, the V factor the
+// partial.  Same chunks of whole 120-key tiles, same partials.
+//
+// The tensor cores take 16-bit operands, so each tile is widened on chip:
+// E4M3 is a subset of fp16, and cvt.rn.f16x2.e4m3x2 widens two codes
+// exactly.  The raw codes arrive by TMA in a ring of stages that is
+// released as soon as a tile is widened, so most of the ring is in flight.
+//   S^T [128 keys x 16] = K [128 x D] . Q^T   A = K in TMEM (fp16, written by
+//                                            the converting threads, one key
+//                                            row per TMEM lane), B = q as fp16
+//                                            (K-major, 128-byte swizzle)
+//   O_t^T [D x 32]      = V^T . P^T          A = V as fp16 in shared memory
+//                                            (MN-major, 128-byte swizzle),
+//                                            B = P, one row per (softmax
+//                                            warp, head), hi then lo parts
+// Queries are used as fp16 values (exact for bf16 values of magnitude in
+// [2^-14, 65504]).
+//
+// Kernel layout (one persistent CTA per SM, 12 warps):
+//   * warp 0: producer.  Work items (sequence, KV head, chunk) from the
+//     device-wide queue; the item's G query rows widened to fp16 into one of
+//     two Q buffers; raw K and V tiles (120 rows of 128 codes) by TMA into a
+//     3-stage ring.
+//   * warp 1: TMEM (512 columns: S and O double buffers, three K buffers)
+//     and the score products; warp 2: the value products.
+//   * warps 4-7: softmax and accumulation, as in decode_tc.cu (each warp its
+//     own online softmax over its 32 keys, per-warp references raised
+//     lazily, the four warps merged at the item end).
+//   * warps 8-11 (TMEM lane quadrants 0-3): widen a tile: thread r writes
+//     key row r of K into TMEM, and the threads write V as fp16 into shared
+//     memory (zero for keys past the tile's end); then the raw stage is free.
+//   * Every wait is bounded (kWaitLimitNs); on expiry the kernel records
+//     TA_DEVERR_TIMEOUT, stops, lets its copies and MMAs land and frees its
+//     TMEM.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace ta {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTile = kDecodeTileKeys;  // 120 keys a tile
+constexpr int kRows = 128;              // MMA rows: rows 120-127 are zero / masked
+constexpr int kN = 16;                  // score-product N: the group's heads, zero-padded
+constexpr int kON = 2 * kN;             // value-product N: (warp, head) columns, hi then lo
+constexpr int kRawStages = 3;
+constexpr int kConvBufs = 3;                      // widened tiles (K in TMEM, V in shared memory)
+constexpr int kRawTile = kTile * kD;              // 120 rows of 128 one-byte codes
+constexpr int kRawStage = 2 * kRawTile;           // K then V
+constexpr int kHalf = kRows * 128;                // one 64-dim half of an fp16 V tile
+constexpr int kVBytes = 2 * kHalf;                // 32 KiB
+constexpr int kQHalf = kN * 128;
+constexpr int kQBytes = 2 * kQHalf;
+constexpr int kPHalf = kON * 128;
+constexpr int kPBytes = 2 * kPHalf;
+constexpr int kVOff = 0;                          // kConvBufs fp16 V tiles
+constexpr int kQOff = kVOff + kConvBufs * kVBytes;  // two fp16 Q operands
+constexpr int kPOff = kQOff + 2 * kQBytes;        // two P operands
+constexpr int kRawOff = kPOff + 2 * kPBytes;      // the raw ring
+constexpr int kMiscOff = kRawOff + kRawStages * kRawStage;
+constexpr uint32_t kRawTx = (uint32_t)kRawStage;  // bytes of one raw stage
+constexpr int kDescRing = 8;
+constexpr int kSoftWarp0 = 4;
+constexpr int kConvWarp0 = 8;
+constexpr int kSoftThreads = 128;
+constexpr int kThreads = 384;
+constexpr uint32_t kOCol = 2 * kN;                // S at TMEM columns 0, 16; O at 32, 64
+constexpr uint32_t kKCol = kOCol + 2 * kON;       // K at 96, 160, 224
+constexpr uint32_t kTmemCols = 512;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kRescaleLog2 = 8.0f;
+
+enum : int { kFirst = 1, kLast = 2, kEnd = 4 };
+enum : int { kModeFinal = 0, kModePartials = 1, kModeFused = 2 };
+
+struct TileDesc {
+    int item;
+    int j0;
+    int n;
+    int flags;
+};
+
+struct Misc {
+    uint64_t raw_full[kRawStages];   // raw codes landed (TMA bytes), descriptor written
+    uint64_t raw_empty[kRawStages];  // raw codes widened (128 converting threads)
+    uint64_t conv_full[kConvBufs];   // K in TMEM and V as fp16 (128 converting threads)
+    uint64_t conv_empty[kConvBufs];  // the value product of the tile read them (MMA commit)
+    uint64_t s_full[2];              // S in TMEM (MMA commit) and its descriptor (score issuer)
+    uint64_t p_full[2][4];           // a warp's P (32 threads)
+    uint64_t p_all[2];               // all four warps' P and factors (128 threads)
+    uint64_t o_full[2];
+    uint64_t o_empty[2];
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
+    uint64_t grp_bar;
+    uint64_t mma_done;
+    TileDesc desc[kDescRing];        // tile t's descriptor at t % kDescRing
+    float alpha[4][4][4];            // [tile % 4][warp][head]
+    float lred[4][4];
+    float mred[4][4];
+    uint32_t tmem_base;
+    int abort;
+    int ticket;
+};
+
+constexpr size_t kSmem = (size_t)kMiscOff + sizeof(Misc) + 1024;  // + alignment slack
+static_assert(kSmem <= 232448, "shared memory per CTA");
+static_assert(kRawTile % 1024 == 0 && kRawOff % 1024 == 0, "raw tiles on 1024-byte boundaries (swizzle atoms)");
+static_assert(kTile * 16 % kSoftThreads == 0, "V widening tasks per thread");
+
+struct Fp8Params {
+    CUtensorMap kmap, vmap;  // raw codes (D, S, B*Hkv), box 128 x 120
+    const __nv_bfloat16 *q;
+    void *out;
+    float *lse;
+    int B, Hq, Hkv, S;
+    float qscale;  // scale * log2(e)
+    const int32_t *seqlens;
+    int n_split, chunk, n_items;
+    int mode;
+    int32_t *status;
+    int32_t *counters;
+    float *part_m, *part_l, *part_o;
+    const float *k_scale, *v_scale;  // per (sequence, KV head), or nullptr (1)
+};
+
+__device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Two E4M3 codes (low byte first) to a packed fp16 pair (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two));
+    return r;
+}
+
+// Four codes of a word to two fp16 pairs.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    lo = e4m3x2_to_f16x2(w & 0xffffu);
+    hi = e4m3x2_to_f16x2(w >> 16);
+}
+
+template <int G, typename OUT>
+__global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid_constant__ Fp8Params p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    Misc *ms = reinterpret_cast<Misc *>(smem + kMiscOff);
+    volatile int *abort_flag = &ms->abort;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Zero the fp16 V tiles (rows 120-127 stay zero), the Q operands (rows
+    // G..15 stay zero) and the P operands.
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < kRawOff / 16; i += kThreads)
+        *reinterpret_cast<uint4 *>(smem + i * 16) = z4;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRawStages; ++s) {
+            mbar_init(&ms->raw_full[s], 1);
+            mbar_init(&ms->raw_empty[s], kSoftThreads);
+        }
+        for (int i = 0; i < kConvBufs; ++i) {
+            mbar_init(&ms->conv_full[i], kSoftThreads);
+            mbar_init(&ms->conv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ms->s_full[i], 2);
+            for (int w = 0; w < 4; ++w)
+                mbar_init(&ms->p_full[i][w], 32);
+            mbar_init(&ms->p_all[i], kSoftThreads);
+            mbar_init(&ms->o_full[i], 1);
+            mbar_init(&ms->o_empty[i], kSoftThreads);
+            mbar_init(&ms->q_full[i], 1);
+            mbar_init(&ms->q_empty[i], 1);
+        }
+        mbar_init(&ms->grp_bar, 4);
+        mbar_init(&ms->mma_done, 2);  // both MMA issuers commit
+        ms->abort = 0;
+        ms->ticket = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&ms->tmem_base, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = ms->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const bool leader = lane == 0;
+        if (leader) {
+            tc::prefetch_tensormap(&p.kmap);
+            tc::prefetch_tensormap(&p.vmap);
+        }
+        const uint64_t policy = l2_policy_evict_first();
+        int stage = 0, ti = 0, ic = 0;
+        uint32_t uses[kRawStages] = {};
+        uint32_t q_uses[2] = {0u, 0u};
+        bool ok = true;
+        while (ok) {
+            int item = 0;
+            if (leader)
+                item = atomicAdd(&p.status[16], 1);
+            item = __shfl_sync(kFull, item, 0);
+            if (item >= p.n_items) {
+                int w = 1;
+                if (leader) {
+                    if (item == p.n_items + (int)gridDim.x - 1)
+                        atomicExch(&p.status[16], 0);  // last grab of the launch: reset the queue
+                    if (uses[stage] > 0)
+                        w = mbar_wait_bounded(&ms->raw_empty[stage], (uses[stage] - 1) & 1, abort_flag);
+                    if (w) {
+                        ms->desc[ti & (kDescRing - 1)] = TileDesc{item, 0, 0, kEnd};
+                        mbar_arrive(&ms->raw_full[stage]);
+                    }
+                }
+                if (__shfl_sync(kFull, w, 0))
+                    ++uses[stage];
+                break;
+            }
+            const int unit = item / p.n_split;
+            const int split = item - unit * p.n_split;
+            const int b = unit / p.Hkv;
+            int L = p.S;
+            if (p.seqlens) {
+                L = p.seqlens[b];
+                if (L < 0 || L > p.S) {
+                    if (leader)
+                        atomicOr(&p.status[0], TA_DEVERR_SEQLEN);
+                    L = L < 0 ? 0 : p.S;
+                }
+            }
+            const int c0 = split * p.chunk;
+            const int c1 = min(c0 + p.chunk, L);
+            // the item's G query rows as fp16: 16-byte chunk c of head h
+            // (8 dims) to row h of the operand, 128-byte swizzle
+            const int qb = ic & 1;
+            int w = 1;
+            if (leader && q_uses[qb] > 0)
+                w = mbar_wait_bounded(&ms->q_empty[qb], (q_uses[qb] - 1) & 1, abort_flag);
+            if (!__shfl_sync(kFull, w, 0))
+                break;
+            unsigned char *qd = smem + kQOff + qb * kQBytes;
+            const __nv_bfloat16 *qsrc = p.q + (size_t)unit * G * kD;
+            for (int i = lane; i < G * 16; i += 32) {
+                const int h = i >> 4, c = i & 15;
+                const uint4 x = *reinterpret_cast<const uint4 *>(qsrc + h * kD + c * 8);
+                const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+                uint32_t hv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    hv[k] = tc::pack_f16x2(bf16_lo(wv[k]), bf16_hi(wv[k]));
+                *reinterpret_cast<uint4 *>(qd + (c >> 3) * kQHalf + h * 128 + ((((c & 7) ^ h) & 7) << 4)) =
+                    make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (leader)
+                mbar_arrive(&ms->q_full[qb]);
+            ++q_uses[qb];
+            ++ic;
+            int j0 = c0, flags = kFirst;
+            for (;;) {
+                const int n = max(0, min(kTile, c1 - j0));
+                const bool last = j0 + n >= c1;
+                if (last)
+                    flags |= kLast;
+                w = 1;
+                if (leader) {
+                    if (uses[stage] > 0)
+                        w = mbar_wait_bounded(&ms->raw_empty[stage], (uses[stage] - 1) & 1, abort_flag);
+                    if (w) {
+                        ms->desc[ti & (kDescRing - 1)] = TileDesc{item, j0, n, flags};
+                        uint64_t *fb = &ms->raw_full[stage];
+                        if (n > 0) {
+                            // rows past S read as zero; V rows in [n, 120) are
+                            // written as zero by the converting threads
+                            unsigned char *rd = smem + kRawOff + stage * kRawStage;
+                            mbar_arrive_expect_tx(fb, kRawTx);
+                            tc::tma_load_3d_hint(rd, &p.kmap, 0, j0, unit, fb, policy);
+                            tc::tma_load_3d_hint(rd + kRawTile, &p.vmap, 0, j0, unit, fb, policy);
+                        } else {
+                            mbar_arrive(fb);
+                        }
+                    }
+                }
+                if (!__shfl_sync(kFull, w, 0)) {
+                    ok = false;
+                    break;
+                }
+                ++uses[stage];
+                ++ti;
+                if (++stage == kRawStages)
+                    stage = 0;
+                if (last)
+                    break;
+                j0 += n;
+                flags = 0;
+            }
+        }
+        __syncwarp();
+        if (leader) {
+            int drain_abort = 0;
+            for (int s = 0; s < kRawStages; ++s)
+                if (uses[s] > 0)
+                    mbar_wait_bounded(&ms->raw_full[s], (uses[s] - 1) & 1, &drain_abort);
+        }
+        __syncwarp();
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ MMA issuers
+        if (lane == 0) {
+            const uint32_t sbase = smem_u32(smem);
+            int t = 0;
+            if (warp == 1) {
+                // score products: S_t^T = K Q^T, K from TMEM, 8 steps of 16 dims
+                constexpr uint32_t kIdS = tc::idesc_f16_f32(kRows, kN, false);
+                int ic = 0;
+                for (;;) {
+                    if (!mbar_wait_bounded(&ms->conv_full[t % kConvBufs], (t / kConvBufs) & 1, abort_flag))
+                        break;
+                    const TileDesc d = ms->desc[t & (kDescRing - 1)];
+                    // S and P buffers of this parity are free once the value
+                    // product of tile t - 2 is done
+                    if (t >= 2 && !mbar_wait_bounded(&ms->o_full[t & 1], ((t - 2) >> 1) & 1, abort_flag))
+                        break;
+                    if (d.flags & kEnd) {
+                        mbar_arrive(&ms->s_full[t & 1]);  // tells the softmax warps to stop
+                        mbar_arrive(&ms->s_full[t & 1]);
+                        break;
+                    }
+                    const int qb = ic & 1;
+                    if ((d.flags & kFirst) && !mbar_wait_bounded(&ms->q_full[qb], (ic >> 1) & 1, abort_flag))
+                        break;
+                    tc::fence_after_sync();
+                    const uint32_t s_tm = tmem + (t & 1) * kN;
+                    const uint32_t k_tm = tmem + kKCol + (t % kConvBufs) * (kD / 2);
+                    const uint32_t qa = sbase + kQOff + qb * kQBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
+                        tc::mma_ts(s_tm, k_tm + kk * 8, tc::sw128_desc(qa + qo, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                    }
+                    // the commit arrives when S is in TMEM; the plain arrive
+                    // releases the descriptor this thread acquired
+                    tc::commit(&ms->s_full[t & 1]);
+                    mbar_arrive(&ms->s_full[t & 1]);
+                    if (d.flags & kLast) {
+                        tc::commit(&ms->q_empty[qb]);
+                        ++ic;
+                    }
+                    ++t;
+                }
+            } else {
+                // value products: O_t^T = V^T P^T, V fp16 MN-major, P K-major
+                constexpr uint32_t kIdPV = tc::idesc_f16_f32_major(kRows, kON, true, false);
+                for (;;) {
+                    if (!mbar_wait_bounded(&ms->conv_full[t % kConvBufs], (t / kConvBufs) & 1, abort_flag))
+                        break;
+                    if (ms->desc[t & (kDescRing - 1)].flags & kEnd)
+                        break;
+                    if (!mbar_wait_bounded(&ms->o_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag))
+                        break;
+                    const uint32_t o_tm = tmem + kOCol + (t & 1) * kON;
+                    const uint32_t vb = sbase + kVOff + (t % kConvBufs) * kVBytes;
+                    const uint32_t pb = sbase + kPOff + (t & 1) * kPBytes;
+                    bool ok = true;
+#pragma unroll
+                    for (int w = 0; w < 4 && ok; ++w) {
+                        ok = mbar_wait_bounded(&ms->p_full[t & 1][w], (t >> 1) & 1, abort_flag);
+                        if (!ok)
+                            break;
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const int kk = 2 * w + i;
+                            const uint64_t a = tc::sw128_desc(vb + kk * 2048, kHalf, 1024);
+                            const uint32_t po = (kk >> 2) * kPHalf + (kk & 3) * 32;
+                            tc::mma_ss(o_tm, a, tc::sw128_desc(pb + po, 16, 1024), kIdPV, kk > 0 ? 1u : 0u);
+                        }
+                    }
+                    if (!ok)
+                        break;
+                    tc::commit(&ms->o_full[t & 1]);
+                    tc::commit(&ms->conv_empty[t % kConvBufs]);
+                    ++t;
+                }
+            }
+            tc::commit(&ms->mma_done);
+            int drain_abort = 0;
+            mbar_wait_bounded(&ms->mma_done, 0, &drain_abort);
+        }
+        __syncwarp();
+    } else if (warp >= kConvWarp0) {
+        // ------------------------------------------------------------ widening
+        const int cq = warp - kConvWarp0;  // TMEM lane quadrant (warp % 4)
+        const int ct = cq * 32 + lane;     // key row (K), and work index (V)
+        const uint32_t lane_base = (uint32_t)(cq * 32) << 16;
+        int t = 0, stage = 0;
+        uint32_t rph = 0;
+        for (;;) {
+            bool w = mbar_wait_bounded(&ms->raw_full[stage], rph, abort_flag);
+            const TileDesc d = ms->desc[t & (kDescRing - 1)];
+            const int cv = t % kConvBufs;
+            w = w && mbar_wait_bounded(&ms->conv_empty[cv], ((t / kConvBufs) & 1) ^ 1, abort_flag);
+            if (!__all_sync(kFull, w))
+                break;
+            if (d.flags & kEnd) {
+                mbar_arrive(&ms->conv_full[cv]);  // the issuers read the end from the descriptor
+                break;
+            }
+            const unsigned char *rk = smem + kRawOff + stage * kRawStage;
+            const unsigned char *rv = rk + kRawTile;
+            // K row ct into TMEM lane ct: 128 codes -> 64 fp16 pairs (the raw
+            // rows are swizzled, so the 32 lanes' chunks fall in 8 bank groups)
+            {
+                uint32_t kr[32];
+                uint32_t kh[32];
+                if (ct < kTile) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(rk + ct * kD + ((c ^ (ct & 7)) << 4));
+                        kr[4 * c + 0] = x.x;
+                        kr[4 * c + 1] = x.y;
+                        kr[4 * c + 2] = x.z;
+                        kr[4 * c + 3] = x.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        kr[i] = 0u;
+                }
+                const uint32_t k_tm = tmem + lane_base + kKCol + cv * (kD / 2);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        e4m3x4_to_f16(kr[16 * half + i], kh[2 * i], kh[2 * i + 1]);
+                    tc::tmem_st32(k_tm + 32 * half, kh);
+                }
+            }
+            // V: task i = (row r, half h, fp16 chunk fc) -> the 8 codes of dims
+            // 64h + 8fc .. + 7 as one 16-byte fp16 chunk (zero past the
+            // tile's end); 8 lanes cover a 128-byte half-row.  All loads first.
+            unsigned char *vd = smem + kVOff + cv * kVBytes;
+            constexpr int kVTasks = kTile * 16 / kSoftThreads;  // 15 a thread
+            uint2 vx[kVTasks];
+#pragma unroll
+            for (int k = 0; k < kVTasks; ++k) {
+                const int i = ct + k * kSoftThreads;
+                const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
+                const int c16 = h * 4 + (fc >> 1);  // raw 16-byte chunk, swizzled
+                vx[k] = r < d.n ? *reinterpret_cast<const uint2 *>(rv + r * kD + ((c16 ^ (r & 7)) << 4) + (fc & 1) * 8)
+                                : make_uint2(0u, 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < kVTasks; ++k) {
+                const int i = ct + k * kSoftThreads;
+                const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
+                uint32_t f[4];
+                e4m3x4_to_f16(vx[k].x, f[0], f[1]);
+                e4m3x4_to_f16(vx[k].y, f[2], f[3]);
+                *reinterpret_cast<uint4 *>(vd + h * kHalf + r * 128 + ((fc ^ (r & 7)) << 4)) =
+                    make_uint4(f[0], f[1], f[2], f[3]);
+            }
+            tc::tmem_wait_st();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc::fence_before_sync();
+            mbar_arrive(&ms->conv_full[cv]);
+            mbar_arrive(&ms->raw_empty[stage]);
+            ++t;
+            if (++stage == kRawStages) {
+                stage = 0;
+                rph ^= 1;
+            }
+        }
+    } else if (warp >= kSoftWarp0) {
+        // ------------------------------------------------------------ softmax + accumulation
+        const int q4 = warp - kSoftWarp0;  // TMEM lane quadrant (warp % 4)
+        const int row = q4 * 32 + lane;    // key row of a tile; output dimension
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        uint32_t gph = 0;
+        int t = 0;
+        float mw[G], l_run[G], o[4][G];
+        int unit = 0, split = 0, b = 0, kvh = 0;
+        float qs = p.qscale;
+        auto group_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ms->grp_bar);
+            const bool w = mbar_wait_bounded(&ms->grp_bar, gph, abort_flag);
+            gph ^= 1;
+            return __all_sync(kFull, w);
+        };
+        auto accumulate = [&](int x) -> bool {
+            bool w = mbar_wait_bounded(&ms->o_full[x & 1], (x >> 1) & 1, abort_flag);
+            w = w && mbar_wait_bounded(&ms->p_all[x & 1], (x >> 1) & 1, abort_flag);  // the factors
+            if (!__all_sync(kFull, w))
+                return false;
+            tc::fence_after_sync();
+            uint32_t r[32];
+            tc::tmem_ld32(tmem + lane_base + kOCol + (x & 1) * kON, r);
+            tc::tmem_wait_ld(r);
+#pragma unroll
+            for (int w2 = 0; w2 < 4; ++w2)
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const int c = w2 * G + g;
+                    const float ov = __uint_as_float(r[c]) + __uint_as_float(r[kN + c]);
+                    o[w2][g] = fmaf(o[w2][g], ms->alpha[x & 3][w2][g], ov);
+                }
+            tc::fence_before_sync();
+            mbar_arrive(&ms->o_empty[x & 1]);
+            return true;
+        };
+        for (;;) {
+            const bool w = mbar_wait_bounded(&ms->s_full[t & 1], (t >> 1) & 1, abort_flag);  // S, descriptor
+            if (!__all_sync(kFull, w))
+                break;
+            const TileDesc d = ms->desc[t & (kDescRing - 1)];
+            if (d.flags & kEnd)
+                break;
+            if (d.flags & kFirst) {
+                unit = d.item / p.n_split;
+                split = d.item - unit * p.n_split;
+                b = unit / p.Hkv;
+                kvh = unit - b * p.Hkv;
+                qs = p.k_scale ? p.qscale * p.k_scale[unit] : p.qscale;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    mw[g] = -INFINITY;
+                    l_run[g] = 0.f;
+#pragma unroll
+                    for (int w2 = 0; w2 < 4; ++w2)
+                        o[w2][g] = 0.f;
+                }
+            }
+            tc::fence_after_sync();
+            uint32_t sr[G];
+            tc::tmem_ld_small<G>(tmem + lane_base + (t & 1) * kN, sr);
+            const bool valid = row < d.n;
+            float s[G], mx[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                s[g] = valid ? __uint_as_float(sr[g]) * qs : -INFINITY;  // log2 units
+                mx[g] = s[g];
+            }
+            // lazy per-warp reference: raised only when a score exceeds it by
+            // more than 2^8 (warp vote), so the weights stay below 2^8
+            float alpha[G], pw[G];
+            bool need = false;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                alpha[g] = 1.f;
+                need |= s[g] > mw[g] + kRescaleLog2;
+            }
+            if (__any_sync(kFull, need)) {
+#pragma unroll
+                for (int mask = 16; mask >= 1; mask >>= 1)
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        mx[g] = fmaxf(mx[g], __shfl_xor_sync(kFull, mx[g], mask));
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (mx[g] > mw[g] + kRescaleLog2) {
+                        alpha[g] = mw[g] == -INFINITY ? 0.f : fast_exp2(mw[g] - mx[g]);
+                        l_run[g] *= alpha[g];
+                        mw[g] = mx[g];
+                    }
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                pw[g] = mw[g] == -INFINITY ? 0.f : fast_exp2(s[g] - mw[g]);
+                l_run[g] += pw[g];
+            }
+            if (lane < G) {
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    if (lane == g)
+                        ms->alpha[t & 3][q4][g] = alpha[g];
+            }
+            // P^T: rows w*G + g (hi) and 16 + w*G + g (lo), column `row`,
+            // fp16 (the type of V), 128-byte swizzle
+            unsigned char *pbase = smem + kPOff + (t & 1) * kPBytes;
+            const int cb = (row & 63) * 2;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const int rh = q4 * G + g, rl = kN + rh;
+                const int base = (row >> 6) * kPHalf + (cb & 15);
+                const __half hi = __float2half_rn(pw[g]);
+                const __half lo = __float2half_rn(pw[g] - __half2float(hi));
+                *reinterpret_cast<__half *>(pbase + base + rh * 128 + ((((cb >> 4) ^ rh) & 7) << 4)) = hi;
+                *reinterpret_cast<__half *>(pbase + base + rl * 128 + ((((cb >> 4) ^ rl) & 7) << 4)) = lo;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc::fence_before_sync();
+            mbar_arrive(&ms->p_full[t & 1][q4]);
+            mbar_arrive(&ms->p_all[t & 1]);
+            if (!(d.flags & kFirst) && !accumulate(t - 1))
+                break;
+            const int tt = t;
+            ++t;
+            if (!(d.flags & kLast))
+                continue;
+            if (!accumulate(tt))
+                break;
+
+            // ---- end of item: merge the four warps' states
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float v = l_run[g];
+#pragma unroll
+                for (int mask = 16; mask >= 1; mask >>= 1)
+                    v += __shfl_xor_sync(kFull, v, mask);
+                if (lane == g) {
+                    ms->lred[q4][g] = v;
+                    ms->mred[q4][g] = mw[g];
+                }
+            }
+            if (!group_sync())
+                break;
+            const float vs = p.v_scale ? p.v_scale[unit] : 1.f;  // value dequantisation factor
+            float ls[G], mt[G], of[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                mt[g] = fmax3(ms->mred[0][g], ms->mred[1][g], fmaxf(ms->mred[2][g], ms->mred[3][g]));
+                ls[g] = 0.f;
+                of[g] = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < 4; ++w2) {
+                    const float m2 = ms->mred[w2][g];
+                    const float be = m2 == -INFINITY ? 0.f : fast_exp2(m2 - mt[g]);
+                    ls[g] = fmaf(ms->lred[w2][g], be, ls[g]);
+                    of[g] = fmaf(o[w2][g], be, of[g]);
+                }
+                of[g] *= vs;
+            }
+            const size_t row0 = (size_t)b * p.Hq + (size_t)kvh * G;
+            if (p.mode == kModeFinal) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float inv = ls[g] > 0.f ? 1.0f / ls[g] : 0.f;
+                    store_out(static_cast<OUT *>(p.out) + (row0 + g) * kD + row, of[g] * inv);
+                    if (row == g && p.lse)
+                        p.lse[row0 + g] = ls[g] > 0.f ? (mt[g] + fast_log2(ls[g])) * kLn2 : -INFINITY;
+                }
+                continue;
+            }
+            const int ns = p.n_split;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const size_t pi = (row0 + g) * ns + split;
+                p.part_o[pi * kD + row] = of[g];
+                if (row == g) {
+                    p.part_m[pi] = mt[g] == -INFINITY ? -INFINITY : mt[g] * kLn2;
+                    p.part_l[pi] = ls[g];
+                }
+            }
+            if (p.mode != kModeFused)
+                continue;
+
+            // ---- fused merge: the CTA that writes a unit's last partial merges it
+            if (!group_sync())
+                break;
+            if (row == 0) {
+                int last = 0;
+                if (atomic_add_acq_rel_gpu(&p.counters[unit], 1) == ns - 1) {
+                    last = 1;
+                    p.counters[unit] = 0;  // ready for the next launch
+                }
+                *reinterpret_cast<volatile int *>(&ms->ticket) = last;
+            }
+            if (!group_sync())
+                break;
+            if (!*reinterpret_cast<volatile int *>(&ms->ticket))
+                continue;
+            for (int idx = row; idx < G * kD / 4; idx += kSoftThreads) {
+                const int h = idx / (kD / 4);
+                const int d4 = (idx - h * (kD / 4)) * 4;
+                const size_t pr = (row0 + h) * ns;
+                const float4 *po = reinterpret_cast<const float4 *>(p.part_o + pr * kD + d4);
+                float mx2 = -INFINITY, lsum = 0.f;
+                float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int n0 = 0; n0 < ns; n0 += 8) {
+                    float mb[8], lb[8];
+                    float4 ob[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        mb[i] = -INFINITY;
+                        if (n0 + i < ns) {
+                            mb[i] = __ldcg(p.part_m + pr + n0 + i);
+                            lb[i] = __ldcg(p.part_l + pr + n0 + i);
+                            ob[i] = __ldcg(po + (size_t)(n0 + i) * (kD / 4));
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (mb[i] != -INFINITY) {
+                            const float mn = fmaxf(mx2, mb[i]);
+                            const float sc = fast_exp2((mx2 - mn) * kLog2e);
+                            const float a = fast_exp2((mb[i] - mn) * kLog2e);
+                            lsum = fmaf(lsum, sc, a * lb[i]);
+                            os.x = fmaf(os.x, sc, a * ob[i].x);
+                            os.y = fmaf(os.y, sc, a * ob[i].y);
+                            os.z = fmaf(os.z, sc, a * ob[i].z);
+                            os.w = fmaf(os.w, sc, a * ob[i].w);
+                            mx2 = mn;
+                        }
+                    }
+                }
+                const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+                OUT *dst = static_cast<OUT *>(p.out) + (row0 + h) * kD + d4;
+                store_out(dst + 0, os.x * inv);
+                store_out(dst + 1, os.y * inv);
+                store_out(dst + 2, os.z * inv);
+                store_out(dst + 3, os.w * inv);
+                if (d4 == 0 && p.lse)
+                    p.lse[row0 + h] = lsum > 0.f ? mx2 + fast_log2(lsum) * kLn2 : -INFINITY;
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag)
+        atomicOr(&p.status[0], TA_DEVERR_TIMEOUT);
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int G, typename OUT>
+cudaError_t launch_typed(const DecodeLaunch &a, const Fp8Params &p)
+{
+    auto kern = decode_fp8_tc_kernel<G, OUT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess)
+        return e;
+    kern<<<a.plan.grid, kThreads, kSmem, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_fp8_tc_eligible(const DecodeLaunch &a)
+{
+    const int G = a.Hq / a.Hkv;
+    return a.kv_fp8 && a.D == kD && (G == 2 || G == 4) && !a.block_table && a.pi_period == 0;
+}
+
+cudaError_t launch_decode_fp8_tc(const DecodeLaunch &a)
+{
+    const int G = a.Hq / a.Hkv;
+    Fp8Params p;
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
+    p.out = a.out;
+    p.lse = a.lse;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.S = a.S;
+    p.qscale = a.scale * kLog2e;
+    p.seqlens = a.seqlens;
+    p.n_split = a.plan.n_split;
+    p.chunk = a.plan.chunk;
+    p.n_items = a.B * a.Hkv * a.plan.n_split;
+    if (a.force_partials)
+        p.mode = kModePartials;
+    else if (a.plan.n_split == 1)
+        p.mode = kModeFinal;
+    else
+        p.mode = decode_merges_itself(a.plan.n_split, a.B * a.Hkv) ? kModeFused : kModePartials;
+    p.status = a.status;
+    p.counters = a.counters;
+    p.part_m = a.part_m;
+    p.part_l = a.part_l;
+    p.part_o = a.part_o;
+    p.k_scale = a.k_scale;
+    p.v_scale = a.v_scale;
+    // K, V codes [B, Hkv, S, D] as (D, S, B*Hkv), one byte each, box 128 x 120,
+    // 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r % 8))
+    const uint64_t units = (uint64_t)a.B * a.Hkv;
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.S, units};
+    const uint64_t strides[2] = {(uint64_t)kD, (uint64_t)a.S * kD};
+    const uint32_t box[3] = {(uint32_t)kD, (uint32_t)kTile, 1};
+    if (!encode_tmap_3d_u8(&p.kmap, a.k, dims, strides, box, true) ||
+        !encode_tmap_3d_u8(&p.vmap, a.v, dims, strides, box, true))
+        return cudaErrorInvalidValue;
+    const bool bf16_out = a.out_dtype == TA_BF16;
+    if (G == 2)
+        return bf16_out ? launch_typed<2, __nv_bfloat16>(a, p) : launch_typed<2, float>(a, p);
+    return bf16_out ? launch_typed<4, __nv_bfloat16>(a, p) : launch_typed<4, float>(a, p);
+}
+
+}  // namespace ta

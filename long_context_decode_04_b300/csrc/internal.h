@@ -74,6 +74,10 @@ inline int64_t pi_max_keys(int64_t S, int64_t window, int64_t period)
 bool encode_tmap_3d(CUtensorMap *m, const void *base, bool bf16, const uint64_t dims[3], const uint64_t strides[2],
                     const uint32_t box[3], bool swizzle128);
 
+// The same for one-byte elements (FP8 codes).
+bool encode_tmap_3d_u8(CUtensorMap *m, const void *base, const uint64_t dims[3], const uint64_t strides[2],
+                       const uint32_t box[3], bool swizzle128);
+
 // Scheduler (sched.cpp).
 ta_status plan_decode(int B, int Hq, int Hkv, int S, int D, int chunk, int n_split, int varlen,
                       int sm_count, ta_decode_plan *plan, const char **why);
@@ -87,6 +91,10 @@ cudaError_t launch_decode(const DecodeLaunch &a);
 // D = 128, G = 2 or 4; launch_decode hands such launches to it.
 bool decode_tc_eligible(const DecodeLaunch &a);
 cudaError_t launch_decode_tc(const DecodeLaunch &a);
+// The tensor-core decode over an E4M3 cache (decode_fp8_tc.cu): contiguous
+// cache, D = 128, G = 2 or 4.
+bool decode_fp8_tc_eligible(const DecodeLaunch &a);
+cudaError_t launch_decode_fp8_tc(const DecodeLaunch &a);
 cudaError_t launch_combine(const float *m, const float *l, const float *o, int R, int N, int D, void *out,
                            ta_dtype out_dtype, float *lse, void *scratch, cudaStream_t stream);
 cudaError_t launch_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse, int B,

@@ -88,6 +88,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_major(int M, int N, bool a
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// fp16 A and B, f32 accumulator, with the major-ness of each operand given.
+__host__ __device__ constexpr uint32_t idesc_f16_f32_major(int M, int N, bool a_mn_major, bool b_mn_major)
+{
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Same with fp16 A and B (A and B of one MMA always share their type).
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major)
 {
