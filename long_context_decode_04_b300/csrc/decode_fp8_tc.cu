@@ -167,11 +167,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Zero the fp16 V tiles (rows 120-127 stay zero), the Q operands (rows
-    // G..15 stay zero) and the P operands.
+    // Zero what no widening or query write covers: rows 120-127 of the fp16 V
+    // tiles, the Q operands (rows G..15) and the P operands.
     const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = threadIdx.x; i < kRawOff / 16; i += kThreads)
-        *reinterpret_cast<uint4 *>(smem + i * 16) = z4;
+    for (int i = threadIdx.x; i < kConvBufs * 2 * 8 * 8; i += kThreads) {
+        const int c = i & 7, r = kTile + ((i >> 3) & 7), hh = (i >> 6) & 1, b = i >> 7;
+        *reinterpret_cast<uint4 *>(smem + kVOff + b * kVBytes + hh * kHalf + r * 128 + c * 16) = z4;
+    }
+    for (int i = threadIdx.x; i < (kRawOff - kQOff) / 16; i += kThreads)
+        *reinterpret_cast<uint4 *>(smem + kQOff + i * 16) = z4;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 
     if (threadIdx.x == 0) {
@@ -219,6 +223,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
         int stage = 0, ti = 0, ic = 0;
         uint32_t uses[kRawStages] = {};
         uint32_t q_uses[2] = {0u, 0u};
+        // The item's G query rows as fp16 into Q buffer ic % 2: 16-byte chunk c
+        // of head h (8 dims) to row h of the operand, 128-byte swizzle.
+        auto widen_q = [&](int item) -> bool {
+            const int unit = item / p.n_split;
+            const int qb = ic & 1;
+            int w = 1;
+            if (leader && q_uses[qb] > 0)
+                w = mbar_wait_bounded(&ms->q_empty[qb], (q_uses[qb] - 1) & 1, abort_flag);
+            if (!__shfl_sync(kFull, w, 0))
+                return false;
+            unsigned char *qd = smem + kQOff + qb * kQBytes;
+            const __nv_bfloat16 *qsrc = p.q + (size_t)unit * G * kD;
+            for (int i = lane; i < G * 16; i += 32) {
+                const int h = i >> 4, c = i & 15;
+                const uint4 x = *reinterpret_cast<const uint4 *>(qsrc + h * kD + c * 8);
+                const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+                uint32_t hv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    hv[k] = tc::pack_f16x2(bf16_lo(wv[k]), bf16_hi(wv[k]));
+                *reinterpret_cast<uint4 *>(qd + (c >> 3) * kQHalf + h * 128 + ((((c & 7) ^ h) & 7) << 4)) =
+                    make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (leader)
+                mbar_arrive(&ms->q_full[qb]);
+            ++q_uses[qb];
+            ++ic;
+            return true;
+        };
         bool ok = true;
         while (ok) {
             int item = 0;
@@ -255,40 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
             }
             const int c0 = split * p.chunk;
             const int c1 = min(c0 + p.chunk, L);
-            // the item's G query rows as fp16: 16-byte chunk c of head h
-            // (8 dims) to row h of the operand, 128-byte swizzle
-            const int qb = ic & 1;
-            int w = 1;
-            if (leader && q_uses[qb] > 0)
-                w = mbar_wait_bounded(&ms->q_empty[qb], (q_uses[qb] - 1) & 1, abort_flag);
-            if (!__shfl_sync(kFull, w, 0))
-                break;
-            unsigned char *qd = smem + kQOff + qb * kQBytes;
-            const __nv_bfloat16 *qsrc = p.q + (size_t)unit * G * kD;
-            for (int i = lane; i < G * 16; i += 32) {
-                const int h = i >> 4, c = i & 15;
-                const uint4 x = *reinterpret_cast<const uint4 *>(qsrc + h * kD + c * 8);
-                const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
-                uint32_t hv[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    hv[k] = tc::pack_f16x2(bf16_lo(wv[k]), bf16_hi(wv[k]));
-                *reinterpret_cast<uint4 *>(qd + (c >> 3) * kQHalf + h * 128 + ((((c & 7) ^ h) & 7) << 4)) =
-                    make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (leader)
-                mbar_arrive(&ms->q_full[qb]);
-            ++q_uses[qb];
-            ++ic;
             int j0 = c0, flags = kFirst;
             for (;;) {
                 const int n = max(0, min(kTile, c1 - j0));
                 const bool last = j0 + n >= c1;
                 if (last)
                     flags |= kLast;
-                w = 1;
+                int w = 1;
                 if (leader) {
                     if (uses[stage] > 0)
                         w = mbar_wait_bounded(&ms->raw_empty[stage], (uses[stage] - 1) & 1, abort_flag);
@@ -313,6 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                 }
                 ++uses[stage];
                 ++ti;
+                if (flags & kFirst) {
+                    // the item's queries, once its first copy is in flight
+                    if (!widen_q(item))
+                        ok = false;
+                }
+                if (!ok)
+                    break;
                 if (++stage == kRawStages)
                     stage = 0;
                 if (last)
