@@ -13,22 +13,25 @@
 // Why tensor cores in a bandwidth-bound step.  The G query heads of a KV
 // head (grouped-query attention) share its keys, so per KV head the scores
 // are the product [keys x D] . [D x G] and the output [D x keys] . [keys x G]:
-// dense contractions of the streamed tile with a small matrix.  On the CUDA
-// cores they cost about 57 issued warp instructions per key row at G = 4,
-// which keeps that kernel issue-bound a little under the HBM roofline.
-// Here each contraction is a handful of tcgen05.mma per tile and the
-// remaining per-key work is a few instructions of softmax, so the kernel
-// streams K and V at the bandwidth of HBM.
+// contractions of the streamed tile with a G-row matrix (G = 1, a
+// matrix-vector product, stays on the CUDA cores).  On the CUDA cores they
+// cost about 57 issued warp instructions per key row at G = 4, which keeps
+// that kernel issue-bound under the HBM roofline.  Here each contraction is
+// a handful of tcgen05.mma per tile and the remaining per-key work is a few
+// instructions of softmax, so the issue slots no longer bound the kernel:
+// how long a ring stage is held between its copy and its value product does.
 //
 // Per 120-key tile (M = 128 rows; rows 120-127 of every staged tile are
 // zero and masked):
 //   S^T [128 keys x 16] = K [128 x D] . Q^T [D x 16]     (A = K, K-major;
 //                                                        B = Q, heads padded to 16)
-//   O_t^T [D x 16]      = V^T [D x 128] . P^T [128 x 16] (A = V, MN-major;
+//   O_t^T [D x 32]      = V^T [D x 128] . P^T [128 x 32] (A = V, MN-major;
 //                                                        B = P, K-major)
-// with P = exp2(s - m) of the running maximum m, written to shared memory
-// as bf16 hi + lo parts (p = hi + lo to about 2^-17 relative; two MMAs add
-// both), so the weights keep fp32-like precision against bf16 V.
+// P has one row per (softmax warp, head) in bf16 hi and lo parts (p = hi +
+// lo to about 2^-17 relative), so one MMA per 16 keys sums both and the
+// weights keep fp32-like precision against bf16 V; p = exp2(s - m) against
+// its warp's reference m, raised lazily (only when a score passes it by
+// more than 2^8).
 //
 // Kernel layout (one persistent CTA per SM, 8 warps):
 //   * warp 0: producer.  Takes work items (sequence, KV head, chunk) from
