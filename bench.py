@@ -231,6 +231,53 @@ def measure_pi(ta, accounting, peaks, dev, w, q, k, v, window=4096, period=64, r
             "frac": round(gbs / peaks["hbm_gbs"], 4)}
 
 
+def measure_other_configs(ta, synth, accounting, peaks, dev, reps=20):
+    """Decode of the single-head fp32 workload (4096 keys, D = 64) and of the
+    1M-key GQA workload with its forced 256-key chunks (4096 splits, merged in
+    two levels by the merge kernel): median of `reps` graph replays each, all
+    KV bytes."""
+    import torch
+    res = {}
+    for name in ("single_head_d64_s4096_f32", "gqa_32x8_d128_s1048576_c256"):
+        w = synth.WORKLOADS[name]
+        x = synth.make_inputs(w)
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        del x
+        chunk = w.chunk or 0
+        plan = ta.plan_decode(w.B, w.Hq, w.Hkv, w.S, w.D, chunk=chunk)
+        kv_bytes = accounting.decode_kv_bytes(w.B, w.Hkv, w.D, w.S, 4 if w.dtype == "f32" else 2)
+        ws = ta.decode_workspace(w.B, w.Hq, w.Hkv, w.S, w.D, chunk=chunk, device=dev)
+        out = torch.empty((w.B, w.Hq, w.D), dtype=q.dtype, device=dev)
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+
+        def fn():
+            ta.decode(q, k, v, scale=w.scale, chunk=chunk, workspace=ws, out=out, lse=lse)
+
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        stream = torch.cuda.current_stream(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = sorted(1e3 * a.elapsed_time(b) for a, b in ev)[reps // 2]
+        gbs = kv_bytes / (us / 1e6) / 1e9
+        res[name] = {"workload": f"B={w.B}, Hq={w.Hq}, Hkv={w.Hkv}, D={w.D}, S={w.S}, {w.dtype}",
+                     "n_split": plan.n_split, "chunk": plan.chunk,
+                     "launches": 1 if plan.n_split <= 64 else 1 + plan.levels,
+                     "kv_bytes": kv_bytes, "us": round(us, 2), "gbs": round(gbs, 1),
+                     "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        del q, k, v, ws, out, lse, g
+        torch.cuda.empty_cache()
+    return res
+
+
 def measure_fp8(ta, synth, accounting, peaks, dev, w, x, reps=20):
     """Decode of the 128K-token workload with its K/V quantised to E4M3 (one
     factor per KV head): median of `reps` graph replays, KV bytes read (1 byte
@@ -495,6 +542,7 @@ def main():
     extra = None if args.no_extra else measure_varlen(ta, synth, accounting, peaks, dev)
     pi_fig = None if args.no_extra else measure_pi(ta, accounting, peaks, dev, w, q, k, v)
     fp8_fig = None if args.no_extra else measure_fp8(ta, synth, accounting, peaks, dev, w, x)
+    others_fig = None if args.no_extra else measure_other_configs(ta, synth, accounting, peaks, dev)
     pvar_fig = None if (args.no_extra or not do_prefill) else measure_prefill_varlen(ta, synth, peaks, dev)
 
     # ---------------- end to end through the public single call, host buffers
@@ -585,6 +633,7 @@ def main():
         "varlen_b16": extra,
         "pi_attention": pi_fig,
         "fp8_kv": fp8_fig,
+        "other_decode_configs": others_fig,
         "prefill_varlen": pvar_fig,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
