@@ -62,7 +62,12 @@ typedef enum { TA_F32 = 0, TA_BF16 = 1 } ta_dtype;
 /* Device-side conditions recorded in the workspace status word (bit set). */
 enum {
     TA_DEVERR_SEQLEN = 1,   /* some seqlens[b] < 0 or > S; clamped to [0, S]     */
-    TA_DEVERR_TIMEOUT = 2,  /* a pipeline wait exceeded its time limit; output invalid */
+    TA_DEVERR_TIMEOUT = 2,  /* a pipeline wait exceeded its time limit; output invalid; the
+                               launch stopped, let its copies and tensor-core operations
+                               finish and returned.  Clear the workspace's control region
+                               (its first 16 KiB, or all of a smaller workspace) before it is
+                               used again; ta_decode_status does this for the library's own
+                               workspace. */
     TA_DEVERR_RANGE = 4,    /* prefill: some |V| > 65280 (outside fp16); output undefined */
     TA_DEVERR_PAGE = 8      /* paged decode: a block-table entry outside [0, num_pages); output undefined */
 };
@@ -94,6 +99,10 @@ typedef struct {
  *     are clamped on the device and TA_DEVERR_SEQLEN is recorded.
  *   chunk / n_split: 0 = scheduler default; chunk > 0 forces keys per chunk
  *     (takes precedence), else n_split > 0 forces the number of chunks.
+ *   wait_limit_ns: every wait of one pipeline stage on another inside the
+ *     kernels gives up after this long, records TA_DEVERR_TIMEOUT and ends
+ *     the launch (0 = the default of 2 s).  The waits that let a stopping
+ *     CTA's own copies and tensor-core operations finish keep the default.
  *   workspace: device scratch of at least ta_decode_plan.workspace_bytes,
  *     256-byte aligned, that the caller zeroes once when it sets it up and
  *     uses for decodes only.  A split decode keeps its status word and one
@@ -127,6 +136,7 @@ typedef struct {
     void *workspace;
     size_t workspace_bytes;
     void *stream;
+    uint64_t wait_limit_ns;  /* time limit of one pipeline wait in the kernels; 0 = 2 s */
 } ta_decode_params;
 
 /*
@@ -152,18 +162,41 @@ ta_status ta_decode(const void *q, const void *k, const void *v, void *out, floa
  *   shape whose plan needs more (ta_decode_workspace_bytes(B, Hq, Hkv, S, D,
  *   0, 0, seqlens != NULL) > 8 MiB) is rejected with TA_ERR_WORKSPACE and
  *   nothing is launched; such shapes need ta_decode or ta_decode_ex.
- *   Set-up: the first call on each device looks up the array's device
- *   address with that device current; make that first call before any
- *   stream capture.
+ *   Set-up: the first call on each device (or ta_decode_noalloc_setup) has
+ *   the CUDA runtime load this library's device code on that device, which
+ *   reserves the array there, and looks up its device address with that
+ *   device current.  That one-time reservation is the only memory it takes;
+ *   make it early: before a pool allocator claims the GPU's memory and
+ *   before any stream capture.
  *   Every call clears the scratch's status word and chunk counters on
  *   `stream` before the kernels run.  All calls on one GPU share the one array: calls that may
  *   overlap on the GPU (different streams or host threads with no ordering
  *   between them) race on it and give wrong results.
+ *   Device-side flags (TA_DEVERR_*) go to the scratch's status word: read
+ *   them with ta_decode_noalloc_status, before the next call clears them.
+ *   The per-device address is cached for the life of the process; after a
+ *   cudaDeviceReset the next call must not be made on that device.
  * Arguments, layouts, alignment and errors as for ta_decode.
  */
 ta_status ta_decode_noalloc(const void *q, const void *k, const void *v, void *out, float *lse,
                             int B, int Hq, int Hkv, int S, int D, float scale,
                             const int32_t *seqlens, void *stream);
+
+/*
+ * The one-time set-up of ta_decode_noalloc on the current device, on its
+ * own: loads the device code (reserving the fixed scratch array) and looks
+ * up the array's address.  Optional; the first ta_decode_noalloc call on a
+ * device does the same.  Launches nothing.
+ */
+ta_status ta_decode_noalloc_setup(void);
+
+/*
+ * Read and clear the status word (TA_DEVERR_* bits) of ta_decode_noalloc's
+ * fixed scratch on the current device, without allocating: synchronises
+ * `stream`, copies the word to the host and zeroes it (and after
+ * TA_DEVERR_TIMEOUT the scratch's whole control region).
+ */
+ta_status ta_decode_noalloc_status(void *stream, int32_t *flags);
 
 /* Split-KV decode with every option of ta_decode_params. */
 ta_status ta_decode_ex(const ta_decode_params *p);
@@ -242,6 +275,7 @@ typedef struct {
     void *workspace;
     size_t workspace_bytes;
     void *stream;
+    uint64_t wait_limit_ns;  /* as in ta_decode_params; 0 = 2 s */
 } ta_paged_decode_params;
 
 ta_status ta_decode_paged(const ta_paged_decode_params *p);
@@ -308,7 +342,8 @@ size_t ta_combine_workspace_bytes(int R, int N, int D);
  *   q, out [B, H, S, D] bf16; k, v [B, Hkv, S, D] bf16; lse [B, H, S] fp32
  *   (may be NULL).  Query row i attends keys 0..i (top-left aligned, square).
  * The softmax weights P enter the PV product as fp16 (relative rounding
- * 2^-12), with V converted to fp16 on chip; |V| must be <= 65280.
+ * 2^-12), with V converted to fp16 on chip; |V| must be <= 65280.  The row
+ * sums l are taken over the same fp16 weights.
  * Supported: D = 128; H % Hkv == 0; S >= 1; scale > 0; q, k, v, out
  * 16-byte aligned.  The library's status word (read with
  * ta_decode_status(NULL, ...)) records TA_DEVERR_TIMEOUT if a pipeline wait
@@ -316,6 +351,37 @@ size_t ta_combine_workspace_bytes(int R, int N, int D);
  */
 ta_status ta_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse,
                             int B, int H, int Hkv, int S, int D, float scale, void *stream);
+
+/*
+ * Causal prefill with every option: the batched layouts of
+ * ta_prefill_causal, or (cu_seqlens != NULL) the packed layouts of
+ * ta_prefill_causal_varlen, with the output in bf16 or fp32.
+ *   q, k, v, out, lse, H, Hkv, D, scale: as ta_prefill_causal (batched) or
+ *     ta_prefill_causal_varlen (packed);
+ *   batched: B sequences of S tokens, cu_seqlens = NULL, total_tokens unused;
+ *   packed:  B = number of sequences, S = max_seqlen, cu_seqlens [B + 1] and
+ *     total_tokens as ta_prefill_causal_varlen;
+ *   out_dtype: TA_BF16 (out rounded to nearest even) or TA_F32 (the fp32
+ *     value the bf16 output is rounded from; same kernel, same arithmetic);
+ *   wait_limit_ns: as in ta_decode_params (0 = 2 s).
+ * Errors and device-side flags as ta_prefill_causal.
+ */
+typedef struct {
+    const void *q;
+    const void *k;
+    const void *v;
+    void *out;
+    float *lse;
+    int32_t B, H, Hkv, S, D;
+    float scale;
+    const int32_t *cu_seqlens;
+    int32_t total_tokens;
+    ta_dtype out_dtype;
+    uint64_t wait_limit_ns;
+    void *stream;
+} ta_prefill_params;
+
+ta_status ta_prefill_causal_ex(const ta_prefill_params *p);
 
 /*
  * Causal prefill of a packed batch of variable-length sequences: the
@@ -336,6 +402,27 @@ ta_status ta_prefill_causal(const void *q, const void *k, const void *v, void *o
 ta_status ta_prefill_causal_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
                                    const int32_t *cu_seqlens, int num_seqs, int max_seqlen, int total_tokens,
                                    int H, int Hkv, int D, float scale, void *stream);
+
+/*
+ * Test hook: the next `count` kernel launches of this process (any entry
+ * point, any thread) are not made; the call that would make each returns
+ * TA_ERR_CUDA with a message naming this hook, after its argument checks and
+ * before anything further is enqueued.  count = 0 cancels.  Returns the
+ * number that was pending.  For testing callers' error handling; a launch
+ * that is not made computes nothing and writes no output.
+ */
+int ta_test_fail_next_launches(int count);
+
+/*
+ * Test hook for the device-side time limit: in each of the next `count`
+ * kernel launches that have pipeline waits (decode and prefill kernels, not
+ * the merge), the CTAs' producer first waits on a barrier that nothing
+ * completes, so that wait runs out after the launch's wait_limit_ns: the
+ * launch then stops every role, lets what it issued finish, frees its tensor
+ * memory, records TA_DEVERR_TIMEOUT and returns; its outputs are not
+ * written.  count = 0 cancels.  Returns the number that was pending.
+ */
+int ta_test_stall_next_launches(int count);
 
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char *ta_last_error(void);

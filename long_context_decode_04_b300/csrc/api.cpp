@@ -2,6 +2,7 @@
 // dispatch to the scheduler and the kernels.  Nothing here computes
 // attention; every arithmetic step runs in the CUDA kernels.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -15,6 +16,9 @@
 namespace {
 
 thread_local std::string g_error;
+thread_local bool g_injected = false;     // the last launch failure came from the test hook
+std::atomic<int> g_fail_launches{0};      // launches still to refuse (ta_test_fail_next_launches)
+std::atomic<int> g_stall_launches{0};     // launches still to stall (ta_test_stall_next_launches)
 
 ta_status fail(ta_status s, const std::string &msg)
 {
@@ -24,6 +28,10 @@ ta_status fail(ta_status s, const std::string &msg)
 
 ta_status cuda_fail(cudaError_t e, const char *where)
 {
+    if (g_injected) {
+        g_injected = false;
+        return fail(TA_ERR_CUDA, std::string(where) + ": launch not made (failure injected by ta_test_fail_next_launches)");
+    }
     return fail(TA_ERR_CUDA, std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
 }
 
@@ -153,11 +161,36 @@ ta_status validate_decode(const ta_decode_params *p)
 
 void ta::record_error(const std::string &msg) { g_error = msg; }
 
+cudaError_t ta::injected_launch_failure()
+{
+    int n = g_fail_launches.load();
+    while (n > 0) {
+        if (g_fail_launches.compare_exchange_weak(n, n - 1)) {
+            g_injected = true;
+            return cudaErrorLaunchFailure;
+        }
+    }
+    return cudaSuccess;
+}
+
+int ta::injected_stall()
+{
+    int n = g_stall_launches.load();
+    while (n > 0)
+        if (g_stall_launches.compare_exchange_weak(n, n - 1))
+            return 1;
+    return 0;
+}
+
 ta_status ta::check_decode_params(const ta_decode_params *p) { return validate_decode(p); }
 
 extern "C" {
 
 const char *ta_last_error(void) { return g_error.c_str(); }
+
+int ta_test_fail_next_launches(int count) { return g_fail_launches.exchange(count > 0 ? count : 0); }
+
+int ta_test_stall_next_launches(int count) { return g_stall_launches.exchange(count > 0 ? count : 0); }
 
 ta_status ta_decode_plan_for(int B, int Hq, int Hkv, int S, int D, int chunk, int n_split, int varlen,
                              int sm_count, ta_decode_plan *plan)
@@ -224,6 +257,8 @@ ta_status decode_impl(const ta_decode_params *p, const int32_t *block_table, int
     a.kv_fp8 = kv_fp8;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    a.wait_ns = ta::wait_limit_or_default(p->wait_limit_ns);
+    a.test_stall = ta::injected_stall();
     a.q = p->q;
     a.k = p->k;
     a.v = p->v;
@@ -348,6 +383,7 @@ ta_status ta_decode_paged(const ta_paged_decode_params *pp)
     p.workspace = pp->workspace;
     p.workspace_bytes = pp->workspace_bytes;
     p.stream = pp->stream;
+    p.wait_limit_ns = pp->wait_limit_ns;
     ta_status s = validate_decode(&p);
     if (s != TA_OK)
         return s;
@@ -405,6 +441,8 @@ ta_status ta_decode_partials(const ta_decode_params *p, float *m, float *l, floa
     a.pi_window = a.pi_period = 0;
     a.kv_fp8 = false;
     a.k_scale = a.v_scale = nullptr;
+    a.wait_ns = ta::wait_limit_or_default(p->wait_limit_ns);
+    a.test_stall = ta::injected_stall();
     a.stream = static_cast<cudaStream_t>(p->stream);
     a.status = static_cast<int32_t *>(ws);
     a.counters = nullptr;
@@ -518,31 +556,61 @@ ta_status ta_combine(const float *m, const float *l, const float *o, int R, int 
     return TA_OK;
 }
 
-ta_status ta_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
-                            int Hkv, int S, int D, float scale, void *stream)
+ta_status ta_prefill_causal_ex(const ta_prefill_params *p)
 {
-    if (!q || !k || !v || !out)
+    if (!p)
+        return fail(TA_ERR_INVALID_ARG, "params pointer is NULL");
+    const bool packed = p->cu_seqlens != nullptr;
+    if (!p->q || !p->k || !p->v || !p->out)
         return fail(TA_ERR_INVALID_ARG, "q, k, v and out must be non-NULL");
-    if (B < 1 || H < 1 || Hkv < 1 || S < 1 || D < 1)
-        return fail(TA_ERR_INVALID_ARG, "B, H, Hkv, S and D must all be >= 1");
-    if (H % Hkv != 0)
+    if (p->B < 1 || p->H < 1 || p->Hkv < 1 || p->S < 1 || p->D < 1 || (packed && p->total_tokens < 1))
+        return fail(TA_ERR_INVALID_ARG, packed ? "num_seqs, max_seqlen, total_tokens, H, Hkv and D must all be >= 1"
+                                               : "B, H, Hkv, S and D must all be >= 1");
+    if (p->H % p->Hkv != 0)
         return fail(TA_ERR_INVALID_ARG, "H must be a multiple of Hkv");
-    if (!std::isfinite(scale))
+    if (!std::isfinite(p->scale))
         return fail(TA_ERR_INVALID_ARG, "scale must be finite");
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4)))
-        return fail(TA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned, lse 4-byte aligned");
-    if (D != 128)
+    if (p->out_dtype != TA_F32 && p->out_dtype != TA_BF16)
+        return fail(TA_ERR_INVALID_ARG, "out_dtype must be TA_F32 or TA_BF16");
+    if (!aligned(p->q, 16) || !aligned(p->k, 16) || !aligned(p->v, 16) || !aligned(p->out, 16) ||
+        (p->lse && !aligned(p->lse, 4)) || (packed && !aligned(p->cu_seqlens, 4)))
+        return fail(TA_ERR_INVALID_ARG,
+                    "q, k, v and out must be 16-byte aligned, lse and cu_seqlens 4-byte aligned");
+    if (p->D != 128)
         return fail(TA_ERR_UNSUPPORTED, "prefill supports head dim D = 128");
-    if (!(scale > 0.f))
+    if (!(p->scale > 0.f))
         return fail(TA_ERR_UNSUPPORTED, "prefill supports scale > 0");
-    if ((double)B * H * S * D > 9.0e18 / 4)
+    if (!packed && (double)p->B * p->H * p->S * p->D > 9.0e18 / 4)
         return fail(TA_ERR_INVALID_ARG, "tensor size overflows");
+    if (packed && ((double)p->total_tokens * p->H * p->D > 9.0e18 / 4 ||
+                   (double)p->B * p->H * ((p->S + 255) / 256) > 2.0e9))
+        return fail(TA_ERR_INVALID_ARG, "problem size overflows");
+    if (!packed && (double)p->B * p->H * ((p->S + 255) / 256) > 2.0e9)
+        return fail(TA_ERR_INVALID_ARG, "problem size overflows");
     void *ws = nullptr;
     ta_status s = library_workspace(256, &ws);
     if (s != TA_OK)
         return s;
-    cudaError_t e = ta::launch_prefill_causal(q, k, v, out, lse, B, H, Hkv, S, D, scale,
-                                              static_cast<int32_t *>(ws), static_cast<cudaStream_t>(stream));
+    ta::PrefillLaunch a;
+    a.q = p->q;
+    a.k = p->k;
+    a.v = p->v;
+    a.out = p->out;
+    a.lse = p->lse;
+    a.B = p->B;
+    a.H = p->H;
+    a.Hkv = p->Hkv;
+    a.S = p->S;
+    a.D = p->D;
+    a.scale = p->scale;
+    a.cu_seqlens = p->cu_seqlens;
+    a.T = packed ? p->total_tokens : 0;
+    a.out_dtype = p->out_dtype;
+    a.status = static_cast<int32_t *>(ws);
+    a.wait_ns = ta::wait_limit_or_default(p->wait_limit_ns);
+    a.test_stall = ta::injected_stall();
+    a.stream = static_cast<cudaStream_t>(p->stream);
+    cudaError_t e = ta::launch_prefill(a);
     if (e == cudaErrorNotSupported)
         return fail(TA_ERR_UNSUPPORTED, "causal prefill kernel is not available in this build");
     if (e != cudaSuccess)
@@ -550,37 +618,51 @@ ta_status ta_prefill_causal(const void *q, const void *k, const void *v, void *o
     return TA_OK;
 }
 
+ta_status ta_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                            int Hkv, int S, int D, float scale, void *stream)
+{
+    ta_prefill_params p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.out = out;
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.S = S;
+    p.D = D;
+    p.scale = scale;
+    p.out_dtype = TA_BF16;
+    p.stream = stream;
+    return ta_prefill_causal_ex(&p);
+}
+
 ta_status ta_prefill_causal_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
                                    const int32_t *cu_seqlens, int num_seqs, int max_seqlen, int total_tokens, int H,
                                    int Hkv, int D, float scale, void *stream)
 {
-    if (!q || !k || !v || !out || !cu_seqlens)
+    if (!cu_seqlens)
         return fail(TA_ERR_INVALID_ARG, "q, k, v, out and cu_seqlens must be non-NULL");
-    if (num_seqs < 1 || max_seqlen < 1 || total_tokens < 1 || H < 1 || Hkv < 1 || D < 1)
-        return fail(TA_ERR_INVALID_ARG, "num_seqs, max_seqlen, total_tokens, H, Hkv and D must all be >= 1");
-    if (H % Hkv != 0)
-        return fail(TA_ERR_INVALID_ARG, "H must be a multiple of Hkv");
-    if (!std::isfinite(scale))
-        return fail(TA_ERR_INVALID_ARG, "scale must be finite");
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4)) ||
-        !aligned(cu_seqlens, 4))
-        return fail(TA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned, lse and cu_seqlens 4-byte aligned");
-    if (D != 128)
-        return fail(TA_ERR_UNSUPPORTED, "prefill supports head dim D = 128");
-    if (!(scale > 0.f))
-        return fail(TA_ERR_UNSUPPORTED, "prefill supports scale > 0");
-    if ((double)total_tokens * H * D > 9.0e18 / 4 || (double)num_seqs * H * ((max_seqlen + 255) / 256) > 2.0e9)
-        return fail(TA_ERR_INVALID_ARG, "problem size overflows");
-    void *ws = nullptr;
-    ta_status s = library_workspace(256, &ws);
-    if (s != TA_OK)
-        return s;
-    cudaError_t e = ta::launch_prefill_causal_varlen(q, k, v, out, lse, cu_seqlens, num_seqs, max_seqlen,
-                                                     total_tokens, H, Hkv, D, scale, static_cast<int32_t *>(ws),
-                                                     static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess)
-        return cuda_fail(e, "prefill kernel launch");
-    return TA_OK;
+    ta_prefill_params p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.out = out;
+    p.lse = lse;
+    p.B = num_seqs;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.S = max_seqlen;
+    p.D = D;
+    p.scale = scale;
+    p.cu_seqlens = cu_seqlens;
+    p.total_tokens = total_tokens;
+    p.out_dtype = TA_BF16;
+    p.stream = stream;
+    return ta_prefill_causal_ex(&p);
 }
 
 }  // extern "C"

@@ -151,6 +151,8 @@ cudaError_t run_levels(const float *m, const float *l, const float *o, int R, in
 cudaError_t launch_combine(const float *m, const float *l, const float *o, int R, int N, int D, void *out,
                            ta_dtype out_dtype, float *lse, void *scratch, cudaStream_t stream)
 {
+    if (cudaError_t inj = injected_launch_failure())
+        return inj;
     if (D == 128)
         return out_dtype == TA_BF16 ? run_levels<128, __nv_bfloat16>(m, l, o, R, N, out, lse, scratch, stream)
                                     : run_levels<128, float>(m, l, o, R, N, out, lse, scratch, stream);

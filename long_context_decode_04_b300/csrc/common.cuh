@@ -8,9 +8,12 @@
 
 namespace ta {
 
-// A pipeline wait that has not completed after this long records
-// TA_DEVERR_TIMEOUT and gives up instead of spinning forever.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Default time limit of a pipeline wait: one that has not completed after
+// this long records TA_DEVERR_TIMEOUT and gives up instead of spinning
+// forever.  A launch may set a shorter limit of its own; the waits that
+// drain a CTA's copies and tensor-core operations before it exits always
+// use this one.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s (the host's default limit too)
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -76,9 +79,10 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Wait for the phase of `bar` with the given parity.  Gives up (returns
-// false) when *abort is set by another thread or after kWaitLimitNs, in
-// which case it sets *abort itself.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort)
+// false) when *abort is set by another thread or after limit_ns
+// nanoseconds, in which case it sets *abort itself.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                  uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -89,7 +93,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if ((i & 15u) == 0) {
             if (*abort)
                 return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 return false;
             }

@@ -92,6 +92,8 @@ struct DecodeParams {
     int32_t *status;    // [0] flags, [16] work-queue counter
     int32_t *counters;  // [B * Hkv] finished chunks per unit (fused mode)
     float *part_m, *part_l, *part_o;
+    uint64_t wait_ns;   // time limit of a pipeline wait
+    int test_stall;     // test hook: the producer first waits on a barrier nothing ends
     // Paged KV cache (block_table != nullptr): k, v are [num_pages, Hkv,
     // page_size, D] and key j of sequence b lives in page
     // block_table[b * pages_per_seq + j / page_size] at row j % page_size.
@@ -372,6 +374,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         uint32_t used_mask = 0, parity_mask = 0;  // per stage: armed, and that phase's parity
         const size_t kv_head_stride = (size_t)p.S * D;
         bool ok = true;
+        if (p.test_stall) {
+            // test hook: a wait that nothing ends (phase 0 of a barrier only
+            // this warp arms), so the launch's time limit runs out
+            int w = 1;
+            if (leader)
+                w = mbar_wait_bounded(&full[0], 0, abort_flag, p.wait_ns);
+            ok = __shfl_sync(kFull, w, 0) != 0;
+        }
         while (ok) {
             int item = 0;
             if (leader)
@@ -382,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
                 if (leader) {
                     if (item == p.n_items + (int)gridDim.x - 1)
                         atomicExch(&p.status[16], 0);  // last grab of the launch: reset the queue
-                    w = mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag);
+                    w = mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, p.wait_ns);
                     if (w) {
                         desc[stage] = TileDesc{item, 0, 0, kEnd};
                         mbar_arrive(&full[stage]);
@@ -429,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
                     flags |= kLast;
                 bool w = true;
                 if (leader) {
-                    w = mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag);
+                    w = mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, p.wait_ns);
                     if (w) {
                         desc[stage] = TileDesc{item, j0, n, flags};
                         if (n > 0)
@@ -564,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     }
 
     for (;;) {
-        bool ok = mbar_wait_bounded(&full[stage], phase, abort_flag);
+        bool ok = mbar_wait_bounded(&full[stage], phase, abort_flag, p.wait_ns);
         if (!__all_sync(kFull, ok))
             break;
         const TileDesc d = desc[stage];
@@ -786,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
                 for (int e = 0; e < C::DPL; ++e)
                     o[h][e] *= vs;
         }
-        ok = mbar_wait_bounded(merge_out, merge_phase ^ 1, abort_flag);
+        ok = mbar_wait_bounded(merge_out, merge_phase ^ 1, abort_flag, p.wait_ns);
         if (!__all_sync(kFull, ok))
             break;
 #pragma unroll
@@ -806,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         __syncwarp();
         if (lane == 0)
             mbar_arrive(merge_in);
-        ok = mbar_wait_bounded(merge_in, merge_phase, abort_flag);
+        ok = mbar_wait_bounded(merge_in, merge_phase, abort_flag, p.wait_ns);
         if (!__all_sync(kFull, ok))
             break;
         const size_t row0 = (size_t)b * p.Hq + (size_t)kvh * G;
@@ -852,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         mbar_arrive(written);
         if (tid == 0) {
             int last = 0;
-            if (mbar_wait_bounded(written, ticket_phase, abort_flag)) {
+            if (mbar_wait_bounded(written, ticket_phase, abort_flag, p.wait_ns)) {
                 const int done = atomicAdd(&p.counters[unit], 1);
                 if (done == p.n_split - 1) {
                     last = 1;
@@ -863,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
             *ticket_flag = last;
             mbar_arrive(ticket);
         }
-        ok = mbar_wait_bounded(ticket, ticket_phase, abort_flag);
+        ok = mbar_wait_bounded(ticket, ticket_phase, abort_flag, p.wait_ns);
         ticket_phase ^= 1;
         if (!__all_sync(kFull, ok))
             break;
@@ -880,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
             fm_l[i] = __ldcg(p.part_l + pi);
         }
         mbar_arrive(fm_ready);
-        ok = mbar_wait_bounded(fm_ready, fm_phase, abort_flag);
+        ok = mbar_wait_bounded(fm_ready, fm_phase, abort_flag, p.wait_ns);
         fm_phase ^= 1;
         if (!__all_sync(kFull, ok))
             break;
@@ -918,6 +928,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
                 p.lse[row0 + h] = ls > 0.f ? mx + fast_log2(ls) * kLn2 : -INFINITY;
         }
     }
+    // A consumer warp that gave up (or saw another give up) records it: the
+    // producer may have returned before the wait that failed.
+    if (lane == 0 && *abort_flag)
+        atomicOr(&p.status[0], TA_DEVERR_TIMEOUT);
 }
 
 template <int D, int G, typename KV, typename OUT>
@@ -955,6 +969,8 @@ cudaError_t dispatch_types(const DecodeLaunch &a, const DecodeParams &p)
 
 cudaError_t launch_decode(const DecodeLaunch &a)
 {
+    if (cudaError_t inj = injected_launch_failure())
+        return inj;
     if (decode_tc_eligible(a))
         return launch_decode_tc(a);
     if (decode_fp8_tc_eligible(a))
@@ -981,6 +997,8 @@ cudaError_t launch_decode(const DecodeLaunch &a)
     else
         p.mode = decode_merges_itself(a.plan.n_split, a.B * a.Hkv) ? kModeFused : kModePartials;
     p.status = a.status;
+    p.wait_ns = a.wait_ns;
+    p.test_stall = a.test_stall;
     p.counters = a.counters;
     p.part_m = a.part_m;
     p.part_l = a.part_l;

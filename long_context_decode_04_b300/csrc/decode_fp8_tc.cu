@@ -135,6 +135,8 @@ struct Fp8Params {
     int32_t *status;
     int32_t *counters;
     float *part_m, *part_l, *part_o;
+    uint64_t wait_ns;  // time limit of a pipeline wait
+    int test_stall;    // test hook: the producer first waits on a barrier nothing ends
     const float *k_scale, *v_scale;  // per (sequence, KV head), or nullptr (1)
 };
 
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
             const int qb = ic & 1;
             int w = 1;
             if (leader && q_uses[qb] > 0)
-                w = mbar_wait_bounded(&ms->q_empty[qb], (q_uses[qb] - 1) & 1, abort_flag);
+                w = mbar_wait_bounded(&ms->q_empty[qb], (q_uses[qb] - 1) & 1, abort_flag, p.wait_ns);
             if (!__shfl_sync(kFull, w, 0))
                 return false;
             unsigned char *qd = smem + kQOff + qb * kQBytes;
@@ -255,6 +257,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
             return true;
         };
         bool ok = true;
+        if (p.test_stall) {
+            // test hook: a wait that nothing ends (phase 0 of a barrier only
+            // this warp arms), so the launch's time limit runs out
+            int w = 1;
+            if (leader)
+                w = mbar_wait_bounded(&ms->raw_full[0], 0, abort_flag, p.wait_ns);
+            ok = __shfl_sync(kFull, w, 0) != 0;
+        }
         while (ok) {
             int item = 0;
             if (leader)
@@ -266,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                     if (item == p.n_items + (int)gridDim.x - 1)
                         atomicExch(&p.status[16], 0);  // last grab of the launch: reset the queue
                     if (uses[stage] > 0)
-                        w = mbar_wait_bounded(&ms->raw_empty[stage], (uses[stage] - 1) & 1, abort_flag);
+                        w = mbar_wait_bounded(&ms->raw_empty[stage], (uses[stage] - 1) & 1, abort_flag, p.wait_ns);
                     if (w) {
                         ms->desc[ti & (kDescRing - 1)] = TileDesc{item, 0, 0, kEnd};
                         mbar_arrive(&ms->raw_full[stage]);
@@ -299,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                 int w = 1;
                 if (leader) {
                     if (uses[stage] > 0)
-                        w = mbar_wait_bounded(&ms->raw_empty[stage], (uses[stage] - 1) & 1, abort_flag);
+                        w = mbar_wait_bounded(&ms->raw_empty[stage], (uses[stage] - 1) & 1, abort_flag, p.wait_ns);
                     if (w) {
                         ms->desc[ti & (kDescRing - 1)] = TileDesc{item, j0, n, flags};
                         uint64_t *fb = &ms->raw_full[stage];
@@ -354,12 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                 constexpr uint32_t kIdS = tc::idesc_f16_f32(kRows, kN, false);
                 int ic = 0;
                 for (;;) {
-                    if (!mbar_wait_bounded(&ms->conv_full[t % kConvBufs], (t / kConvBufs) & 1, abort_flag))
+                    if (!mbar_wait_bounded(&ms->conv_full[t % kConvBufs], (t / kConvBufs) & 1, abort_flag, p.wait_ns))
                         break;
                     const TileDesc d = ms->desc[t & (kDescRing - 1)];
                     // S and P buffers of this parity are free once the value
                     // product of tile t - 2 is done
-                    if (t >= 2 && !mbar_wait_bounded(&ms->o_full[t & 1], ((t - 2) >> 1) & 1, abort_flag))
+                    if (t >= 2 && !mbar_wait_bounded(&ms->o_full[t & 1], ((t - 2) >> 1) & 1, abort_flag, p.wait_ns))
                         break;
                     if (d.flags & kEnd) {
                         mbar_arrive(&ms->s_full[t & 1]);  // tells the softmax warps to stop
@@ -367,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                         break;
                     }
                     const int qb = ic & 1;
-                    if ((d.flags & kFirst) && !mbar_wait_bounded(&ms->q_full[qb], (ic >> 1) & 1, abort_flag))
+                    if ((d.flags & kFirst) && !mbar_wait_bounded(&ms->q_full[qb], (ic >> 1) & 1, abort_flag, p.wait_ns))
                         break;
                     tc::fence_after_sync();
                     const uint32_t s_tm = tmem + (t & 1) * kN;
@@ -392,11 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                 // value products: O_t^T = V^T P^T, V fp16 MN-major, P K-major
                 constexpr uint32_t kIdPV = tc::idesc_f16_f32_major(kRows, kON, true, false);
                 for (;;) {
-                    if (!mbar_wait_bounded(&ms->conv_full[t % kConvBufs], (t / kConvBufs) & 1, abort_flag))
+                    if (!mbar_wait_bounded(&ms->conv_full[t % kConvBufs], (t / kConvBufs) & 1, abort_flag, p.wait_ns))
                         break;
                     if (ms->desc[t & (kDescRing - 1)].flags & kEnd)
                         break;
-                    if (!mbar_wait_bounded(&ms->o_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag))
+                    if (!mbar_wait_bounded(&ms->o_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag, p.wait_ns))
                         break;
                     const uint32_t o_tm = tmem + kOCol + (t & 1) * kON;
                     const uint32_t vb = sbase + kVOff + (t % kConvBufs) * kVBytes;
@@ -404,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                     bool ok = true;
 #pragma unroll
                     for (int w = 0; w < 4 && ok; ++w) {
-                        ok = mbar_wait_bounded(&ms->p_full[t & 1][w], (t >> 1) & 1, abort_flag);
+                        ok = mbar_wait_bounded(&ms->p_full[t & 1][w], (t >> 1) & 1, abort_flag, p.wait_ns);
                         if (!ok)
                             break;
                         tc::fence_after_sync();
@@ -436,10 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
         int t = 0, stage = 0;
         uint32_t rph = 0;
         for (;;) {
-            bool w = mbar_wait_bounded(&ms->raw_full[stage], rph, abort_flag);
+            bool w = mbar_wait_bounded(&ms->raw_full[stage], rph, abort_flag, p.wait_ns);
             const TileDesc d = ms->desc[t & (kDescRing - 1)];
             const int cv = t % kConvBufs;
-            w = w && mbar_wait_bounded(&ms->conv_empty[cv], ((t / kConvBufs) & 1) ^ 1, abort_flag);
+            w = w && mbar_wait_bounded(&ms->conv_empty[cv], ((t / kConvBufs) & 1) ^ 1, abort_flag, p.wait_ns);
             if (!__all_sync(kFull, w))
                 break;
             if (d.flags & kEnd) {
@@ -525,13 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&ms->grp_bar);
-            const bool w = mbar_wait_bounded(&ms->grp_bar, gph, abort_flag);
+            const bool w = mbar_wait_bounded(&ms->grp_bar, gph, abort_flag, p.wait_ns);
             gph ^= 1;
             return __all_sync(kFull, w);
         };
         auto accumulate = [&](int x) -> bool {
-            bool w = mbar_wait_bounded(&ms->o_full[x & 1], (x >> 1) & 1, abort_flag);
-            w = w && mbar_wait_bounded(&ms->p_all[x & 1], (x >> 1) & 1, abort_flag);  // the factors
+            bool w = mbar_wait_bounded(&ms->o_full[x & 1], (x >> 1) & 1, abort_flag, p.wait_ns);
+            w = w && mbar_wait_bounded(&ms->p_all[x & 1], (x >> 1) & 1, abort_flag, p.wait_ns);  // the factors
             if (!__all_sync(kFull, w))
                 return false;
             tc::fence_after_sync();
@@ -551,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
             return true;
         };
         for (;;) {
-            const bool w = mbar_wait_bounded(&ms->s_full[t & 1], (t >> 1) & 1, abort_flag);  // S, descriptor
+            const bool w = mbar_wait_bounded(&ms->s_full[t & 1], (t >> 1) & 1, abort_flag, p.wait_ns);  // S, descriptor
             if (!__all_sync(kFull, w))
                 break;
             const TileDesc d = ms->desc[t & (kDescRing - 1)];
@@ -810,6 +820,8 @@ cudaError_t launch_decode_fp8_tc(const DecodeLaunch &a)
     else
         p.mode = decode_merges_itself(a.plan.n_split, a.B * a.Hkv) ? kModeFused : kModePartials;
     p.status = a.status;
+    p.wait_ns = a.wait_ns;
+    p.test_stall = a.test_stall;
     p.counters = a.counters;
     p.part_m = a.part_m;
     p.part_l = a.part_l;

@@ -18,6 +18,19 @@
 // device code on a GPU and which stays reserved there until the process
 // exits.
 //
+// Set-up: the array belongs to this file's device code, which the CUDA
+// runtime loads on a device when it is first needed there (lazy module
+// loading); the first cudaGetSymbolAddress on a device is that moment, and
+// it is also when the array's 8 MiB are reserved.  So the first call on a
+// device (or ta_decode_noalloc_setup) should come early: before a pool
+// allocator takes the GPU's memory, and before any stream capture.  The
+// address is cached per device for the life of the process; a
+// cudaDeviceReset invalidates it, and nothing here notices.
+//
+// Device-side flags (a length outside [0, S], a timed-out wait) land in the
+// scratch's status word; ta_decode_noalloc_status reads and clears it
+// without allocating.
+//
 // What the scratch holds: the decode workspace (status word and work-queue
 // counter in its first 256 bytes, the per-(sequence, KV head) chunk
 // counters, then the per-chunk partials (m, l, o) and the merge's
@@ -75,6 +88,38 @@ ta_status scratch_for_current_device(void **ptr)
 }  // namespace
 
 extern "C" {
+
+ta_status ta_decode_noalloc_setup(void)
+{
+    void *scratch = nullptr;
+    return scratch_for_current_device(&scratch);
+}
+
+ta_status ta_decode_noalloc_status(void *stream, int32_t *flags)
+{
+    if (!flags)
+        return fail(TA_ERR_INVALID_ARG, "flags pointer is NULL");
+    void *scratch = nullptr;
+    ta_status s = scratch_for_current_device(&scratch);
+    if (s != TA_OK)
+        return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return fail(TA_ERR_CUDA, std::string("cudaStreamSynchronize: ") + cudaGetErrorString(e));
+    int32_t word = 0;
+    e = cudaMemcpy(&word, scratch, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return fail(TA_ERR_CUDA, std::string("cudaMemcpy(status word): ") + cudaGetErrorString(e));
+    // after a timeout the work-queue and chunk counters may be left behind
+    e = cudaMemsetAsync(scratch, 0, (word & TA_DEVERR_TIMEOUT) ? ta::kCtrlBytes : ta::kStatusBytes, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return fail(TA_ERR_CUDA, std::string("cudaMemsetAsync(status word): ") + cudaGetErrorString(e));
+    *flags = word;
+    return TA_OK;
+}
 
 ta_status ta_decode_noalloc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq,
                             int Hkv, int S, int D, float scale, const int32_t *seqlens, void *stream)

@@ -140,6 +140,8 @@ struct TcParams {
     int32_t *status;    // [0] flags, [16] work-queue counter
     int32_t *counters;  // [B * Hkv] finished chunks per unit (fused mode)
     float *part_m, *part_l, *part_o;
+    uint64_t wait_ns;   // time limit of a pipeline wait
+    int test_stall;     // test hook: the producer first waits on a barrier nothing ends
     // pi-Attention key set (pi_period > 0): the query at i = L - 1 attends
     // the window [max(0, i - pi_window), i] and the keys i - m * pi_period
     // (m >= 1) before it; the chunks cut the ascending list of those keys.
@@ -225,6 +227,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         uint32_t q_uses[2] = {0u, 0u};
         int ic = 0;  // items taken
         bool ok = true;
+        if (p.test_stall) {
+            // test hook: a wait that nothing ends (phase 0 of a barrier only
+            // this warp arms), so the launch's time limit runs out
+            int w = 1;
+            if (leader)
+                w = mbar_wait_bounded(&ms->full[0], 0, abort_flag, p.wait_ns);
+            ok = __shfl_sync(kFull, w, 0) != 0;
+        }
         while (ok) {
             int item = 0;
             if (leader)
@@ -236,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     if (item == p.n_items + (int)gridDim.x - 1)
                         atomicExch(&p.status[16], 0);  // last grab of the launch: reset the queue
                     if (uses[stage] > 0)
-                        w = mbar_wait_bounded(&ms->kv_empty[stage], (uses[stage] - 1) & 1, abort_flag);
+                        w = mbar_wait_bounded(&ms->kv_empty[stage], (uses[stage] - 1) & 1, abort_flag, p.wait_ns);
                     if (w) {
                         ms->desc[stage] = TileDesc{item, 0, 0, kEnd};
                         mbar_arrive(&ms->full[stage]);
@@ -281,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             int w = 1;
             if (leader) {
                 if (q_uses[qb] > 0)
-                    w = mbar_wait_bounded(&ms->q_empty[qb], (q_uses[qb] - 1) & 1, abort_flag);
+                    w = mbar_wait_bounded(&ms->q_empty[qb], (q_uses[qb] - 1) & 1, abort_flag, p.wait_ns);
                 if (w) {
                     unsigned char *qd = smem + kQOff + qb * kQBytes;
                     mbar_arrive_expect_tx(&ms->q_full[qb], 2u * G * 128u);
@@ -327,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 w = 1;
                 if (leader) {
                     if (uses[stage] > 0)
-                        w = mbar_wait_bounded(&ms->kv_empty[stage], (uses[stage] - 1) & 1, abort_flag);
+                        w = mbar_wait_bounded(&ms->kv_empty[stage], (uses[stage] - 1) & 1, abort_flag, p.wait_ns);
                     if (w) {
                         ms->desc[stage] = TileDesc{item, j0, n, flags};
                         if (bytes)
@@ -419,19 +429,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 constexpr uint32_t kIdS = tc::idesc_bf16_f32_major(kRows, kN, false, false);
                 int ic = 0;
                 for (;;) {
-                    if (!mbar_wait_bounded(&ms->full[stage], sph, abort_flag))
+                    if (!mbar_wait_bounded(&ms->full[stage], sph, abort_flag, p.wait_ns))
                         break;
                     const TileDesc d = ms->desc[stage];
                     // S and P buffers of this parity are free once the value
                     // product of tile t - 2 is done (its softmax read S, it read P)
-                    if (t >= 2 && !mbar_wait_bounded(&ms->o_full[t & 1], ((t - 2) >> 1) & 1, abort_flag))
+                    if (t >= 2 && !mbar_wait_bounded(&ms->o_full[t & 1], ((t - 2) >> 1) & 1, abort_flag, p.wait_ns))
                         break;
                     if (d.flags & kEnd) {
                         mbar_arrive(&ms->s_full[t & 1]);  // tells the softmax warps to stop
                         break;
                     }
                     const int qb = ic & 1;
-                    if ((d.flags & kFirst) && !mbar_wait_bounded(&ms->q_full[qb], (ic >> 1) & 1, abort_flag))
+                    if ((d.flags & kFirst) && !mbar_wait_bounded(&ms->q_full[qb], (ic >> 1) & 1, abort_flag, p.wait_ns))
                         break;
                     tc::fence_after_sync();
                     // S_t^T = K Q^T over D in 8 steps of 16
@@ -459,11 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             } else {
                 constexpr uint32_t kIdPV = tc::idesc_bf16_f32_major(kRows, kON, true, false);
                 for (;;) {
-                    if (!mbar_wait_bounded(&ms->full[stage], sph, abort_flag))
+                    if (!mbar_wait_bounded(&ms->full[stage], sph, abort_flag, p.wait_ns))
                         break;
                     if (ms->desc[stage].flags & kEnd)
                         break;
-                    if (!mbar_wait_bounded(&ms->o_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag))
+                    if (!mbar_wait_bounded(&ms->o_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag, p.wait_ns))
                         break;
                     // O_t^T = V^T P^T: A = V (MN-major: the two 64-dim halves
                     // 16 KiB apart, 8-key groups 1 KiB apart), B = P (K-major).
@@ -475,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     bool ok = true;
 #pragma unroll
                     for (int w = 0; w < 4 && ok; ++w) {
-                        ok = mbar_wait_bounded(&ms->p_full[t & 1][w], (t >> 1) & 1, abort_flag);
+                        ok = mbar_wait_bounded(&ms->p_full[t & 1][w], (t >> 1) & 1, abort_flag, p.wait_ns);
                         if (!ok)
                             break;
                         tc::fence_after_sync();
@@ -525,14 +535,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&ms->grp_bar);
-            const bool w = mbar_wait_bounded(&ms->grp_bar, gph, abort_flag);
+            const bool w = mbar_wait_bounded(&ms->grp_bar, gph, abort_flag, p.wait_ns);
             gph ^= 1;
             return __all_sync(kFull, w);
         };
         // o[w] = o[w] * alpha_w + O_x[w] for the four warps' columns of tile x
         auto accumulate = [&](int x) -> bool {
-            bool w = mbar_wait_bounded(&ms->o_full[x & 1], (x >> 1) & 1, abort_flag);
-            w = w && mbar_wait_bounded(&ms->p_all[x & 1], (x >> 1) & 1, abort_flag);  // the factors
+            bool w = mbar_wait_bounded(&ms->o_full[x & 1], (x >> 1) & 1, abort_flag, p.wait_ns);
+            w = w && mbar_wait_bounded(&ms->p_all[x & 1], (x >> 1) & 1, abort_flag, p.wait_ns);  // the factors
             if (!__all_sync(kFull, w))
                 return false;
             tc::fence_after_sync();
@@ -552,8 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             return true;
         };
         for (;;) {
-            bool w = mbar_wait_bounded(&ms->s_full[t & 1], (t >> 1) & 1, abort_flag);
-            w = w && mbar_wait_bounded(&ms->full[stage], sph, abort_flag);  // descriptor and V visible
+            bool w = mbar_wait_bounded(&ms->s_full[t & 1], (t >> 1) & 1, abort_flag, p.wait_ns);
+            w = w && mbar_wait_bounded(&ms->full[stage], sph, abort_flag, p.wait_ns);  // descriptor and V visible
             if (!__all_sync(kFull, w))
                 break;
             const TileDesc d = ms->desc[stage];
@@ -831,6 +841,8 @@ cudaError_t launch_decode_tc(const DecodeLaunch &a)
     else
         p.mode = decode_merges_itself(a.plan.n_split, a.B * a.Hkv) ? kModeFused : kModePartials;
     p.status = a.status;
+    p.wait_ns = a.wait_ns;
+    p.test_stall = a.test_stall;
     p.counters = a.counters;
     p.part_m = a.part_m;
     p.part_l = a.part_l;

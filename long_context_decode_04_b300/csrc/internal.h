@@ -23,6 +23,10 @@ constexpr int kMaxFusedUnits = (kCtrlBytes - kStatusBytes) / 4;
 // Up to this many chunks per (sequence, KV head), and kMaxFusedUnits units,
 // the decode kernel merges the partials itself.
 constexpr int kFusedMergeMaxSplits = 64;
+// Time limit of a pipeline wait inside the kernels when the caller sets none.
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
+inline uint64_t wait_limit_or_default(uint64_t ns) { return ns ? ns : kDefaultWaitLimitNs; }
 
 struct DecodeLaunch {
     const void *q, *k, *v;
@@ -42,11 +46,22 @@ struct DecodeLaunch {
     int pi_window, pi_period;          // pi-Attention key set (period 0: every key)
     bool kv_fp8;                       // K/V are e4m3 bytes (q bf16), dequantised by
     const float *k_scale, *v_scale;    //   per (sequence, KV head) factors
+    uint64_t wait_ns;                  // time limit of a pipeline wait (ns)
+    int test_stall;                    // test hook (ta_test_stall_next_launches)
     cudaStream_t stream;
 };
 
 // Set the calling thread's message returned by ta_last_error (api.cpp).
 void record_error(const std::string &msg);
+
+// The test hook of ta_test_fail_next_launches (api.cpp): called by every
+// launcher just before it would launch; cudaErrorLaunchFailure (and no
+// launch) while injected failures are pending, else cudaSuccess.
+cudaError_t injected_launch_failure();
+// The test hook of ta_test_stall_next_launches (api.cpp): 1 while stalled
+// launches are pending (the launch's producer then first waits on a barrier
+// that nothing completes, so its time limit runs out), else 0.
+int injected_stall();
 
 // The argument checks of ta_decode_ex, on their own (api.cpp): TA_OK or the
 // status (with its message recorded) that ta_decode_ex would return.
@@ -97,11 +112,23 @@ bool decode_fp8_tc_eligible(const DecodeLaunch &a);
 cudaError_t launch_decode_fp8_tc(const DecodeLaunch &a);
 cudaError_t launch_combine(const float *m, const float *l, const float *o, int R, int N, int D, void *out,
                            ta_dtype out_dtype, float *lse, void *scratch, cudaStream_t stream);
-cudaError_t launch_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse, int B,
-                                  int H, int Hkv, int S, int D, float scale, int32_t *status,
-                                  cudaStream_t stream);
-cudaError_t launch_prefill_causal_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
-                                         const int32_t *cu_seqlens, int num_seqs, int max_seqlen, int T, int H,
-                                         int Hkv, int D, float scale, int32_t *status, cudaStream_t stream);
+// One causal prefill launch (prefill.cu): batched [B, H, S, D] layouts, or
+// packed [T, heads, D] layouts when cu_seqlens is given (B sequences, S =
+// the longest).
+struct PrefillLaunch {
+    const void *q, *k, *v;
+    void *out;
+    float *lse;
+    int B, H, Hkv, S, D;
+    float scale;
+    const int32_t *cu_seqlens;
+    int T;
+    ta_dtype out_dtype;
+    int32_t *status;
+    uint64_t wait_ns;
+    int test_stall;
+    cudaStream_t stream;
+};
+cudaError_t launch_prefill(const PrefillLaunch &a);
 
 }  // namespace ta

@@ -36,12 +36,14 @@
 //            tile, keep the running reference m (rescaled lazily: only when
 //            the row maximum exceeds it by more than 2^8, and then also
 //            O_t in TMEM), write P = 2^(s*scale*log2e - m) as fp16 into the
-//            first 64 columns of the S tile, and accumulate the row sum l
-//            from P before rounding (fp16 rounding of P moves the output by
-//            at most ~2^-12 of the value range).  The two warpgroups
-//            ping-pong: while one does its softmax the tensor cores run the
-//            other's PV and QK^T.
-//            Epilogue: out = O / l in bf16, lse = (m + log2 l) * ln 2.
+//            first 64 columns of the S tile, and accumulate two row sums:
+//            l over P as computed (for lse) and lr over P as rounded to fp16,
+//            the weights the PV product uses (for the output, which is then a
+//            weighted mean whose weights sum to one exactly; their fp16
+//            rounding moves it by at most ~2^-12 of the value range).  The two
+//            warpgroups ping-pong: while one does its softmax the tensor cores
+//            run the other's PV and QK^T.
+//            Epilogue: out = O / lr in bf16 or fp32, lse = (m + log2 l) * ln 2.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
 // Every wait is bounded; on expiry TA_DEVERR_TIMEOUT is recorded, all roles
 // stop, outstanding copies and MMAs are drained and the TMEM is freed.
@@ -81,13 +83,15 @@ struct PrefillParams {
     CUtensorMap qmap;
     CUtensorMap kmap;
     CUtensorMap vmap;
-    __nv_bfloat16 *out;
+    void *out;              // bf16 or fp32 (the kernel's OUT type)
     float *lse;
     int S, H, G, n_qt, BH;  // S: keys per sequence (batched) or max_seqlen (packed)
     float c;                // scale * log2(e)
     int32_t *status;
     const int32_t *cu_seqlens;  // packed: [BH / H + 1] token offsets; nullptr: batched
     int T;                      // packed: total tokens
+    uint64_t wait_ns;           // time limit of a pipeline wait
+    int test_stall;             // test hook: the producer first waits on a barrier nothing ends
 };
 
 struct Bars {
@@ -105,6 +109,28 @@ struct Bars {
     int abort;
 };
 
+// l += the two fp16 weights of a packed pair, each widened exactly
+// (mixed-precision FMA with f16 operands and an fp32 accumulator)
+__device__ __forceinline__ float add_f16x2(float acc, uint32_t w)
+{
+    float r;
+    asm("{\n\t.reg .f16 lo, hi, one;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "mov.b16 one, 0x3C00;\n\t"
+        "fma.rn.f32.f16 %0, lo, one, %2;\n\t"
+        "fma.rn.f32.f16 %0, hi, one, %0;\n\t}"
+        : "=f"(r)
+        : "r"(w), "f"(acc));
+    return r;
+}
+
+__device__ __forceinline__ uint4 out_pack4(const float *x, __nv_bfloat16 *)
+{
+    return make_uint4(tc::pack_bf16x2(x[0], x[1]), tc::pack_bf16x2(x[2], x[3]), tc::pack_bf16x2(x[4], x[5]),
+                      tc::pack_bf16x2(x[6], x[7]));
+}
+
+template <typename OUT>
 __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __grid_constant__ PrefillParams p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -175,21 +201,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
             tc::prefetch_tensormap(&p.qmap);
             tc::prefetch_tensormap(&p.kmap);
             tc::prefetch_tensormap(&p.vmap);
+            // test hook: a wait that nothing ends (phase 0 of a barrier only
+            // this thread arms), so the launch's time limit runs out and the
+            // CTA issues nothing
+            const bool go = !p.test_stall || mbar_wait_bounded(&bars->k_full[0], 0, abort_flag, p.wait_ns);
             const int n_q = active1 ? 2 : 1;
-            mbar_arrive_expect_tx(&bars->q_full, n_q * kTileBytes);
-            for (int t = 0; t < n_q; ++t) {
-                unsigned char *dst = smem + kQOff + t * kTileBytes;
-                tc::tma_load_3d(dst, &p.qmap, 0, y0 + q0 + t * kBM, zq, &bars->q_full);
-                tc::tma_load_3d(dst + kHalfBytes, &p.qmap, 64, y0 + q0 + t * kBM, zq, &bars->q_full);
+            if (go) {
+                mbar_arrive_expect_tx(&bars->q_full, n_q * kTileBytes);
+                for (int t = 0; t < n_q; ++t) {
+                    unsigned char *dst = smem + kQOff + t * kTileBytes;
+                    tc::tma_load_3d(dst, &p.qmap, 0, y0 + q0 + t * kBM, zq, &bars->q_full);
+                    tc::tma_load_3d(dst + kHalfBytes, &p.qmap, 64, y0 + q0 + t * kBM, zq, &bars->q_full);
+                }
             }
             // Issue order K0, K1, V0, K2, V1, ...: K runs one tile ahead of
             // V, since S of a tile needs K while its PV comes a softmax later.
             int k_armed[kKStages] = {0, 0, 0}, v_armed[kVStages] = {0, 0};
-            bool ok = true;
+            bool ok = go;
             for (int i = 0; ok && i <= nk; ++i) {
                 if (i < nk) {  // K tile i
                     const int st = i % kKStages, use = i / kKStages;
-                    if (use > 0 && !mbar_wait_bounded(&bars->k_empty[st], (use - 1) & 1, abort_flag)) {
+                    if (use > 0 && !mbar_wait_bounded(&bars->k_empty[st], (use - 1) & 1, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -202,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                 if (i > 0) {  // V tile i - 1
                     const int j = i - 1;
                     const int st = j % kVStages, use = j / kVStages;
-                    if (use > 0 && !mbar_wait_bounded(&bars->v_empty[st], (use - 1) & 1, abort_flag)) {
+                    if (use > 0 && !mbar_wait_bounded(&bars->v_empty[st], (use - 1) & 1, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -213,10 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                     ++v_armed[st];
                 }
             }
-            if (*abort_flag) {
-                // Every copy issued must land before the CTA exits.
+            {
+                // Every copy issued lands before the CTA exits, whether or
+                // not some role gave up: a role may give up after this
+                // thread has issued its last copy, so the drain cannot
+                // depend on the abort flag (on the normal path the waits
+                // end as soon as the last copies land).
                 int drain_abort = 0;
-                mbar_wait_bounded(&bars->q_full, 0, &drain_abort);
+                if (go)
+                    mbar_wait_bounded(&bars->q_full, 0, &drain_abort);
                 for (int st = 0; st < kKStages; ++st)
                     if (k_armed[st] > 0)
                         mbar_wait_bounded(&bars->k_full[st], (k_armed[st] - 1) & 1, &drain_abort);
@@ -232,12 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
             constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kBM, kBN, false);
             constexpr uint32_t kIdescPV = tc::idesc_f16_f32(kBM, kHD, true);
             const uint32_t sbase = smem_u32(smem);
-            bool ok = mbar_wait_bounded(&bars->q_full, 0, abort_flag);
+            bool ok = mbar_wait_bounded(&bars->q_full, 0, abort_flag, p.wait_ns);
             tc::fence_after_sync();
             for (int j = 0; ok && j <= nk; ++j) {
                 const int st = j % kKStages;
                 if (j < nk) {
-                    ok = mbar_wait_bounded(&bars->k_full[st], (j / kKStages) & 1, abort_flag);
+                    ok = mbar_wait_bounded(&bars->k_full[st], (j / kKStages) & 1, abort_flag, p.wait_ns);
                     if (!ok)
                         break;
                     tc::fence_after_sync();
@@ -250,10 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                     const uint32_t o_tmem = tmem + 2 * kBN + t * kHD;
                     if (j > 0 && t_active && j - 1 <= diag) {
                         // O_t += P_t(j-1) V_{j-1}
-                        ok = mbar_wait_bounded(&bars->p_full[t], (j - 1) & 1, abort_flag);
+                        ok = mbar_wait_bounded(&bars->p_full[t], (j - 1) & 1, abort_flag, p.wait_ns);
                         if (ok && !v_ready) {
                             ok = mbar_wait_bounded(&bars->v_conv[(j - 1) % kVStages], ((j - 1) / kVStages) & 1,
-                                                   abort_flag);
+                                                   abort_flag, p.wait_ns);
                             v_ready = true;
                         }
                         if (!ok)
@@ -303,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
         uint32_t vmax = 0;  // largest |v| bit pattern seen, per 16-bit half
         for (int j = 0; j < nk; ++j) {
             const int st = j % kVStages;
-            bool ok = mbar_wait_bounded(&bars->v_full[st], (j / kVStages) & 1, abort_flag);
+            bool ok = mbar_wait_bounded(&bars->v_full[st], (j / kVStages) & 1, abort_flag, p.wait_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok)
                 break;
@@ -338,10 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
             const uint32_t s_tmem = tmem + lane_base + t * kBN;
             const uint32_t o_tmem = tmem + lane_base + 2 * kBN + t * kHD;
             const float c = p.c;
-            float m_used = -INFINITY, l = 0.f;
+            // l: the row sum of the weights as computed (for lse); lr: the
+            // same weights as rounded to fp16, the values the PV product
+            // multiplies (for the normalisation of O, so that the output is
+            // a weighted mean whose weights sum to one exactly)
+            float m_used = -INFINITY, l = 0.f, lr = 0.f;
             bool ok = true;
             for (int j = 0; j <= diag; ++j) {
-                ok = mbar_wait_bounded(&bars->s_full[t], j & 1, abort_flag);
+                ok = mbar_wait_bounded(&bars->s_full[t], j & 1, abort_flag, p.wait_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok)
                     break;
@@ -383,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                     m_used = mcand;
                 }
                 const float neg_m = -m_used;
-                float ls = 0.f;
+                float ls[2] = {0.f, 0.f}, lsr[2] = {0.f, 0.f};
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t pk[32];
@@ -393,11 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                         const float p1 = fast_exp2(fmaf(s[half * 64 + 2 * i + 1], c, neg_m));
                         const uint32_t w = tc::pack_f16x2(p0, p1);
                         pk[i] = w;
-                        ls += p0 + p1;
+                        ls[i & 1] += p0 + p1;
+                        lsr[i & 1] = add_f16x2(lsr[i & 1], w);
                     }
                     tc::tmem_st32(s_tmem + half * 32, pk);
                 }
-                l = l * alpha + ls;
+                l = l * alpha + (ls[0] + ls[1]);
+                lr = lr * alpha + (lsr[0] + lsr[1]);
                 if (j > 0 && __any_sync(0xffffffffu, resc)) {
                     // O_t holds every PV up to j-1 (see the MMA issuer);
                     // bring it to the new reference.
@@ -422,34 +465,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                 mbar_arrive(&bars->p_full[t]);
             }
             if (ok) {
-                ok = mbar_wait_bounded(&bars->o_full[t], 0, abort_flag);
+                ok = mbar_wait_bounded(&bars->o_full[t], 0, abort_flag, p.wait_ns);
                 ok = __all_sync(0xffffffffu, ok);
             }
             if (ok) {
                 tc::fence_after_sync();
                 const int row = qrow0 + r;
-                const float inv = 1.0f / l;
+                const float inv = 1.0f / lr;
                 // output row: [b*H + h][S][D] batched, [T][H][D] packed; lse
                 // [b*H + h][S] batched, [H][T] packed
-                __nv_bfloat16 *orow = p.cu_seqlens ? p.out + ((size_t)(y0 + row) * p.H + zq) * kHD
-                                                   : p.out + ((size_t)bh * p.S + row) * kHD;
+                OUT *const obase = static_cast<OUT *>(p.out);
+                OUT *orow = p.cu_seqlens ? obase + ((size_t)(y0 + row) * p.H + zq) * kHD
+                                         : obase + ((size_t)bh * p.S + row) * kHD;
                 const size_t lse_at = p.cu_seqlens ? (size_t)zq * p.T + y0 + row : (size_t)bh * p.S + row;
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t u[32];
                     tc::tmem_ld32(o_tmem + ch * 32, u);
                     tc::tmem_wait_ld(u);
-                    uint32_t pk[16];
+                    float o[32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pk[i] = tc::pack_bf16x2(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = __uint_as_float(u[i]) * inv;
                     if (row < L) {
                         // streaming stores: the output is not read again here,
                         // so its lines leave L2 first instead of lingering dirty
                         uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
+                        if constexpr (sizeof(OUT) == 2) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            __stcs(dst + i, make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]));
+                            for (int i = 0; i < 4; ++i)
+                                __stcs(dst + i, out_pack4(o + 8 * i, (__nv_bfloat16 *)nullptr));
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                __stcs(dst + i, make_uint4(__float_as_uint(o[4 * i]), __float_as_uint(o[4 * i + 1]),
+                                                           __float_as_uint(o[4 * i + 2]),
+                                                           __float_as_uint(o[4 * i + 3])));
+                        }
                     }
                 }
                 if (row < L && p.lse)
@@ -482,68 +534,48 @@ bool make_map(CUtensorMap *m, const void *base, int S, int rows3)
 
 }  // namespace
 
-cudaError_t launch_prefill_causal(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
-                                  int Hkv, int S, int D, float scale, int32_t *status, cudaStream_t stream)
+cudaError_t launch_prefill(const PrefillLaunch &a)
 {
-    if (D != kHD)
+    if (a.D != kHD)
         return cudaErrorNotSupported;
+    if (cudaError_t inj = injected_launch_failure())
+        return inj;
     PrefillParams p;
-    if (!make_map(&p.qmap, q, S, B * H) || !make_map(&p.kmap, k, S, B * Hkv) || !make_map(&p.vmap, v, S, B * Hkv))
-        return cudaErrorInvalidValue;
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    p.lse = lse;
-    p.S = S;
-    p.H = H;
-    p.G = H / Hkv;
-    p.n_qt = (S + 2 * kBM - 1) / (2 * kBM);
-    p.BH = B * H;
-    p.c = scale * kLog2e;
-    p.status = status;
-    p.cu_seqlens = nullptr;
-    p.T = 0;
-    cudaError_t e = cudaFuncSetAttribute(prefill_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    if (!a.cu_seqlens) {
+        if (!make_map(&p.qmap, a.q, a.S, a.B * a.H) || !make_map(&p.kmap, a.k, a.S, a.B * a.Hkv) ||
+            !make_map(&p.vmap, a.v, a.S, a.B * a.Hkv))
+            return cudaErrorInvalidValue;
+    } else {
+        // the packed tensors as {D, T, heads}: token stride heads * D, head stride D
+        const uint64_t qdims[3] = {(uint64_t)kHD, (uint64_t)a.T, (uint64_t)a.H};
+        const uint64_t qstr[2] = {(uint64_t)a.H * kHD * 2, (uint64_t)kHD * 2};
+        const uint64_t kdims[3] = {(uint64_t)kHD, (uint64_t)a.T, (uint64_t)a.Hkv};
+        const uint64_t kstr[2] = {(uint64_t)a.Hkv * kHD * 2, (uint64_t)kHD * 2};
+        const uint32_t box[3] = {64, (uint32_t)kBM, 1};
+        if (!encode_tmap_3d(&p.qmap, a.q, true, qdims, qstr, box, true) ||
+            !encode_tmap_3d(&p.kmap, a.k, true, kdims, kstr, box, true) ||
+            !encode_tmap_3d(&p.vmap, a.v, true, kdims, kstr, box, true))
+            return cudaErrorInvalidValue;
+    }
+    p.out = a.out;
+    p.lse = a.lse;
+    p.S = a.S;  // packed: max_seqlen
+    p.H = a.H;
+    p.G = a.H / a.Hkv;
+    p.n_qt = (a.S + 2 * kBM - 1) / (2 * kBM);
+    p.BH = a.B * a.H;  // packed: B = number of sequences
+    p.c = a.scale * kLog2e;
+    p.status = a.status;
+    p.cu_seqlens = a.cu_seqlens;
+    p.T = a.cu_seqlens ? a.T : 0;
+    p.wait_ns = a.wait_ns;
+    p.test_stall = a.test_stall;
+    auto kern = a.out_dtype == TA_F32 ? prefill_causal_kernel<float> : prefill_causal_kernel<__nv_bfloat16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess)
         return e;
     const long long grid = (long long)p.n_qt * p.BH;
-    prefill_causal_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_prefill_causal_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
-                                         const int32_t *cu_seqlens, int num_seqs, int max_seqlen, int T, int H,
-                                         int Hkv, int D, float scale, int32_t *status, cudaStream_t stream)
-{
-    if (D != kHD)
-        return cudaErrorNotSupported;
-    PrefillParams p;
-    // the packed tensors as {D, T, heads}: token stride heads * D, head stride D
-    const uint64_t qdims[3] = {(uint64_t)kHD, (uint64_t)T, (uint64_t)H};
-    const uint64_t qstr[2] = {(uint64_t)H * kHD * 2, (uint64_t)kHD * 2};
-    const uint64_t kdims[3] = {(uint64_t)kHD, (uint64_t)T, (uint64_t)Hkv};
-    const uint64_t kstr[2] = {(uint64_t)Hkv * kHD * 2, (uint64_t)kHD * 2};
-    const uint32_t box[3] = {64, (uint32_t)kBM, 1};
-    if (!encode_tmap_3d(&p.qmap, q, true, qdims, qstr, box, true) ||
-        !encode_tmap_3d(&p.kmap, k, true, kdims, kstr, box, true) ||
-        !encode_tmap_3d(&p.vmap, v, true, kdims, kstr, box, true))
-        return cudaErrorInvalidValue;
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    p.lse = lse;
-    p.S = max_seqlen;
-    p.H = H;
-    p.G = H / Hkv;
-    p.n_qt = (max_seqlen + 2 * kBM - 1) / (2 * kBM);
-    p.BH = num_seqs * H;
-    p.c = scale * kLog2e;
-    p.status = status;
-    p.cu_seqlens = cu_seqlens;
-    p.T = T;
-    cudaError_t e = cudaFuncSetAttribute(prefill_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess)
-        return e;
-    const long long grid = (long long)p.n_qt * p.BH;
-    prefill_causal_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p);
+    kern<<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(p);
     return cudaGetLastError();
 }
 

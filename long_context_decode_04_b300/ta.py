@@ -44,7 +44,7 @@ class DecodeParams(ctypes.Structure):
                 ("seqlens", ctypes.c_void_p), ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
                 ("chunk", ctypes.c_int32), ("n_split", ctypes.c_int32),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("stream", ctypes.c_void_p)]
+                ("stream", ctypes.c_void_p), ("wait_limit_ns", ctypes.c_uint64)]
 
 
 class PagedDecodeParams(ctypes.Structure):
@@ -56,7 +56,16 @@ class PagedDecodeParams(ctypes.Structure):
                 ("scale", ctypes.c_float), ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
                 ("chunk", ctypes.c_int32), ("n_split", ctypes.c_int32),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("stream", ctypes.c_void_p)]
+                ("stream", ctypes.c_void_p), ("wait_limit_ns", ctypes.c_uint64)]
+
+
+class PrefillParams(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("S", ctypes.c_int32), ("D", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("cu_seqlens", ctypes.c_void_p), ("total_tokens", ctypes.c_int32), ("out_dtype", ctypes.c_int),
+                ("wait_limit_ns", ctypes.c_uint64), ("stream", ctypes.c_void_p)]
 
 
 _lib = None
@@ -88,11 +97,18 @@ def lib() -> ctypes.CDLL:
         L.ta_combine_workspace_bytes.restype = st
         L.ta_prefill_causal.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         L.ta_prefill_causal_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+        L.ta_prefill_causal_ex.argtypes = [ctypes.POINTER(PrefillParams)]
+        L.ta_decode_noalloc_setup.argtypes = []
+        L.ta_decode_noalloc_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        L.ta_test_fail_next_launches.argtypes = [i]
+        L.ta_test_fail_next_launches.restype = ctypes.c_int
+        L.ta_test_stall_next_launches.argtypes = [i]
+        L.ta_test_stall_next_launches.restype = ctypes.c_int
         L.ta_last_error.argtypes = []
         L.ta_last_error.restype = ctypes.c_char_p
         for fn in ("ta_decode", "ta_decode_noalloc", "ta_decode_ex", "ta_decode_paged", "ta_decode_pi", "ta_decode_fp8",
                    "ta_prefill_causal_varlen", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
-                   "ta_prefill_causal"):
+                   "ta_prefill_causal", "ta_prefill_causal_ex", "ta_decode_noalloc_setup", "ta_decode_noalloc_status"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -134,7 +150,7 @@ def decode_workspace(B, Hq, Hkv, S, D, *, chunk=0, n_split=0, varlen=False, devi
 
 
 def decode(q, k, v, *, seqlens=None, scale=None, out_dtype=None, chunk=0, n_split=0, workspace=None,
-           out=None, lse=None):
+           out=None, lse=None, wait_limit_ns=0):
     """Split-KV decode.  q [B,Hq,D], k/v [B,Hkv,S,D] (bf16 or fp32, CUDA), seqlens [B] int32.
 
     Returns (out [B,Hq,D], lse [B,Hq] fp32).  ``workspace`` (uint8 CUDA tensor
@@ -161,12 +177,13 @@ def decode(q, k, v, *, seqlens=None, scale=None, out_dtype=None, chunk=0, n_spli
     if workspace is not None:
         p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     p.stream = torch.cuda.current_stream(q.device).cuda_stream
+    p.wait_limit_ns = int(wait_limit_ns)
     _check(lib().ta_decode_ex(ctypes.byref(p)))
     return out, lse
 
 
 def decode_pi(q, k, v, window, period, *, seqlens=None, scale=None, out_dtype=None, chunk=0, n_split=0,
-              workspace=None, out=None, lse=None):
+              workspace=None, out=None, lse=None, wait_limit_ns=0):
     """Decode over the pi-Attention key set: the window of the last ``window``
     keys plus every ``period``-th key before it, counted back from the
     newest.  Shapes as ``decode``; returns (out, lse)."""
@@ -176,13 +193,14 @@ def decode_pi(q, k, v, window, period, *, seqlens=None, scale=None, out_dtype=No
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    p = _params(q, k, v, seqlens, scale, chunk, n_split, workspace, out=out, lse=lse, out_dtype=out.dtype)
+    p = _params(q, k, v, seqlens, scale, chunk, n_split, workspace, out=out, lse=lse, out_dtype=out.dtype,
+                wait_limit_ns=wait_limit_ns)
     _check(lib().ta_decode_pi(ctypes.byref(p), int(window), int(period)))
     return out, lse
 
 
 def decode_fp8(q, k8, v8, *, k_scale=None, v_scale=None, seqlens=None, scale=None, out_dtype=None, chunk=0,
-               n_split=0, workspace=None, out=None, lse=None):
+               n_split=0, workspace=None, out=None, lse=None, wait_limit_ns=0):
     """Decode over an E4M3 KV cache.  q [B,Hq,D] bf16; k8/v8 [B,Hkv,S,D] uint8
     (E4M3 bit patterns); k_scale/v_scale [B*Hkv] fp32 or None.  Returns
     (out, lse)."""
@@ -192,7 +210,8 @@ def decode_fp8(q, k8, v8, *, k_scale=None, v_scale=None, seqlens=None, scale=Non
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    p = _params(q, k8, v8, seqlens, scale, chunk, n_split, workspace, out=out, lse=lse, out_dtype=out.dtype)
+    p = _params(q, k8, v8, seqlens, scale, chunk, n_split, workspace, out=out, lse=lse, out_dtype=out.dtype,
+                wait_limit_ns=wait_limit_ns)
     _check(lib().ta_decode_fp8(ctypes.byref(p), _ptr(k_scale), _ptr(v_scale)))
     return out, lse
 
@@ -206,7 +225,7 @@ def decode_pi_workspace(B, Hq, Hkv, S, D, window, period, *, chunk=0, n_split=0,
 
 
 def decode_paged(q, k_pages, v_pages, block_table, seqlens, *, scale=None, out_dtype=None, chunk=0, n_split=0,
-                 workspace=None, out=None, lse=None):
+                 workspace=None, out=None, lse=None, wait_limit_ns=0):
     """Split-KV decode over a paged KV cache.
 
     q [B,Hq,D]; k_pages/v_pages [num_pages,Hkv,page_size,D]; block_table
@@ -235,11 +254,13 @@ def decode_paged(q, k_pages, v_pages, block_table, seqlens, *, scale=None, out_d
     if workspace is not None:
         p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     p.stream = torch.cuda.current_stream(q.device).cuda_stream
+    p.wait_limit_ns = int(wait_limit_ns)
     _check(lib().ta_decode_paged(ctypes.byref(p)))
     return out, lse
 
 
-def _params(q, k, v, seqlens, scale, chunk, n_split, workspace, out=None, lse=None, out_dtype=None):
+def _params(q, k, v, seqlens, scale, chunk, n_split, workspace, out=None, lse=None, out_dtype=None,
+            wait_limit_ns=0):
     B, Hq, D = q.shape
     _, Hkv, S, _ = k.shape
     p = DecodeParams()
@@ -255,6 +276,7 @@ def _params(q, k, v, seqlens, scale, chunk, n_split, workspace, out=None, lse=No
     if workspace is not None:
         p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     p.stream = torch.cuda.current_stream(q.device).cuda_stream
+    p.wait_limit_ns = int(wait_limit_ns)
     return p
 
 
@@ -292,6 +314,29 @@ def decode_noalloc(q, k, v, out, lse, scale, seqlens=None):
     return out, lse
 
 
+def decode_noalloc_setup() -> None:
+    """``ta_decode_noalloc_setup``: load the device code and find the fixed scratch on the current device."""
+    _check(lib().ta_decode_noalloc_setup())
+
+
+def decode_noalloc_status(device="cuda") -> int:
+    """Read and clear the status word of ``ta_decode_noalloc``'s fixed scratch (TA_DEVERR_* bits)."""
+    flags = ctypes.c_int32(0)
+    _check(lib().ta_decode_noalloc_status(_stream(torch.device(device)), ctypes.byref(flags)))
+    return flags.value
+
+
+def test_fail_next_launches(count: int) -> int:
+    """``ta_test_fail_next_launches``: refuse the next ``count`` kernel launches; returns the number pending."""
+    return int(lib().ta_test_fail_next_launches(int(count)))
+
+
+def test_stall_next_launches(count: int) -> int:
+    """``ta_test_stall_next_launches``: the next ``count`` decode / prefill launches
+    run out their wait time limit; returns the number pending."""
+    return int(lib().ta_test_stall_next_launches(int(count)))
+
+
 def decode_status(workspace=None, device="cuda") -> int:
     """Read and clear the device status word (TA_DEVERR_* bits)."""
     flags = ctypes.c_int32(0)
@@ -317,32 +362,57 @@ def combine_workspace_bytes(R, N, D) -> int:
     return int(lib().ta_combine_workspace_bytes(R, N, D))
 
 
-def prefill_causal(q, k, v, *, scale=None, out=None, lse=None):
-    """Causal prefill. q [B,H,S,D], k/v [B,Hkv,S,D] bf16 CUDA -> (out [B,H,S,D] bf16, lse [B,H,S] fp32)."""
+def _prefill_ex(q, k, v, out, lse, B, H, Hkv, S, D, scale, cu_seqlens, total_tokens, wait_limit_ns):
+    p = PrefillParams()
+    p.q, p.k, p.v, p.out, p.lse = q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr()
+    p.B, p.H, p.Hkv, p.S, p.D = B, H, Hkv, S, D
+    p.scale = scale
+    p.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
+    p.total_tokens = total_tokens
+    p.out_dtype = _dtype_code(out.dtype)
+    p.wait_limit_ns = int(wait_limit_ns)
+    p.stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(lib().ta_prefill_causal_ex(ctypes.byref(p)))
+
+
+def prefill_causal(q, k, v, *, scale=None, out=None, lse=None, out_dtype=None, wait_limit_ns=0):
+    """Causal prefill. q [B,H,S,D], k/v [B,Hkv,S,D] bf16 CUDA -> (out [B,H,S,D], lse [B,H,S] fp32).
+
+    ``out_dtype`` torch.bfloat16 (default) or torch.float32; the plain
+    ``ta_prefill_causal`` entry point serves the defaults, ``ta_prefill_causal_ex``
+    the rest."""
     B, H, S, D = q.shape
     Hkv = k.shape[1]
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    _check(lib().ta_prefill_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, S, D, scale,
-                                   _stream(q.device)))
+    if out.dtype == torch.bfloat16 and not wait_limit_ns:
+        _check(lib().ta_prefill_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, S, D, scale,
+                                       _stream(q.device)))
+    else:
+        _prefill_ex(q, k, v, out, lse, B, H, Hkv, S, D, scale, None, 0, wait_limit_ns)
     return out, lse
 
 
-def prefill_causal_varlen(q, k, v, cu_seqlens, max_seqlen, *, scale=None, out=None, lse=None):
+def prefill_causal_varlen(q, k, v, cu_seqlens, max_seqlen, *, scale=None, out=None, lse=None, out_dtype=None,
+                          wait_limit_ns=0):
     """Causal prefill of packed variable-length sequences.  q [T,H,D], k/v
-    [T,Hkv,D] bf16, cu_seqlens [num_seqs+1] int32 (CUDA) -> (out [T,H,D] bf16,
-    lse [H,T] fp32)."""
+    [T,Hkv,D] bf16, cu_seqlens [num_seqs+1] int32 (CUDA) -> (out [T,H,D], lse
+    [H,T] fp32); ``out_dtype`` as ``prefill_causal``."""
     T, H, D = q.shape
     Hkv = k.shape[1]
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
-    _check(lib().ta_prefill_causal_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
-                                          cu_seqlens.numel() - 1, int(max_seqlen), T, H, Hkv, D, scale,
-                                          _stream(q.device)))
+    if out.dtype == torch.bfloat16 and not wait_limit_ns:
+        _check(lib().ta_prefill_causal_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
+                                              cu_seqlens.numel() - 1, int(max_seqlen), T, H, Hkv, D, scale,
+                                              _stream(q.device)))
+    else:
+        _prefill_ex(q, k, v, out, lse, cu_seqlens.numel() - 1, H, Hkv, int(max_seqlen), D, scale, cu_seqlens, T,
+                    wait_limit_ns)
     return out, lse

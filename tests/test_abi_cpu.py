@@ -206,3 +206,46 @@ def test_fp8_decode_rejects_unsupported_shapes():
     assert L.ta_decode_fp8(ctypes.byref(p), None, None) == ta.TA_ERR_INVALID_ARG
     p = ta.DecodeParams(**base)
     assert L.ta_decode_fp8(ctypes.byref(p), ctypes.c_void_p(0x6002), None) == ta.TA_ERR_INVALID_ARG
+
+
+def test_prefill_ex_rejects_bad_arguments():
+    L = ta.lib()
+
+    def call(**kw):
+        base = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, B=1, H=8, Hkv=2, S=128, D=128,
+                    scale=0.1, cu_seqlens=None, total_tokens=0, out_dtype=ta.TA_F32, wait_limit_ns=0, stream=None)
+        base.update(kw)
+        p = ta.PrefillParams(**base)
+        return L.ta_prefill_causal_ex(ctypes.byref(p))
+
+    assert L.ta_prefill_causal_ex(None) == ta.TA_ERR_INVALID_ARG
+    assert call(out_dtype=7) == ta.TA_ERR_INVALID_ARG
+    assert call(H=6, Hkv=4) == ta.TA_ERR_INVALID_ARG
+    assert call(out=0x4004) == ta.TA_ERR_INVALID_ARG
+    assert call(D=64) == ta.TA_ERR_UNSUPPORTED
+    assert call(scale=-1.0) == ta.TA_ERR_UNSUPPORTED
+    assert call(cu_seqlens=0x6000, total_tokens=0) == ta.TA_ERR_INVALID_ARG  # packed needs tokens
+    assert call(cu_seqlens=0x6002, total_tokens=256) == ta.TA_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the hook ahead of the no-GPU error path")
+def test_launch_failure_hook_refuses_launches_after_validation():
+    """ta_test_fail_next_launches: a valid merge call whose launch is refused returns
+    TA_ERR_CUDA naming the hook (the merge of <= 64 partials makes no CUDA call
+    before its launch, so this runs without a GPU); a rejected call does not use
+    up an injected failure; once the count is spent the real outcome returns."""
+    L = ta.lib()
+    vp = ctypes.c_void_p
+    args = (vp(0x1000), vp(0x2000), vp(0x3000), 4, 2, 128, vp(0x4000), ta.TA_F32, None, None, 0, None)
+    assert L.ta_test_fail_next_launches(2) == 0
+    # bad arguments are rejected before the launch: no injected failure is used
+    assert L.ta_combine(vp(0x1000), vp(0x2000), vp(0x3000), 4, 0, 128, vp(0x4000), ta.TA_F32, None, None, 0,
+                        None) == ta.TA_ERR_INVALID_ARG
+    for _ in range(2):
+        assert L.ta_combine(*args) == ta.TA_ERR_CUDA
+        assert b"ta_test_fail_next_launches" in L.ta_last_error()
+    assert L.ta_test_fail_next_launches(0) == 0
+    assert L.ta_combine(*args) == ta.TA_ERR_CUDA  # no GPU here: the real launch error
+    assert b"ta_test_fail_next_launches" not in L.ta_last_error()
+    assert L.ta_test_fail_next_launches(5) == 0
+    assert L.ta_test_fail_next_launches(0) == 5  # cancelled with 5 pending

@@ -25,18 +25,20 @@ def _packed(lens, H, Hkv, seed):
     return q, k, v, cu, x["scale"]
 
 
-def _run(q, k, v, cu, max_len, scale):
-    out, lse = ta.prefill_causal_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cu.to(DEV), max_len, scale=scale)
+def _run(q, k, v, cu, max_len, scale, out_dtype=torch.bfloat16):
+    out, lse = ta.prefill_causal_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cu.to(DEV), max_len, scale=scale,
+                                        out_dtype=out_dtype)
     torch.cuda.synchronize()
     return out, lse
 
 
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 @pytest.mark.parametrize("lens", [[1, 127, 128, 129, 255, 256, 257, 700], [1000, 0, 3, 513], [384] * 3])
-def test_varlen_prefill_matches_oracle(lens):
+def test_varlen_prefill_matches_oracle(lens, out_dtype):
     q, k, v, cu, scale = _packed(lens, 8, 2, seed=1100 + len(lens))
-    out, lse = _run(q, k, v, cu, max(lens), scale)
+    out, lse = _run(q, k, v, cu, max(lens), scale, out_dtype)
     ro, rl = oracle.prefill_causal_varlen(q, k, v, cu.numpy(), scale)
-    check_out(out.float().cpu().numpy().reshape(-1, 128), ro.reshape(-1, 128), bf16=True)
+    check_out(out.float().cpu().numpy().reshape(-1, 128), ro.reshape(-1, 128), bf16=out_dtype == torch.bfloat16)
     check_lse(lse.cpu().numpy(), rl)
     assert ta.decode_status() == 0
 
@@ -69,11 +71,12 @@ def test_offsets_past_max_seqlen_are_flagged_not_followed():
     assert np.all(o[300 + 512:] == 7.0)
 
 
-def test_varlen_32_heads_mixed_lengths():
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_varlen_32_heads_mixed_lengths(out_dtype):
     rng = np.random.Generator(np.random.PCG64(1400))
     lens = [int(x) for x in rng.integers(1, 4096, size=4, endpoint=True)]
     q, k, v, cu, scale = _packed(lens, 32, 8, seed=1400)
-    out, lse = _run(q, k, v, cu, max(lens), scale)
+    out, lse = _run(q, k, v, cu, max(lens), scale, out_dtype)
     ro, rl = oracle.prefill_causal_varlen(q, k, v, cu.numpy(), scale)
-    check_out(out.float().cpu().numpy().reshape(-1, 128), ro.reshape(-1, 128), bf16=True)
+    check_out(out.float().cpu().numpy().reshape(-1, 128), ro.reshape(-1, 128), bf16=out_dtype == torch.bfloat16)
     check_lse(lse.cpu().numpy(), rl)

@@ -1,14 +1,17 @@
 """ta_decode_noalloc, the decode entry point for callers that cannot allocate
 device memory (their GPU memory is held by a pool allocator, or allocation
 after start-up is forbidden): it must give what ta_decode gives, call after
-call, using only its fixed scratch array.
+call, using only its fixed scratch array, and its results must match the
+float64 oracle within the usual tolerances.
 
 Called through the C ABI.  Kept in a file that pytest collects last, so that
 a run stopping at the first failure has already run every other test.
 """
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from long_context_decode_04_b300 import synth, ta
 from tests.parity import check_lse, check_out
 
@@ -21,7 +24,7 @@ def _inputs(name, **kw):
     x = synth.make_inputs(synth.WORKLOADS[name], **kw)
     q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
     sl = None if x["seqlens"] is None else x["seqlens"].to(DEV)
-    return q, k, v, sl, x["scale"]
+    return x, (q, k, v, sl, x["scale"])
 
 
 def _both(q, k, v, sl, scale):
@@ -36,9 +39,15 @@ def _both(q, k, v, sl, scale):
     return out, lse, ref_out, ref_lse
 
 
-def _compare(out, lse, ref_out, ref_lse):
+def _compare(x, out, lse, ref_out, ref_lse):
+    # against ta_decode (the same arithmetic: the tolerance is generous) ...
     check_out(out.float().cpu().numpy(), ref_out.double().cpu().numpy(), bf16=True)
     check_lse(lse.cpu().numpy(), ref_lse.double().cpu().numpy())
+    # ... and against the float64 oracle
+    sl = None if x["seqlens"] is None else x["seqlens"].numpy()
+    ro, rl = oracle.decode(x["q"], x["k"], x["v"], x["scale"], seqlens=sl)
+    check_out(out.float().cpu().numpy().reshape(ro.shape), ro, bf16=True)
+    check_lse(lse.cpu().numpy().reshape(-1), rl)
 
 
 @pytest.mark.parametrize("name,kw", [
@@ -50,14 +59,65 @@ def test_noalloc_matches_ta_decode_on_two_calls_in_a_row(name, kw):
     S = kw.get("S", synth.WORKLOADS[name].S)
     need = ta.plan_decode(B, Hq, Hkv, S, 128, varlen=name.startswith("varlen")).workspace_bytes
     assert need <= SCRATCH_BYTES
-    first = _inputs(name, **kw)
-    second = _inputs(name, seed=77, **kw)  # different values, same shape
+    x1, first = _inputs(name, **kw)
+    x2, second = _inputs(name, seed=77, **kw)  # different values, same shape
     a = _both(*first)
     b = _both(*second)
-    _compare(*a)
-    _compare(*b)
+    _compare(x1, *a)
+    _compare(x2, *b)
     # the two calls really computed different things from the shared scratch
     assert not torch.equal(a[0], b[0])
+
+
+def test_noalloc_separate_merge_path_over_64_chunks():
+    """A plan with more than 64 chunks (so a separate merge launch reads the
+    partials from, and writes its intermediates into, the fixed scratch): one
+    sequence of 131072 keys passed with its length (the length-agnostic plan
+    over-decomposes), twice in a row."""
+    w = synth.WORKLOADS["gqa_32x8_d128_s131072"]
+    plan = ta.plan_decode(1, 32, 8, w.S, 128, varlen=True)
+    assert plan.n_split > 64 and plan.workspace_bytes <= SCRATCH_BYTES
+    for seed in (None, 78):
+        x = synth.make_inputs(w, seed=seed)
+        x["seqlens"] = torch.tensor([w.S], dtype=torch.int32)
+        q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+        res = _both(q, k, v, x["seqlens"].to(DEV), x["scale"])
+        _compare(x, *res)
+
+
+def test_noalloc_allocates_nothing_after_its_set_up():
+    ta.decode_noalloc_setup()
+    _, args = _inputs("gqa_32x8_d128_s131072", S=20000)
+    q = args[0]
+    out = torch.empty(1, 32, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(1, 32, dtype=torch.float32, device=DEV)
+    ta.decode_noalloc(q, args[1], args[2], out, lse, args[4])  # first call: module and scratch in place
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        ta.decode_noalloc(q, args[1], args[2], out, lse, args[4])
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"device free memory moved by {free0 - free1} bytes"
+    assert ta.decode_noalloc_status() == 0
+
+
+def test_noalloc_reports_device_flags_through_its_own_status_word():
+    _, (q, k, v, sl, scale) = _inputs("varlen_b16_32x8_d128_s1k_32k", S=4096, B=3)
+    out = torch.empty(3, 32, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(3, 32, dtype=torch.float32, device=DEV)
+    bad = torch.tensor([4097, 100, -2], dtype=torch.int32, device=DEV)  # outside [0, S]: clamped
+    ta.decode_noalloc(q, k, v, out, lse, scale, seqlens=bad)
+    assert ta.decode_noalloc_status() & ta.TA_DEVERR_SEQLEN
+    assert ta.decode_noalloc_status() == 0  # read and cleared
+    ok = torch.tensor([4096, 100, 0], dtype=torch.int32, device=DEV)
+    o2 = torch.empty_like(out)
+    l2 = torch.empty_like(lse)
+    ta.decode_noalloc(q, k, v, o2, l2, scale, seqlens=ok)
+    torch.cuda.synchronize()
+    assert ta.decode_noalloc_status() == 0
+    # the clamped lengths are the lengths 4096 and 0
+    assert torch.equal(out, o2) and torch.equal(torch.nan_to_num(lse), torch.nan_to_num(l2))
 
 
 def test_noalloc_rejects_a_shape_beyond_its_scratch():
