@@ -5,7 +5,7 @@ fused causal prefill at S = 16384.
 One step = one pass of the path over one batch of synthetic input:
   1. one decode token (ta_decode_ex): the KV-chunk plan, the split-KV
      partials of every (KV head, chunk) and their log-sum-exp merge -- one
-     launch, since the decode kernel merges up to 64 chunks itself;
+     launch, since the decode kernel merges up to 128 chunks itself;
   2. the causal prefill of the prefill workload (ta_prefill_causal).
 Each phase is a CUDA graph replay bracketed by CUDA events on the stream it
 is launched on.
@@ -274,7 +274,7 @@ def measure_other_configs(ta, synth, accounting, peaks, dev, reps=20):
         gbs = kv_bytes / (us / 1e6) / 1e9
         res[name] = {"workload": f"B={w.B}, Hq={w.Hq}, Hkv={w.Hkv}, D={w.D}, S={w.S}, {w.dtype}",
                      "n_split": plan.n_split, "chunk": plan.chunk,
-                     "launches": 1 if plan.n_split <= 64 else 1 + plan.levels,
+                     "launches": 1 + plan.levels,
                      "kv_bytes": kv_bytes, "us": round(us, 2), "gbs": round(gbs, 1),
                      "frac": round(gbs / peaks["hbm_gbs"], 4)}
         del q, k, v, ws, out, lse, g
@@ -464,8 +464,8 @@ def main():
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
     kv_bytes = accounting.decode_kv_bytes(w.B, w.Hkv, w.D, w.S, 2)
-    # up to 64 chunks the decode kernel merges them itself: one launch
-    decode_launches = 1 if plan.n_split <= 64 else 1 + plan.levels
+    # up to 128 chunks the decode kernel merges them itself: one launch
+    decode_launches = 1 + plan.levels
 
     # ---------------- prefill workload
     do_prefill = not args.no_prefill
@@ -641,7 +641,7 @@ def main():
         "config": {
             "workload": WORKLOAD_DESC,
             "split_kv": {"n_split": plan.n_split, "chunk": plan.chunk, "grid": plan.grid,
-                         "merge": "fused in the decode kernel" if plan.n_split <= 64
+                         "merge": "fused in the decode kernel" if plan.levels == 0
                          else f"{plan.levels} merge launches"},
             "prefill_workload": (f"{PREFILL_WORKLOAD}: B=1, H=32, Hkv=8, D=128, S=16384, causal, bf16"
                                  if do_prefill else "not in this build"),

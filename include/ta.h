@@ -74,9 +74,12 @@ enum {
 
 /*
  * Split-KV plan chosen by the KV-chunk scheduler.  Chunk c of a sequence
- * covers keys [c * chunk, min((c + 1) * chunk, S)).  The merge runs in
- * `levels` launches of fan-in <= `fanin` (0 levels: one chunk, the decode
- * kernel writes the result itself).
+ * covers keys [c * chunk, min((c + 1) * chunk, S)).  The decode kernels hand
+ * out work items in the order chunk 0 of every (sequence, KV head), chunk 1
+ * of every one, and so on.  With up to 128 chunks (and B * Hkv <= 4032) the
+ * decode kernel merges the partials itself; otherwise `levels` merge
+ * launches of fan-in <= `fanin` follow it (levels = 0 when no merge launch
+ * follows).
  */
 typedef struct {
     int32_t n_split;        /* chunks per (sequence, KV head)                */
@@ -112,7 +115,7 @@ typedef struct {
  *     NULL = use the library's own per-device workspace (grown on demand
  *     with cudaMalloc, which synchronises; calls using it on different
  *     streams must not overlap).
- *   With up to 64 chunks (and B * Hkv <= 4032) the decode kernel merges a
+ *   With up to 128 chunks (and B * Hkv <= 4032) the decode kernel merges a
  *   sequence's partials itself (the last CTA to finish a chunk of a
  *   (sequence, KV head) merges them); otherwise a separate tree of merge
  *   launches follows it.

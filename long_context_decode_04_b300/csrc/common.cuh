@@ -146,6 +146,18 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Split-KV work items: item i is chunk i / units of (sequence, KV head)
+// unit i % units, so the device-wide queue hands out every unit's first
+// chunk, then every unit's second chunk, and so on; chunk c covers keys
+// [c * chunk, (c + 1) * chunk) of the unit's list.
+struct ChunkMap {
+    int units, chunk;
+    __device__ __forceinline__ int unit_of(int item) const { return item % units; }
+    __device__ __forceinline__ int split_of(int item) const { return item / units; }
+    __device__ __forceinline__ int start_of(int split) const { return split * chunk; }
+    __device__ __forceinline__ int len_of(int) const { return chunk; }
+};
+
 // 2^x on the special-function unit (PTX ex2.approx, flush-to-zero).
 __device__ __forceinline__ float fast_exp2(float x)
 {

@@ -88,6 +88,7 @@ struct DecodeParams {
     float qscale;  // scale * log2(e)
     const int32_t *seqlens;
     int n_split, chunk, n_items;
+    ChunkMap cm;  // work item -> (unit, chunk) and the chunk's keys
     int mode;
     int32_t *status;    // [0] flags, [16] work-queue counter
     int32_t *counters;  // [B * Hkv] finished chunks per unit (fused mode)
@@ -312,7 +313,7 @@ struct Cfg {
                                    (2 * STAGES + 5) * 8 + STAGES * sizeof(TileDesc) + 16 + 1024;
     static_assert(NCH >= 1 && RB % 128 == 0, "row must be a multiple of 128 bytes");
     static_assert(STAGES >= 2, "need at least two stages");
-    static_assert(kDecodeTileKeys % TILE == 0, "chunks must be whole tiles");
+    static_assert(kDecodeTileKeysCC % TILE == 0, "chunks of the CUDA-core shapes are whole tiles");
     static_assert(DPL % 2 == 0, "lanes own an even number of output dims");
 };
 
@@ -382,10 +383,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
                 w = mbar_wait_bounded(&full[0], 0, abort_flag, p.wait_ns);
             ok = __shfl_sync(kFull, w, 0) != 0;
         }
+        // A CTA's first item is its block index; later ones come from the
+        // device-wide queue, which counts the grabs after the first (the
+        // last grab, item n_items + gridDim.x - 1, resets it).
+        bool first_grab = true;
         while (ok) {
             int item = 0;
             if (leader)
-                item = atomicAdd(&p.status[16], 1);
+                item = first_grab ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&p.status[16], 1);
+            first_grab = false;
             item = __shfl_sync(kFull, item, 0);
             if (item >= p.n_items) {
                 bool w = true;
@@ -404,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
                 }
                 break;
             }
-            const int unit = item / p.n_split;
-            const int split = item - unit * p.n_split;
+            const int unit = p.cm.unit_of(item);
+            const int split = p.cm.split_of(item);
             const int b = unit / p.Hkv;
             int L = p.S;
             if (p.seqlens) {
@@ -426,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
                 n_skip = w0 > r0 ? (w0 - 1 - r0) / p.pi_period + 1 : 0;
                 N = n_skip + (i - w0 + 1);
             }
-            const int c0 = split * p.chunk;
-            const int c1 = min(c0 + p.chunk, N);
+            const int c0 = p.cm.start_of(split);
+            const int c1 = min(c0 + p.cm.len_of(split), N);
             const KV *kbase = static_cast<const KV *>(p.k) + (size_t)unit * kv_head_stride;
             const KV *vbase = static_cast<const KV *>(p.v) + (size_t)unit * kv_head_stride;
             int j0 = c0;
@@ -581,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         if (d.flags & kEnd)
             break;
         if (d.flags & kFirst) {
-            unit = d.item / p.n_split;
-            split = d.item - unit * p.n_split;
+            unit = p.cm.unit_of(d.item);
+            split = p.cm.split_of(d.item);
             b = unit / p.Hkv;
             kvh = unit - b * p.Hkv;
             qs = p.k_scale ? p.qscale * p.k_scale[unit] : p.qscale;
@@ -989,6 +995,7 @@ cudaError_t launch_decode(const DecodeLaunch &a)
     p.seqlens = a.seqlens;
     p.n_split = a.plan.n_split;
     p.chunk = a.plan.chunk;
+    p.cm = ChunkMap{a.B * a.Hkv, a.plan.chunk};
     p.n_items = a.B * a.Hkv * a.plan.n_split;
     if (a.force_partials)
         p.mode = kModePartials;

@@ -9,7 +9,7 @@
 // hyperion-consulting.io, "the rise of FP4" and the COMPUTE layer): K and V
 // are E4M3 codes with one fp32 dequantisation factor per (sequence, KV
 // head) each, q is bf16.  The K factor scales the scores, the V factor the
-// partial.  Same chunks of whole 120-key tiles, same partials.
+// partial.  Same chunks of whole 128-key tiles, same partials.
 //
 // The tensor cores take 16-bit operands, so each tile is widened on chip:
 // E4M3 is a subset of fp16, and cvt.rn.f16x2.e4m3x2 widens two codes
@@ -29,7 +29,7 @@
 // Kernel layout (one persistent CTA per SM, 12 warps):
 //   * warp 0: producer.  Work items (sequence, KV head, chunk) from the
 //     device-wide queue; the item's G query rows widened to fp16 into one of
-//     two Q buffers; raw K and V tiles (120 rows of 128 codes) by TMA into a
+//     two Q buffers; raw K and V tiles (128 rows of 128 codes) by TMA into a
 //     3-stage ring.
 //   * warp 1: TMEM (512 columns: S and O double buffers, three K buffers)
 //     and the score products; warp 2: the value products.
@@ -47,19 +47,20 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "decode_tc_common.cuh"
 #include "tcgen05.cuh"
 
 namespace ta {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kTile = kDecodeTileKeys;  // 120 keys a tile
-constexpr int kRows = 128;              // MMA rows: rows 120-127 are zero / masked
+constexpr int kTile = kDecodeTileKeysTC;  // 128 keys a tile
+constexpr int kRows = 128;                // MMA rows: one key a row
 constexpr int kN = 16;                  // score-product N: the group's heads, zero-padded
 constexpr int kON = 2 * kN;             // value-product N: (warp, head) columns, hi then lo
 constexpr int kRawStages = 3;
 constexpr int kConvBufs = 3;                      // widened tiles (K in TMEM, V in shared memory)
-constexpr int kRawTile = kTile * kD;              // 120 rows of 128 one-byte codes
+constexpr int kRawTile = kTile * kD;              // 128 rows of 128 one-byte codes
 constexpr int kRawStage = 2 * kRawTile;           // K then V
 constexpr int kHalf = kRows * 128;                // one 64-dim half of an fp16 V tile
 constexpr int kVBytes = 2 * kHalf;                // 32 KiB
@@ -85,7 +86,7 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr float kRescaleLog2 = 8.0f;
 
 enum : int { kFirst = 1, kLast = 2, kEnd = 4 };
-enum : int { kModeFinal = 0, kModePartials = 1, kModeFused = 2 };
+constexpr int kModeFinal = tcd::kModeFinal, kModePartials = tcd::kModePartials, kModeFused = tcd::kModeFused;
 
 struct TileDesc {
     int item;
@@ -110,11 +111,9 @@ struct Misc {
     uint64_t mma_done;
     TileDesc desc[kDescRing];        // tile t's descriptor at t % kDescRing
     float alpha[4][4][4];            // [tile % 4][warp][head]
-    float lred[4][4];
-    float mred[4][4];
+    tcd::ItemSmem isum;
     uint32_t tmem_base;
     int abort;
-    int ticket;
 };
 
 constexpr size_t kSmem = (size_t)kMiscOff + sizeof(Misc) + 1024;  // + alignment slack
@@ -123,7 +122,7 @@ static_assert(kRawTile % 1024 == 0 && kRawOff % 1024 == 0, "raw tiles on 1024-by
 static_assert(kTile * 16 % kSoftThreads == 0, "V widening tasks per thread");
 
 struct Fp8Params {
-    CUtensorMap kmap, vmap;  // raw codes (D, S, B*Hkv), box 128 x 120
+    CUtensorMap kmap, vmap;  // raw codes (D, S, B*Hkv), box 128 x 128
     const __nv_bfloat16 *q;
     void *out;
     float *lse;
@@ -131,6 +130,7 @@ struct Fp8Params {
     float qscale;  // scale * log2(e)
     const int32_t *seqlens;
     int n_split, chunk, n_items;
+    ChunkMap cm;  // work item -> (unit, chunk) and the chunk's keys
     int mode;
     int32_t *status;
     int32_t *counters;
@@ -140,8 +140,6 @@ struct Fp8Params {
     const float *k_scale, *v_scale;  // per (sequence, KV head), or nullptr (1)
 };
 
-__device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
-__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
 // Two E4M3 codes (low byte first) to a packed fp16 pair (exact).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
@@ -169,13 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Zero what no widening or query write covers: rows 120-127 of the fp16 V
-    // tiles, the Q operands (rows G..15) and the P operands.
+    // Zero what no widening or query write covers: the Q operands (rows
+    // G..15) and the P operands.
     const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = threadIdx.x; i < kConvBufs * 2 * 8 * 8; i += kThreads) {
-        const int c = i & 7, r = kTile + ((i >> 3) & 7), hh = (i >> 6) & 1, b = i >> 7;
-        *reinterpret_cast<uint4 *>(smem + kVOff + b * kVBytes + hh * kHalf + r * 128 + c * 16) = z4;
-    }
     for (int i = threadIdx.x; i < (kRawOff - kQOff) / 16; i += kThreads)
         *reinterpret_cast<uint4 *>(smem + kQOff + i * 16) = z4;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -202,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
         mbar_init(&ms->grp_bar, 4);
         mbar_init(&ms->mma_done, 2);  // both MMA issuers commit
         ms->abort = 0;
-        ms->ticket = 0;
+        ms->isum.merge_unit = -1;
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -228,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
         // The item's G query rows as fp16 into Q buffer ic % 2: 16-byte chunk c
         // of head h (8 dims) to row h of the operand, 128-byte swizzle.
         auto widen_q = [&](int item) -> bool {
-            const int unit = item / p.n_split;
+            const int unit = p.cm.unit_of(item);
             const int qb = ic & 1;
             int w = 1;
             if (leader && q_uses[qb] > 0)
@@ -265,10 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                 w = mbar_wait_bounded(&ms->raw_full[0], 0, abort_flag, p.wait_ns);
             ok = __shfl_sync(kFull, w, 0) != 0;
         }
+        // A CTA's first item is its block index; later ones come from the
+        // device-wide queue, which counts the grabs after the first (the
+        // last grab, item n_items + gridDim.x - 1, resets it).
+        bool first_grab = true;
         while (ok) {
             int item = 0;
             if (leader)
-                item = atomicAdd(&p.status[16], 1);
+                item = first_grab ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&p.status[16], 1);
+            first_grab = false;
             item = __shfl_sync(kFull, item, 0);
             if (item >= p.n_items) {
                 int w = 1;
@@ -286,8 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                     ++uses[stage];
                 break;
             }
-            const int unit = item / p.n_split;
-            const int split = item - unit * p.n_split;
+            const int unit = p.cm.unit_of(item);
+            const int split = p.cm.split_of(item);
             const int b = unit / p.Hkv;
             int L = p.S;
             if (p.seqlens) {
@@ -298,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                     L = L < 0 ? 0 : p.S;
                 }
             }
-            const int c0 = split * p.chunk;
-            const int c1 = min(c0 + p.chunk, L);
+            const int c0 = p.cm.start_of(split);
+            const int c1 = min(c0 + p.cm.len_of(split), L);
             int j0 = c0, flags = kFirst;
             for (;;) {
                 const int n = max(0, min(kTile, c1 - j0));
@@ -314,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                         ms->desc[ti & (kDescRing - 1)] = TileDesc{item, j0, n, flags};
                         uint64_t *fb = &ms->raw_full[stage];
                         if (n > 0) {
-                            // rows past S read as zero; V rows in [n, 120) are
+                            // rows past S read as zero; V rows in [n, 128) are
                             // written as zero by the converting threads
                             unsigned char *rd = smem + kRawOff + stage * kRawStage;
                             mbar_arrive_expect_tx(fb, kRawTx);
@@ -531,6 +530,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
         float mw[G], l_run[G], o[4][G];
         int unit = 0, split = 0, b = 0, kvh = 0;
         float qs = p.qscale;
+        const tcd::ItemOut io{p.out, p.lse, p.Hq, p.mode, p.n_split, p.part_m, p.part_l, p.part_o, p.counters};
+        float *const stage_area = ms->isum.stage;
+        tcd::PendingTicket pt;
+        bool ended = false;
         auto group_sync = [&]() -> bool {
             __syncwarp();
             if (lane == 0)
@@ -565,11 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
             if (!__all_sync(kFull, w))
                 break;
             const TileDesc d = ms->desc[t & (kDescRing - 1)];
-            if (d.flags & kEnd)
+            if (d.flags & kEnd) {
+                ended = true;
                 break;
+            }
             if (d.flags & kFirst) {
-                unit = d.item / p.n_split;
-                split = d.item - unit * p.n_split;
+                unit = p.cm.unit_of(d.item);
+                split = p.cm.split_of(d.item);
                 b = unit / p.Hkv;
                 kvh = unit - b * p.Hkv;
                 qs = p.k_scale ? p.qscale * p.k_scale[unit] : p.qscale;
@@ -653,119 +658,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
             if (!accumulate(tt))
                 break;
 
-            // ---- end of item: merge the four warps' states
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float v = l_run[g];
-#pragma unroll
-                for (int mask = 16; mask >= 1; mask >>= 1)
-                    v += __shfl_xor_sync(kFull, v, mask);
-                if (lane == g) {
-                    ms->lred[q4][g] = v;
-                    ms->mred[q4][g] = mw[g];
-                }
-            }
-            if (!group_sync())
+            // ---- end of item: the partial, the result, and in fused mode the merge
+            if (!tcd::finish_item<G, OUT>(io, &ms->isum, stage_area, q4, lane, unit, split, b, kvh, p.v_scale ? p.v_scale[unit] : 1.f, mw, l_run,
+                                          o, pt, group_sync))
                 break;
-            const float vs = p.v_scale ? p.v_scale[unit] : 1.f;  // value dequantisation factor
-            float ls[G], mt[G], of[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                mt[g] = fmax3(ms->mred[0][g], ms->mred[1][g], fmaxf(ms->mred[2][g], ms->mred[3][g]));
-                ls[g] = 0.f;
-                of[g] = 0.f;
-#pragma unroll
-                for (int w2 = 0; w2 < 4; ++w2) {
-                    const float m2 = ms->mred[w2][g];
-                    const float be = m2 == -INFINITY ? 0.f : fast_exp2(m2 - mt[g]);
-                    ls[g] = fmaf(ms->lred[w2][g], be, ls[g]);
-                    of[g] = fmaf(o[w2][g], be, of[g]);
-                }
-                of[g] *= vs;
-            }
-            const size_t row0 = (size_t)b * p.Hq + (size_t)kvh * G;
-            if (p.mode == kModeFinal) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float inv = ls[g] > 0.f ? 1.0f / ls[g] : 0.f;
-                    store_out(static_cast<OUT *>(p.out) + (row0 + g) * kD + row, of[g] * inv);
-                    if (row == g && p.lse)
-                        p.lse[row0 + g] = ls[g] > 0.f ? (mt[g] + fast_log2(ls[g])) * kLn2 : -INFINITY;
-                }
-                continue;
-            }
-            const int ns = p.n_split;
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const size_t pi = (row0 + g) * ns + split;
-                p.part_o[pi * kD + row] = of[g];
-                if (row == g) {
-                    p.part_m[pi] = mt[g] == -INFINITY ? -INFINITY : mt[g] * kLn2;
-                    p.part_l[pi] = ls[g];
-                }
-            }
-            if (p.mode != kModeFused)
-                continue;
-
-            // ---- fused merge: the CTA that writes a unit's last partial merges it
-            if (!group_sync())
-                break;
-            if (row == 0) {
-                int last = 0;
-                if (atomic_add_acq_rel_gpu(&p.counters[unit], 1) == ns - 1) {
-                    last = 1;
-                    p.counters[unit] = 0;  // ready for the next launch
-                }
-                *reinterpret_cast<volatile int *>(&ms->ticket) = last;
-            }
-            if (!group_sync())
-                break;
-            if (!*reinterpret_cast<volatile int *>(&ms->ticket))
-                continue;
-            for (int idx = row; idx < G * kD / 4; idx += kSoftThreads) {
-                const int h = idx / (kD / 4);
-                const int d4 = (idx - h * (kD / 4)) * 4;
-                const size_t pr = (row0 + h) * ns;
-                const float4 *po = reinterpret_cast<const float4 *>(p.part_o + pr * kD + d4);
-                float mx2 = -INFINITY, lsum = 0.f;
-                float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int n0 = 0; n0 < ns; n0 += 8) {
-                    float mb[8], lb[8];
-                    float4 ob[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        mb[i] = -INFINITY;
-                        if (n0 + i < ns) {
-                            mb[i] = __ldcg(p.part_m + pr + n0 + i);
-                            lb[i] = __ldcg(p.part_l + pr + n0 + i);
-                            ob[i] = __ldcg(po + (size_t)(n0 + i) * (kD / 4));
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (mb[i] != -INFINITY) {
-                            const float mn = fmaxf(mx2, mb[i]);
-                            const float sc = fast_exp2((mx2 - mn) * kLog2e);
-                            const float a = fast_exp2((mb[i] - mn) * kLog2e);
-                            lsum = fmaf(lsum, sc, a * lb[i]);
-                            os.x = fmaf(os.x, sc, a * ob[i].x);
-                            os.y = fmaf(os.y, sc, a * ob[i].y);
-                            os.z = fmaf(os.z, sc, a * ob[i].z);
-                            os.w = fmaf(os.w, sc, a * ob[i].w);
-                            mx2 = mn;
-                        }
-                    }
-                }
-                const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
-                OUT *dst = static_cast<OUT *>(p.out) + (row0 + h) * kD + d4;
-                store_out(dst + 0, os.x * inv);
-                store_out(dst + 1, os.y * inv);
-                store_out(dst + 2, os.z * inv);
-                store_out(dst + 3, os.w * inv);
-                if (d4 == 0 && p.lse)
-                    p.lse[row0 + h] = lsum > 0.f ? mx2 + fast_log2(lsum) * kLn2 : -INFINITY;
-            }
         }
+        if (ended)
+            tcd::finish_pending<G, OUT>(io, &ms->isum, stage_area, q4, lane, pt, group_sync);
     }
 
     tc::fence_before_sync();
@@ -812,6 +711,7 @@ cudaError_t launch_decode_fp8_tc(const DecodeLaunch &a)
     p.seqlens = a.seqlens;
     p.n_split = a.plan.n_split;
     p.chunk = a.plan.chunk;
+    p.cm = ChunkMap{a.B * a.Hkv, a.plan.chunk};
     p.n_items = a.B * a.Hkv * a.plan.n_split;
     if (a.force_partials)
         p.mode = kModePartials;
@@ -828,7 +728,7 @@ cudaError_t launch_decode_fp8_tc(const DecodeLaunch &a)
     p.part_o = a.part_o;
     p.k_scale = a.k_scale;
     p.v_scale = a.v_scale;
-    // K, V codes [B, Hkv, S, D] as (D, S, B*Hkv), one byte each, box 128 x 120,
+    // K, V codes [B, Hkv, S, D] as (D, S, B*Hkv), one byte each, box 128 x 128,
     // 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r % 8))
     const uint64_t units = (uint64_t)a.B * a.Hkv;
     const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.S, units};

@@ -7,8 +7,8 @@
 // attention, "basic concepts and operating principle"), one partial
 // (m, l, o) per KV chunk and the log-sum-exp merge of a sequence's
 // partials (Tree Attention explainer, aibr.jp/archives/143699, sections 1
-// and 3).  The chunks are the same whole 120-key tiles, so the plan and the
-// partials' layout do not depend on which of the two kernels runs.
+// and 3).  Chunks are whole 128-key tiles (the MMA's M); the partials'
+// layout is the one every decode kernel writes.
 //
 // Why tensor cores in a bandwidth-bound step.  The G query heads of a KV
 // head (grouped-query attention) share its keys, so per KV head the scores
@@ -21,8 +21,7 @@
 // instructions of softmax, so the issue slots no longer bound the kernel:
 // how long a ring stage is held between its copy and its value product does.
 //
-// Per 120-key tile (M = 128 rows; rows 120-127 of every staged tile are
-// zero and masked):
+// Per 128-key tile (M = 128 rows, one key row per TMEM lane):
 //   S^T [128 keys x 16] = K [128 x D] . Q^T [D x 16]     (A = K, K-major;
 //                                                        B = Q, heads padded to 16)
 //   O_t^T [D x 32]      = V^T [D x 128] . P^T [128 x 32] (A = V, MN-major;
@@ -37,7 +36,7 @@
 //   * warp 0: producer.  Takes work items (sequence, KV head, chunk) from
 //     the device-wide queue, loads the item's G query rows (TMA, 128-byte
 //     swizzle) into one of two Q buffers and the chunk's K/V tiles into a
-//     3-stage ring (TMA boxes of 120 rows x 64 dims; boxes of 8 rows at a
+//     3-stage ring (TMA boxes of 128 rows x 64 dims; boxes of 8 rows at a
 //     pi-Attention sequence's boundary between periodic and window keys).
 //   * warp 1: allocates 128 TMEM columns (S double buffer, O double
 //     buffer) and issues the score products; warp 2 issues the value
@@ -59,14 +58,15 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "decode_tc_common.cuh"
 #include "tcgen05.cuh"
 
 namespace ta {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kTile = kDecodeTileKeys;  // 120 keys a tile
-constexpr int kRows = 128;              // MMA rows: staged rows 120-127 stay zero
+constexpr int kTile = kDecodeTileKeysTC;  // 128 keys a tile
+constexpr int kRows = 128;                // MMA rows: one key a row
 constexpr int kN = 16;                  // MMA N: the group's heads, zero-padded
 constexpr int kStages = 3;
 constexpr int kHalf = kRows * 128;          // one 64-dim half of a staged K or V tile
@@ -90,7 +90,7 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr float kRescaleLog2 = 8.0f;
 
 enum : int { kFirst = 1, kLast = 2, kEnd = 4 };
-enum : int { kModeFinal = 0, kModePartials = 1, kModeFused = 2 };
+constexpr int kModeFinal = tcd::kModeFinal, kModePartials = tcd::kModePartials, kModeFused = tcd::kModeFused;
 
 struct TileDesc {
     int item;
@@ -114,11 +114,9 @@ struct Misc {
     uint64_t mma_done;
     TileDesc desc[kStages];
     float alpha[4][4][4];        // [tile % 4][warp][head] factor by which a warp's maximum rose
-    float lred[4][4];            // [warp][head] weight sums at the item end
-    float mred[4][4];            // [warp][head] running maxima at the item end
+    tcd::ItemSmem isum;          // the item end's sums, maxima and ticket
     uint32_t tmem_base;
     int abort;
-    int ticket;
 };
 
 constexpr size_t kSmem = (size_t)kMiscOff + sizeof(Misc) + 1024;  // + alignment slack
@@ -126,8 +124,8 @@ static_assert(kSmem <= 232448, "shared memory per CTA");
 static_assert(kTile <= kRows && kTile % 8 == 0, "tile rows");
 
 struct TcParams {
-    // q rows (box 64 x G); K/V tiles of 120 rows and groups of 8 rows;
-    // pi-Attention periodic keys as rows (tiles of 120 and groups of 8)
+    // q rows (box 64 x G); K/V tiles of 128 rows and groups of 8 rows;
+    // pi-Attention periodic keys as rows (tiles of 128 and groups of 8)
     CUtensorMap qmap, kmap, vmap, k8map, v8map, kpimap, vpimap, kpi8map, vpi8map;
     const void *k, *v;
     void *out;
@@ -136,6 +134,7 @@ struct TcParams {
     float qscale;  // scale * log2(e)
     const int32_t *seqlens;
     int n_split, chunk, n_items;
+    ChunkMap cm;  // work item -> (unit, chunk) and the chunk's keys
     int mode;
     int32_t *status;    // [0] flags, [16] work-queue counter
     int32_t *counters;  // [B * Hkv] finished chunks per unit (fused mode)
@@ -146,10 +145,15 @@ struct TcParams {
     // the window [max(0, i - pi_window), i] and the keys i - m * pi_period
     // (m >= 1) before it; the chunks cut the ascending list of those keys.
     int pi_window, pi_period;
+    // Paged cache (block_table != nullptr): k, v are page pools [num_pages,
+    // Hkv, page_size, D] seen as (D, page_size, num_pages * Hkv) with boxes
+    // of pg_rows = min(page_size, 128) rows; page_size divides 128 or is a
+    // multiple of it, so a 128-key tile is whole pages or part of one.
+    const int32_t *block_table;
+    int page_size, pages_per_seq, num_pages, pg_rows;
+    CUtensorMap kpgmap, vpgmap;
 };
 
-__device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
-__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
 template <int G, typename OUT>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ TcParams p)
@@ -162,13 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Zero what no copy writes: rows 120-127 of every staged half, the Q
-    // buffers (rows G..15 stay zero) and the P buffers.
+    // Zero what no copy writes: the Q buffers (rows G..15 stay zero) and the
+    // P buffers.  (Staged rows past a tile's keys are masked and their V
+    // rows zeroed per tile by the softmax threads.)
     const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = threadIdx.x; i < kStages * 4 * 8 * 8; i += kThreads) {
-        const int c = i & 7, r = kTile + ((i >> 3) & 7), hh = (i >> 6) & 3, s = i >> 8;
-        *reinterpret_cast<uint4 *>(smem + s * kStageBytes + hh * kHalf + r * 128 + c * 16) = z4;
-    }
     for (int i = threadIdx.x; i < (kMiscOff - kQOff) / 16; i += kThreads)
         *reinterpret_cast<uint4 *>(smem + kQOff + i * 16) = z4;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         mbar_init(&ms->grp_bar, 4);
         mbar_init(&ms->mma_done, 2);  // both MMA issuers commit
         ms->abort = 0;
-        ms->ticket = 0;
+        ms->isum.merge_unit = -1;
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -207,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         // ------------------------------------------------------------ producer
         // Lane 0 takes the decisions (work queue, ring waits, expected
         // bytes, descriptors); the 32 lanes share the copies of a tile.  A
-        // tile is one TMA box of 120 rows when its keys are contiguous in
-        // memory, else 15 groups of 8 rows: a box of 8 rows for a group whose
+        // tile is one TMA box of 128 rows when its keys are contiguous in
+        // memory, else 16 groups of 8 rows: a box of 8 rows for a group whose
         // keys are contiguous (all periodic or all window keys), plain loads
         // and swizzled stores for the one group that straddles the two.  The full barrier
         // takes two arrivals from lane 0, with the expected TMA bytes before
@@ -216,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         const bool leader = lane == 0;
         if (leader) {
             tc::prefetch_tensormap(&p.qmap);
-            tc::prefetch_tensormap(&p.kmap);
-            tc::prefetch_tensormap(&p.vmap);
+            tc::prefetch_tensormap(p.block_table ? &p.kpgmap : &p.kmap);
+            tc::prefetch_tensormap(p.block_table ? &p.vpgmap : &p.vmap);
         }
         const uint64_t policy = l2_policy_evict_first();
         const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.k);
@@ -235,10 +236,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 w = mbar_wait_bounded(&ms->full[0], 0, abort_flag, p.wait_ns);
             ok = __shfl_sync(kFull, w, 0) != 0;
         }
+        // A CTA's first item is its block index; later ones come from the
+        // device-wide queue, which counts the grabs after the first (the
+        // last grab, item n_items + gridDim.x - 1, resets it).
+        bool first_grab = true;
         while (ok) {
             int item = 0;
             if (leader)
-                item = atomicAdd(&p.status[16], 1);
+                item = first_grab ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&p.status[16], 1);
+            first_grab = false;
             item = __shfl_sync(kFull, item, 0);
             if (item >= p.n_items) {
                 int w = 1;
@@ -257,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     ++uses[stage];
                 break;
             }
-            const int unit = item / p.n_split;
-            const int split = item - unit * p.n_split;
+            const int unit = p.cm.unit_of(item);
+            const int split = p.cm.split_of(item);
             const int b = unit / p.Hkv;
             int L = p.S;
             if (p.seqlens) {
@@ -279,8 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 n_skip = w0 > r0 ? (w0 - 1 - r0) / p.pi_period + 1 : 0;
                 N = n_skip + (i - w0 + 1);
             }
-            const int c0 = split * p.chunk;
-            const int c1 = min(c0 + p.chunk, N);
+            const int c0 = p.cm.start_of(split);
+            const int c1 = min(c0 + p.cm.len_of(split), N);
             // element offset of the K/V row of list position pos
             auto row_of = [&](int pos) -> size_t {
                 const int key = pos < n_skip ? r0 + pos * p.pi_period : w0 + (pos - n_skip);
@@ -309,12 +315,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 const bool last = j0 + n >= c1;
                 if (last)
                     flags |= kLast;
-                // whole-tile boxes: contiguous keys (y = ya of kmap), or 120
+                // whole-tile boxes: contiguous keys (y = ya of kmap), or 128
                 // periodic keys (y = j0 of kpimap)
-                const bool whole = n > 0 && (p.pi_period == 0 || j0 >= n_skip);
-                const bool whole_pi = n > 0 && p.pi_period > 0 && j0 + kTile <= n_skip;
+                const bool paged = p.block_table != nullptr;
+                const bool whole = !paged && n > 0 && (p.pi_period == 0 || j0 >= n_skip);
+                const bool whole_pi = !paged && n > 0 && p.pi_period > 0 && j0 + kTile <= n_skip;
                 const int ya = p.pi_period > 0 ? w0 + (j0 - n_skip) : j0;
-                const int ng = (whole || whole_pi) ? 0 : (n + 7) >> 3;  // groups of 8 rows
+                const int ng = (whole || whole_pi || paged) ? 0 : (n + 7) >> 3;  // groups of 8 rows
+                // paged cache: piece t (lane t) is rows [t * pg_rows, (t + 1) *
+                // pg_rows) of the tile, all in one page (pg_rows = min(page
+                // size, 128), and tiles start on page boundaries or inside
+                // one page), one box of pg_rows rows from the page pool
+                bool pg = false;
+                int pg_y = 0, pg_z = 0;
+                if (paged && lane * p.pg_rows < n) {
+                    const int key = j0 + lane * p.pg_rows;
+                    const int pid = p.block_table[(size_t)b * p.pages_per_seq + key / p.page_size];
+                    if (pid >= 0 && pid < p.num_pages) {
+                        pg = true;
+                        pg_y = key % p.page_size;
+                        pg_z = pid * p.Hkv + (unit - b * p.Hkv);
+                    } else {
+                        atomicOr(&p.status[0], TA_DEVERR_PAGE);  // not followed; output undefined
+                    }
+                }
+                const unsigned pg_mask = __ballot_sync(kFull, pg);
                 bool g8 = false;
                 const CUtensorMap *gk = &p.k8map, *gv = &p.v8map;
                 int gx = 0, gy = 0;
@@ -333,7 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 }
                 const unsigned g8_mask = __ballot_sync(kFull, g8);
                 const unsigned man_mask = __ballot_sync(kFull, lane < ng && !g8);
-                const uint32_t bytes = (whole || whole_pi) ? kTxBytes : (uint32_t)__popc(g8_mask) * 4096u;
+                const uint32_t bytes = (whole || whole_pi) ? kTxBytes
+                                       : paged ? (uint32_t)__popc(pg_mask) * 4u * (uint32_t)p.pg_rows * 128u
+                                               : (uint32_t)__popc(g8_mask) * 4096u;
                 w = 1;
                 if (leader) {
                     if (uses[stage] > 0)
@@ -354,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 unsigned char *vd = kd + kTileBytes;
                 uint64_t *fb = &ms->full[stage];
                 if (leader && (whole || whole_pi)) {
-                    // rows past S read as zero; rows in [n, 120) are zeroed by
+                    // rows past S read as zero; rows in [n, 128) are zeroed by
                     // the softmax threads before the value product
                     const CUtensorMap *mk = whole ? &p.kmap : &p.kpimap;
                     const CUtensorMap *mv = whole ? &p.vmap : &p.vpimap;
@@ -363,6 +390,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     tc::tma_load_3d_hint(kd + kHalf, mk, x0 + 64, y, unit, fb, policy);
                     tc::tma_load_3d_hint(vd, mv, x0, y, unit, fb, policy);
                     tc::tma_load_3d_hint(vd + kHalf, mv, x0 + 64, y, unit, fb, policy);
+                }
+                if (pg) {
+                    const int r = lane * p.pg_rows * 128;
+                    tc::tma_load_3d_hint(kd + r, &p.kpgmap, 0, pg_y, pg_z, fb, policy);
+                    tc::tma_load_3d_hint(kd + kHalf + r, &p.kpgmap, 64, pg_y, pg_z, fb, policy);
+                    tc::tma_load_3d_hint(vd + r, &p.vpgmap, 0, pg_y, pg_z, fb, policy);
+                    tc::tma_load_3d_hint(vd + kHalf + r, &p.vpgmap, 64, pg_y, pg_z, fb, policy);
                 }
                 if (g8) {
                     const int r = 8 * lane * 128;
@@ -531,6 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         int t = 0;
         float mw[G], l_run[G], o[4][G];
         int unit = 0, split = 0, b = 0, kvh = 0;
+        const tcd::ItemOut io{p.out, p.lse, p.Hq, p.mode, p.n_split, p.part_m, p.part_l, p.part_o, p.counters};
+        float *const stage_area = ms->isum.stage;
+        tcd::PendingTicket pt;
+        bool ended = false;
         auto group_sync = [&]() -> bool {
             __syncwarp();
             if (lane == 0)
@@ -567,11 +605,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             if (!__all_sync(kFull, w))
                 break;
             const TileDesc d = ms->desc[stage];
-            if (d.flags & kEnd)
+            if (d.flags & kEnd) {
+                ended = true;
                 break;
+            }
             if (d.flags & kFirst) {
-                unit = d.item / p.n_split;
-                split = d.item - unit * p.n_split;
+                unit = p.cm.unit_of(d.item);
+                split = p.cm.split_of(d.item);
                 b = unit / p.Hkv;
                 kvh = unit - b * p.Hkv;
 #pragma unroll
@@ -670,122 +710,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             if (!accumulate(tt))
                 break;
 
-            // ---- end of item: merge the four warps' states
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float v = l_run[g];
-#pragma unroll
-                for (int mask = 16; mask >= 1; mask >>= 1)
-                    v += __shfl_xor_sync(kFull, v, mask);
-                if (lane == g) {
-                    ms->lred[q4][g] = v;
-                    ms->mred[q4][g] = mw[g];
-                }
-            }
-            if (!group_sync())
+            // ---- end of item: the partial, the result, and in fused mode the merge
+            if (!tcd::finish_item<G, OUT>(io, &ms->isum, stage_area, q4, lane, unit, split, b, kvh, 1.f, mw, l_run,
+                                          o, pt, group_sync))
                 break;
-            float ls[G], mt[G], of[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                mt[g] = fmax3(ms->mred[0][g], ms->mred[1][g], fmaxf(ms->mred[2][g], ms->mred[3][g]));
-                ls[g] = 0.f;
-                of[g] = 0.f;
-#pragma unroll
-                for (int w2 = 0; w2 < 4; ++w2) {
-                    const float m2 = ms->mred[w2][g];
-                    const float be = m2 == -INFINITY ? 0.f : fast_exp2(m2 - mt[g]);
-                    ls[g] = fmaf(ms->lred[w2][g], be, ls[g]);
-                    of[g] = fmaf(o[w2][g], be, of[g]);
-                }
-            }
-            const size_t row0 = (size_t)b * p.Hq + (size_t)kvh * G;
-            if (p.mode == kModeFinal) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float inv = ls[g] > 0.f ? 1.0f / ls[g] : 0.f;
-                    store_out(static_cast<OUT *>(p.out) + (row0 + g) * kD + row, of[g] * inv);
-                    if (row == g && p.lse)
-                        p.lse[row0 + g] = ls[g] > 0.f ? (mt[g] + fast_log2(ls[g])) * kLn2 : -INFINITY;
-                }
-                continue;
-            }
-            const int ns = p.n_split;
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const size_t pi = (row0 + g) * ns + split;
-                p.part_o[pi * kD + row] = of[g];
-                if (row == g) {
-                    p.part_m[pi] = mt[g] == -INFINITY ? -INFINITY : mt[g] * kLn2;
-                    p.part_l[pi] = ls[g];
-                }
-            }
-            if (p.mode != kModeFused)
-                continue;
-
-            // ---- fused merge: the CTA that writes a unit's last partial merges it.
-            // The rendezvous orders the warpgroup's partial stores before
-            // thread 0's GPU-scope acquire-release ticket, which publishes
-            // them to the merging CTA (and, for that CTA, acquires the others').
-            if (!group_sync())
-                break;
-            if (row == 0) {
-                int last = 0;
-                if (atomic_add_acq_rel_gpu(&p.counters[unit], 1) == ns - 1) {
-                    last = 1;
-                    p.counters[unit] = 0;  // ready for the next launch
-                }
-                *reinterpret_cast<volatile int *>(&ms->ticket) = last;
-            }
-            if (!group_sync())
-                break;
-            if (!*reinterpret_cast<volatile int *>(&ms->ticket))
-                continue;
-            // Thread (h, d4) folds head h's ns partials in order with a running
-            // maximum (log-sum-exp rule, natural-log m), loading 16 at a time.
-            for (int idx = row; idx < G * kD / 4; idx += kSoftThreads) {
-                const int h = idx / (kD / 4);
-                const int d4 = (idx - h * (kD / 4)) * 4;
-                const size_t pr = (row0 + h) * ns;
-                const float4 *po = reinterpret_cast<const float4 *>(p.part_o + pr * kD + d4);
-                float mx2 = -INFINITY, lsum = 0.f;
-                float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int n0 = 0; n0 < ns; n0 += 16) {
-                    float mb[16], lb[16];
-                    float4 ob[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        mb[i] = -INFINITY;
-                        if (n0 + i < ns) {
-                            mb[i] = __ldcg(p.part_m + pr + n0 + i);
-                            lb[i] = __ldcg(p.part_l + pr + n0 + i);
-                            ob[i] = __ldcg(po + (size_t)(n0 + i) * (kD / 4));
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        if (mb[i] != -INFINITY) {
-                            const float mn = fmaxf(mx2, mb[i]);
-                            const float sc = fast_exp2((mx2 - mn) * kLog2e);
-                            const float a = fast_exp2((mb[i] - mn) * kLog2e);
-                            lsum = fmaf(lsum, sc, a * lb[i]);
-                            os.x = fmaf(os.x, sc, a * ob[i].x);
-                            os.y = fmaf(os.y, sc, a * ob[i].y);
-                            os.z = fmaf(os.z, sc, a * ob[i].z);
-                            os.w = fmaf(os.w, sc, a * ob[i].w);
-                            mx2 = mn;
-                        }
-                    }
-                }
-                const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
-                OUT *dst = static_cast<OUT *>(p.out) + (row0 + h) * kD + d4;
-                store_out(dst + 0, os.x * inv);
-                store_out(dst + 1, os.y * inv);
-                store_out(dst + 2, os.z * inv);
-                store_out(dst + 3, os.w * inv);
-                if (d4 == 0 && p.lse)
-                    p.lse[row0 + h] = lsum > 0.f ? mx2 + fast_log2(lsum) * kLn2 : -INFINITY;
-            }
         }
+        if (ended)
+            tcd::finish_pending<G, OUT>(io, &ms->isum, stage_area, q4, lane, pt, group_sync);
     }
 
     tc::fence_before_sync();
@@ -814,9 +745,14 @@ cudaError_t launch_typed(const DecodeLaunch &a, const TcParams &p)
 bool decode_tc_eligible(const DecodeLaunch &a)
 {
     const int G = a.Hq / a.Hkv;
-    // (a paged cache stays on the CUDA-core kernel: its 120-key tiles cut
-    // pages into pieces that would each need a TMA box of their own)
-    return a.D == kD && (G == 2 || G == 4) && a.in_dtype == TA_BF16 && !a.kv_fp8 && !a.block_table;
+    // a paged cache whose pages tile the 128-key tiles (page sizes 8, 16, 32,
+    // 64 or multiples of 128: one TMA box per page piece, on the 128-byte
+    // swizzle's 8-row grid); other page sizes go to the CUDA-core kernel
+    // (and tiles that start on a multiple of 128 keys: chunks of whole tiles)
+    const bool tiles_aligned = a.plan.n_split == 1 || a.plan.chunk % kTile == 0;
+    const bool pages_ok = !a.block_table || (tiles_aligned && ((a.page_size % 128 == 0) ||
+                          (a.page_size >= 8 && a.page_size <= 64 && 128 % a.page_size == 0)));
+    return a.D == kD && (G == 2 || G == 4) && a.in_dtype == TA_BF16 && !a.kv_fp8 && pages_ok;
 }
 
 cudaError_t launch_decode_tc(const DecodeLaunch &a)
@@ -833,6 +769,7 @@ cudaError_t launch_decode_tc(const DecodeLaunch &a)
     p.seqlens = a.seqlens;
     p.n_split = a.plan.n_split;
     p.chunk = a.plan.chunk;
+    p.cm = ChunkMap{a.B * a.Hkv, a.plan.chunk};
     p.n_items = a.B * a.Hkv * a.plan.n_split;
     if (a.force_partials)
         p.mode = kModePartials;
@@ -853,7 +790,7 @@ cudaError_t launch_decode_tc(const DecodeLaunch &a)
     p.pi_period = a.pi_period;
     // Tensor maps, boxes of 64 dims (128 bytes, the swizzle span):
     //   q [B, Hq, D] as (D, G, B*Hkv), box G rows;
-    //   K, V [B, Hkv, S, D] as (D, S, B*Hkv), boxes of 120 and 8 rows;
+    //   K, V [B, Hkv, S, D] as (D, S, B*Hkv), boxes of 128 and 8 rows;
     //   pi-Attention: each (sequence, KV head) as rows of pi_period keys,
     //     (pi*D, ceil(S/pi), B*Hkv): the box at x = r*D, y = m holds keys
     //     r + (m + t) * pi; it is only used where all its rows are keys of
@@ -862,22 +799,39 @@ cudaError_t launch_decode_tc(const DecodeLaunch &a)
     const uint64_t qd[3] = {(uint64_t)kD, (uint64_t)G, units};
     const uint64_t qs[2] = {(uint64_t)kD * 2, (uint64_t)G * kD * 2};
     const uint32_t qbox[3] = {64, (uint32_t)G, 1};
-    const uint32_t box120[3] = {64, (uint32_t)kTile, 1};
+    const uint32_t boxt[3] = {64, (uint32_t)kTile, 1};
     const uint32_t box8[3] = {64, 8, 1};
     const uint64_t kd[3] = {(uint64_t)kD, (uint64_t)a.S, units};
     const uint64_t ks[2] = {(uint64_t)kD * 2, (uint64_t)a.S * kD * 2};
-    bool ok = encode_tmap_3d(&p.qmap, a.q, true, qd, qs, qbox, true) &&
-              encode_tmap_3d(&p.kmap, a.k, true, kd, ks, box120, true) &&
-              encode_tmap_3d(&p.vmap, a.v, true, kd, ks, box120, true) &&
-              encode_tmap_3d(&p.k8map, a.k, true, kd, ks, box8, true) &&
-              encode_tmap_3d(&p.v8map, a.v, true, kd, ks, box8, true);
-    p.kpimap = p.vpimap = p.kpi8map = p.vpi8map = p.qmap;  // unused without pi-Attention
+    bool ok = encode_tmap_3d(&p.qmap, a.q, true, qd, qs, qbox, true);
+    // maps a launch does not use are copies of the q map (never read)
+    p.kmap = p.vmap = p.k8map = p.v8map = p.qmap;
+    p.kpimap = p.vpimap = p.kpi8map = p.vpi8map = p.qmap;
+    p.kpgmap = p.vpgmap = p.qmap;
+    p.block_table = a.block_table;
+    p.page_size = a.page_size;
+    p.pages_per_seq = a.pages_per_seq;
+    p.num_pages = a.num_pages;
+    p.pg_rows = a.page_size < kTile ? a.page_size : kTile;
+    if (a.block_table) {
+        // page pools [num_pages, Hkv, page_size, D] as (D, page_size, num_pages * Hkv)
+        const uint64_t gd[3] = {(uint64_t)kD, (uint64_t)a.page_size, (uint64_t)a.num_pages * a.Hkv};
+        const uint64_t gs[2] = {(uint64_t)kD * 2, (uint64_t)a.page_size * kD * 2};
+        const uint32_t gbox[3] = {64, (uint32_t)p.pg_rows, 1};
+        ok = ok && encode_tmap_3d(&p.kpgmap, a.k, true, gd, gs, gbox, true) &&
+             encode_tmap_3d(&p.vpgmap, a.v, true, gd, gs, gbox, true);
+    } else {
+        ok = ok && encode_tmap_3d(&p.kmap, a.k, true, kd, ks, boxt, true) &&
+             encode_tmap_3d(&p.vmap, a.v, true, kd, ks, boxt, true) &&
+             encode_tmap_3d(&p.k8map, a.k, true, kd, ks, box8, true) &&
+             encode_tmap_3d(&p.v8map, a.v, true, kd, ks, box8, true);
+    }
     if (a.pi_period > 0) {
         const uint64_t per = (uint64_t)a.pi_period;
         const uint64_t pd[3] = {per * kD, ((uint64_t)a.S + per - 1) / per, units};
         const uint64_t ps[2] = {per * kD * 2, (uint64_t)a.S * kD * 2};
-        ok = ok && encode_tmap_3d(&p.kpimap, a.k, true, pd, ps, box120, true) &&
-             encode_tmap_3d(&p.vpimap, a.v, true, pd, ps, box120, true) &&
+        ok = ok && encode_tmap_3d(&p.kpimap, a.k, true, pd, ps, boxt, true) &&
+             encode_tmap_3d(&p.vpimap, a.v, true, pd, ps, boxt, true) &&
              encode_tmap_3d(&p.kpi8map, a.k, true, pd, ps, box8, true) &&
              encode_tmap_3d(&p.vpi8map, a.v, true, pd, ps, box8, true);
     }

@@ -1,0 +1,267 @@
+// decode_tc_common.cuh -- the end of a work item, shared by the two
+// tensor-core decodes (decode_tc.cu: bf16 cache; decode_fp8_tc.cu: E4M3
+// cache).
+//
+// Both kernels run a warpgroup of four softmax warps; warp w keeps, for
+// each of the G query heads of the item's KV head, its own running
+// reference mw (log2 units), weight sum l_run and, per thread (output
+// dimension `row`), the four warps' unnormalised outputs o[w][g].  At the
+// end of an item these are merged by the log-sum-exp rule (Tree Attention
+// explainer, aibr.jp/archives/143699, sections 1 and 3: the reduction along
+// the sequence axis is associative) into the item's partial (m, l, o), which
+// is either the result (one chunk), or written to the partials, and in
+// fused mode the CTA that writes a unit's last partial merges all of them
+// (learning that it is the last one item later, so no item waits for it).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ta {
+namespace tcd {
+
+constexpr int kD = 128;
+constexpr int kSoftThreads = 128;
+constexpr unsigned kFull = 0xffffffffu;
+
+enum : int { kModeFinal = 0, kModePartials = 1, kModeFused = 2 };
+
+__device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Where an item's result goes.
+struct ItemOut {
+    void *out;       // [B*Hq, D] OUT
+    float *lse;      // [B*Hq] or nullptr
+    int Hq;
+    int mode;
+    int n_split;
+    float *part_m, *part_l, *part_o;  // [R, n_split], [R, n_split], [R, n_split, D]
+    int32_t *counters;                // [B*Hkv] finished chunks per unit (fused mode)
+};
+
+template <int G>
+constexpr int stage_floats() { return 2 * G * kFusedMergeMaxSplits + 2 * G; }
+
+// Shared memory of the item end: the four warps' sums and references, the
+// decision of a deferred ticket (below), and the merge's staging area.  (The
+// staging area is its own: the weight buffers of the value product are not
+// free for it, since the entries of a warp's rows outside its own 32 keys
+// must stay zero.)
+struct ItemSmem {
+    float lred[4][4];  // [warp][head] weight sums
+    float mred[4][4];  // [warp][head] references
+    int merge_unit;    // unit whose partials are all written (-1: none)
+    float stage[stage_floats<4>()];
+};
+
+// A ticket taken and not yet looked at.  In fused mode the CTA that writes
+// a unit's last partial merges that unit; which CTA that is comes back from
+// a GPU-scope atomic on the unit's counter.  Thread 0 of the warpgroup
+// issues that atomic and only reads its result at the next item's end (or
+// after the last item), so no item waits for the round trip.
+struct PendingTicket {
+    int unit = -1;   // -1: none
+    int old = 0;     // the counter's value before this CTA's increment
+};
+
+// The merge of a unit whose partials are all written: out = sum_n e^(m_n -
+// max) o_n / sum_n e^(m_n - max) l_n, lse = max + ln(that sum), over the
+// unit's ns partials of each of its G heads.  The G x ns references (natural
+// log) and sums are staged in shared memory in one round of loads; warp h
+// turns head h's references into weights and sums them; every thread then
+// adds its 4 output dimensions of all ns partials with independent loads.
+template <int G, typename OUT, typename Sync>
+__device__ __forceinline__ bool merge_unit(const ItemOut &io, float *stage, int q4, int lane, size_t row0,
+                                           Sync &&group_sync)
+{
+    const int row = q4 * 32 + lane;
+    const int ns = io.n_split;
+
+    float *sw = stage;               // [G][ns] references, then weights
+    float *sl = stage + G * ns;      // [G][ns] sums
+    float *shd = stage + 2 * G * ns; // [G][2] maximum, weighted sum
+    for (int i = row; i < G * ns; i += kSoftThreads) {
+        const size_t pi = row0 * ns + i;  // head i / ns, partial i % ns
+        sw[i] = __ldcg(io.part_m + pi);
+        sl[i] = __ldcg(io.part_l + pi);
+    }
+    if (!group_sync())
+        return false;
+    if (q4 < G) {
+        float *wh = sw + q4 * ns;
+        const float *lh = sl + q4 * ns;
+        float mx = -INFINITY;
+        for (int n = lane; n < ns; n += 32)
+            mx = fmaxf(mx, wh[n]);
+#pragma unroll
+        for (int mask = 16; mask >= 1; mask >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, mask));
+        float lsum = 0.f;
+        for (int n = lane; n < ns; n += 32) {
+            const float m = wh[n];
+            const float a = m == -INFINITY ? 0.f : fast_exp2((m - mx) * kLog2e);
+            wh[n] = a;
+            lsum = fmaf(a, lh[n], lsum);
+        }
+#pragma unroll
+        for (int mask = 16; mask >= 1; mask >>= 1)
+            lsum += __shfl_xor_sync(kFull, lsum, mask);
+        if (lane == 0) {
+            shd[2 * q4] = mx;
+            shd[2 * q4 + 1] = lsum;
+        }
+    }
+    if (!group_sync())
+        return false;
+    for (int idx = row; idx < G * kD / 4; idx += kSoftThreads) {
+        const int h = idx / (kD / 4);
+        const int d4 = (idx - h * (kD / 4)) * 4;
+        const float *wh = sw + h * ns;
+        const float4 *po = reinterpret_cast<const float4 *>(io.part_o + (row0 + h) * ns * kD + d4);
+        float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int n = 0; n < ns; ++n) {
+            const float4 x = __ldcg(po + (size_t)n * (kD / 4));
+            const float a = wh[n];
+            os.x = fmaf(a, x.x, os.x);
+            os.y = fmaf(a, x.y, os.y);
+            os.z = fmaf(a, x.z, os.z);
+            os.w = fmaf(a, x.w, os.w);
+        }
+        const float mx = shd[2 * h], lsum = shd[2 * h + 1];
+        const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+        OUT *dst = static_cast<OUT *>(io.out) + (row0 + h) * kD + d4;
+        store_out(dst + 0, os.x * inv);
+        store_out(dst + 1, os.y * inv);
+        store_out(dst + 2, os.z * inv);
+        store_out(dst + 3, os.w * inv);
+        if (d4 == 0 && io.lse)
+            io.lse[row0 + h] = lsum > 0.f ? mx + fast_log2(lsum) * kLn2 : -INFINITY;
+    }
+    // the staging area is read above; the softmax warps write the next tile's
+    // weights to the same buffers only after this rendezvous
+    return group_sync();
+}
+
+// Thread 0 publishes the decision of its pending ticket (called before a
+// rendezvous, after which every thread reads sm->merge_unit).
+__device__ __forceinline__ void publish_ticket(const ItemOut &io, ItemSmem *sm, int row, PendingTicket &pt)
+{
+    if (row != 0)
+        return;
+    int u = -1;
+    if (pt.unit >= 0 && pt.old == io.n_split - 1) {
+        u = pt.unit;
+        io.counters[u] = 0;  // ready for the next launch
+    }
+    sm->merge_unit = u;
+}
+
+// The end of an item for softmax thread `row` (warp q4 of the warpgroup):
+// the four warps' states merged into the item's partial, which is the
+// result (one chunk) or is written to the partials; a unit whose partials
+// a deferred ticket found complete is merged; in fused mode this item's
+// ticket is taken (and left pending).  vscale multiplies the partial's
+// output (a value dequantisation factor, 1 for bf16 caches).  group_sync()
+// is a rendezvous of the four warps that returns false when the launch gave
+// up.  Returns false on give-up.
+template <int G, typename OUT, typename Sync>
+__device__ __forceinline__ bool finish_item(const ItemOut &io, ItemSmem *sm, float *stage, int q4, int lane, int unit,
+                                            int split, int b, int kvh, float vscale, const float (&mw)[G],
+                                            const float (&l_run)[G], const float (&o)[4][G], PendingTicket &pt,
+                                            Sync &&group_sync)
+{
+    const int row = q4 * 32 + lane;
+    // the four warps' states, merged
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        float v = l_run[g];
+#pragma unroll
+        for (int mask = 16; mask >= 1; mask >>= 1)
+            v += __shfl_xor_sync(kFull, v, mask);
+        if (lane == g) {
+            sm->lred[q4][g] = v;
+            sm->mred[q4][g] = mw[g];
+        }
+    }
+    if (io.mode == kModeFused)
+        publish_ticket(io, sm, row, pt);
+    if (!group_sync())
+        return false;
+    float ls[G], mt[G], of[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        mt[g] = fmax3(sm->mred[0][g], sm->mred[1][g], fmaxf(sm->mred[2][g], sm->mred[3][g]));
+        ls[g] = 0.f;
+        of[g] = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < 4; ++w2) {
+            const float m2 = sm->mred[w2][g];
+            const float be = m2 == -INFINITY ? 0.f : fast_exp2(m2 - mt[g]);
+            ls[g] = fmaf(sm->lred[w2][g], be, ls[g]);
+            of[g] = fmaf(o[w2][g], be, of[g]);
+        }
+        of[g] *= vscale;
+    }
+    const size_t row0 = (size_t)b * io.Hq + (size_t)kvh * G;
+    if (io.mode == kModeFinal) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float inv = ls[g] > 0.f ? 1.0f / ls[g] : 0.f;
+            store_out(static_cast<OUT *>(io.out) + (row0 + g) * kD + row, of[g] * inv);
+            if (row == g && io.lse)
+                io.lse[row0 + g] = ls[g] > 0.f ? (mt[g] + fast_log2(ls[g])) * kLn2 : -INFINITY;
+        }
+        return true;
+    }
+    const int ns = io.n_split;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const size_t pi = (row0 + g) * ns + split;
+        io.part_o[pi * kD + row] = of[g];
+        if (row == g) {
+            io.part_m[pi] = mt[g] == -INFINITY ? -INFINITY : mt[g] * kLn2;
+            io.part_l[pi] = ls[g];
+        }
+    }
+    if (io.mode != kModeFused)
+        return true;
+    // the unit an earlier ticket found complete (read after the rendezvous)
+    const int mu = *reinterpret_cast<volatile int *>(&sm->merge_unit);
+    // (unit u = b * Hkv + kvh has output rows u * G .. u * G + G - 1)
+    if (mu >= 0 && !merge_unit<G, OUT>(io, stage, q4, lane, (size_t)mu * G, group_sync))
+        return false;
+    // This item's ticket.  The rendezvous orders the warpgroup's partial
+    // stores before thread 0's GPU-scope acquire-release increment, which
+    // publishes them to the merging CTA (and, for that CTA, acquires the
+    // others').  Its result is read at the next item's end.
+    if (!group_sync())
+        return false;
+    if (row == 0) {
+        pt.unit = unit;
+        pt.old = atomic_add_acq_rel_gpu(&io.counters[unit], 1);
+    }
+    return true;
+}
+
+// After the last item: the decision of the last pending ticket, and its merge.
+template <int G, typename OUT, typename Sync>
+__device__ __forceinline__ bool finish_pending(const ItemOut &io, ItemSmem *sm, float *stage, int q4, int lane,
+                                               PendingTicket &pt, Sync &&group_sync)
+{
+    if (io.mode != kModeFused)
+        return true;
+    publish_ticket(io, sm, q4 * 32 + lane, pt);
+    if (!group_sync())
+        return false;
+    const int mu = *reinterpret_cast<volatile int *>(&sm->merge_unit);
+    if (mu >= 0)
+        return merge_unit<G, OUT>(io, stage, q4, lane, (size_t)mu * G, group_sync);
+    return true;
+}
+
+}  // namespace tcd
+}  // namespace ta

@@ -13,7 +13,12 @@ namespace ta {
 
 constexpr int kFanin = 64;            // partials merged by one warp per level
 constexpr int kStatusBytes = 256;     // status word region at the workspace start
-constexpr int kDecodeTileKeys = 120;  // chunks are whole multiples of this many keys (the decode tile)
+// Keys of one decode tile, the unit the chunks are whole multiples of: 128
+// (the MMA's M) for the tensor-core kernels' shapes, D = 128 with G = 2 or 4
+// query heads per KV head; 120 (15 warps of 8 keys) for the CUDA-core kernel.
+constexpr int kDecodeTileKeysTC = 128;
+constexpr int kDecodeTileKeysCC = 120;
+inline int decode_tile_keys(int D, int G) { return D == 128 && (G == 2 || G == 4) ? kDecodeTileKeysTC : kDecodeTileKeysCC; }
 // A split decode's workspace starts with a fixed control region that no
 // other use of the workspace writes: the status word and work-queue counter
 // (first 256 bytes), then one chunk counter per (sequence, KV head).
@@ -22,7 +27,7 @@ constexpr int kCtrlBytes = 16384;
 constexpr int kMaxFusedUnits = (kCtrlBytes - kStatusBytes) / 4;
 // Up to this many chunks per (sequence, KV head), and kMaxFusedUnits units,
 // the decode kernel merges the partials itself.
-constexpr int kFusedMergeMaxSplits = 64;
+constexpr int kFusedMergeMaxSplits = 128;
 // Time limit of a pipeline wait inside the kernels when the caller sets none.
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 

@@ -124,6 +124,36 @@ __device__ __forceinline__ float add_f16x2(float acc, uint32_t w)
     return r;
 }
 
+// Packed fp32 pairs (two lanes of one 64-bit register, one instruction per pair).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float2 f2_unpack(uint64_t w)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(w));
+    return r;
+}
+
+// a * b + c on both lanes
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ uint4 out_pack4(const float *x, __nv_bfloat16 *)
 {
     return make_uint4(tc::pack_bf16x2(x[0], x[1]), tc::pack_bf16x2(x[2], x[3]), tc::pack_bf16x2(x[4], x[5]),
@@ -423,23 +453,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                     alpha = fast_exp2(m_used - mcand);
                     m_used = mcand;
                 }
-                const float neg_m = -m_used;
-                float ls[2] = {0.f, 0.f}, lsr[2] = {0.f, 0.f};
+                // two columns at a time in packed fp32 pairs: the exponent
+                // s * scale * log2(e) - m, then the sum of the weights
+                const uint64_t c2 = f2_pack(c, c), negm2 = f2_pack(-m_used, -m_used);
+                uint64_t ls2 = f2_pack(0.f, 0.f);
+                float lsr[2] = {0.f, 0.f};
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float p0 = fast_exp2(fmaf(s[half * 64 + 2 * i], c, neg_m));
-                        const float p1 = fast_exp2(fmaf(s[half * 64 + 2 * i + 1], c, neg_m));
+                        const float2 e = f2_unpack(
+                            f2_fma(f2_pack(s[half * 64 + 2 * i], s[half * 64 + 2 * i + 1]), c2, negm2));
+                        const float p0 = fast_exp2(e.x);
+                        const float p1 = fast_exp2(e.y);
                         const uint32_t w = tc::pack_f16x2(p0, p1);
                         pk[i] = w;
-                        ls[i & 1] += p0 + p1;
+                        ls2 = f2_add(ls2, f2_pack(p0, p1));
                         lsr[i & 1] = add_f16x2(lsr[i & 1], w);
                     }
                     tc::tmem_st32(s_tmem + half * 32, pk);
                 }
-                l = l * alpha + (ls[0] + ls[1]);
+                const float2 ls = f2_unpack(ls2);
+                l = l * alpha + (ls.x + ls.y);
                 lr = lr * alpha + (lsr[0] + lsr[1]);
                 if (j > 0 && __any_sync(0xffffffffu, resc)) {
                     // O_t holds every PV up to j-1 (see the MMA issuer);

@@ -8,7 +8,8 @@
 // here keeps every SM busy: the persistent decode kernel runs
 // sm_count * ctas_per_sm CTAs, and the chunk count is chosen so that the
 // (sequence, KV head, chunk) work items fill those CTAs evenly.  Chunks are
-// whole numbers of the kernel's 120-key tiles.
+// whole numbers of the decode kernel's tiles (128 keys for the tensor-core
+// shapes, 120 for the CUDA-core kernel).
 #include <algorithm>
 #include <climits>
 
@@ -72,11 +73,12 @@ ta_status plan_decode(int B, int Hq, int Hkv, int S, int D, int chunk, int n_spl
         return TA_ERR_INVALID_ARG;
     }
     const int64_t units = (int64_t)B * Hkv;           // independent (sequence, KV head) pairs
+    const int64_t tile = decode_tile_keys(D, Hq / Hkv);
     const int64_t slots = (int64_t)sm_count * decode_ctas_per_sm();
     auto chunk_for = [&](int64_t ns) {
         // a whole number of the kernel's tiles, at least two
-        int64_t c = ceil_div(ceil_div(S, ns), kDecodeTileKeys) * kDecodeTileKeys;
-        c = std::max<int64_t>(c, 2 * kDecodeTileKeys);
+        int64_t c = ceil_div(ceil_div(S, ns), tile) * tile;
+        c = std::max<int64_t>(c, 2 * tile);
         return std::min<int64_t>(c, S);
     };
     int64_t c;
@@ -93,7 +95,7 @@ ta_status plan_decode(int B, int Hq, int Hkv, int S, int D, int chunk, int n_spl
         // minimises (waves of items over the CTA slots) x (keys per item +
         // a fixed per-item cost of 64 keys), preferring fewer chunks on ties.
         int64_t best_c = chunk_for(1), best_cost = INT64_MAX;
-        const int64_t max_ns = std::min<int64_t>(ceil_div(S, 2 * kDecodeTileKeys), 8 * ceil_div(slots, units) + 1);
+        const int64_t max_ns = std::min<int64_t>(ceil_div(S, 2 * tile), 8 * ceil_div(slots, units) + 1);
         for (int64_t ns = 1; ns <= std::max<int64_t>(1, max_ns); ++ns) {
             const int64_t cc = chunk_for(ns);
             const int64_t real_ns = ceil_div(S, cc);
@@ -113,7 +115,7 @@ ta_status plan_decode(int B, int Hq, int Hkv, int S, int D, int chunk, int n_spl
         return TA_ERR_INVALID_ARG;
     }
     int levels = 0;
-    if (ns > 1) {
+    if (ns > 1 && !decode_merges_itself((int)ns, (int)std::min<int64_t>(units, INT_MAX))) {
         int64_t n = ns;
         levels = 1;
         while (n > kFanin) {

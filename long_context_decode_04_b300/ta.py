@@ -143,6 +143,11 @@ def plan_decode(B, Hq, Hkv, S, D, *, chunk=0, n_split=0, varlen=False, sm_count=
     return p
 
 
+def chunk_bounds(plan: DecodePlan, S: int):
+    """[(start, end)] of the plan's chunks over S keys (include/ta.h)."""
+    return [(min(c * plan.chunk, S), min((c + 1) * plan.chunk, S)) for c in range(plan.n_split)]
+
+
 def decode_workspace(B, Hq, Hkv, S, D, *, chunk=0, n_split=0, varlen=False, device="cuda") -> torch.Tensor:
     """A zeroed device workspace big enough for ``decode(..., workspace=...)``."""
     plan = plan_decode(B, Hq, Hkv, S, D, chunk=chunk, n_split=n_split, varlen=varlen)

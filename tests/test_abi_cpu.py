@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def _chunks(plan, S):
-    return [(c * plan.chunk, min((c + 1) * plan.chunk, S)) for c in range(plan.n_split)]
+    return ta.chunk_bounds(plan, S)
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,S,D", [
@@ -44,8 +44,8 @@ def test_plan_covers_every_key_once(B, Hq, Hkv, S, D, varlen):
     assert ch[-1][0] < ch[-1][1]
     items = B * Hkv * plan.n_split
     assert plan.grid == min(items, SMS)
-    if plan.n_split == 1:
-        assert plan.levels == 0
+    if plan.n_split == 1 or (plan.n_split <= 128 and B * Hkv <= 4032):
+        assert plan.levels == 0  # one chunk, or the decode kernel merges its chunks itself
     else:
         n, lv = plan.n_split, 1
         while n > plan.fanin:
@@ -56,10 +56,24 @@ def test_plan_covers_every_key_once(B, Hq, Hkv, S, D, varlen):
 
 
 def test_plan_of_the_128k_workload_fills_the_sms_evenly():
+    """Two items per SM: 8 KV heads x 37 chunks of 28 whole 128-key tiles."""
     plan = ta.plan_decode(1, 32, 8, 131072, 128, sm_count=SMS)
     items = 8 * plan.n_split
     assert items % SMS == 0 and plan.grid == SMS
-    assert plan.chunk % 120 == 0 and plan.chunk >= 240  # whole 120-key tiles
+    assert plan.chunk % 128 == 0 and plan.chunk >= 256  # whole 128-key tiles of the tensor-core kernel
+    assert plan.levels == 0  # merged inside the decode kernel
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,tile", [(32, 8, 128, 128), (16, 8, 128, 128), (8, 8, 128, 120),
+                                           (4, 4, 64, 120), (32, 8, 64, 120), (64, 8, 64, 120)])
+def test_plan_chunks_are_whole_tiles_of_the_kernel_for_the_shape(Hq, Hkv, D, tile):
+    """Chunks are whole 128-key tiles for the tensor-core shapes (D = 128, G = 2 or
+    4) and whole 120-key tiles for the CUDA-core kernel's shapes, at least two."""
+    for S in (300, 5000, 131072, 1 << 20):
+        for varlen in (False, True):
+            plan = ta.plan_decode(2, Hq, Hkv, S, D, varlen=varlen, sm_count=SMS)
+            if plan.n_split > 1:
+                assert plan.chunk % tile == 0 and plan.chunk >= 2 * tile, (S, varlen, plan.chunk)
 
 
 def test_plan_overrides():

@@ -50,7 +50,7 @@ def test_small_shapes_f32_out(name, S):
     _compare(x, out, lse, bf16=False)
 
 
-@pytest.mark.parametrize("n_split", [1, 2, 3, 7, 64, 65, 200])
+@pytest.mark.parametrize("n_split", [1, 2, 3, 7, 64, 65, 128, 129, 200])
 def test_forced_splits_and_levels(n_split):
     w = synth.WORKLOADS["gqa_32x8_d128_s131072"]
     x = synth.make_inputs(w, S=4099)
@@ -140,9 +140,9 @@ def test_probe_columns_at_large_counts():
     expect = []
     for b, L in enumerate(lens):
         probes = {0, L - 1}
-        for c in range(plan.n_split):
-            for j in (c * plan.chunk, c * plan.chunk + plan.chunk - 1):
-                if j < L:
+        for c0, c1 in ta.chunk_bounds(plan, S):
+            for j in (c0, c1 - 1):
+                if 0 <= j < L:
                     probes.add(j)
         for j in probes:
             v[b, :, j, 1] = 1.0

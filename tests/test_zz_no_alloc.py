@@ -69,14 +69,15 @@ def test_noalloc_matches_ta_decode_on_two_calls_in_a_row(name, kw):
     assert not torch.equal(a[0], b[0])
 
 
-def test_noalloc_separate_merge_path_over_64_chunks():
-    """A plan with more than 64 chunks (so a separate merge launch reads the
-    partials from, and writes its intermediates into, the fixed scratch): one
-    sequence of 131072 keys passed with its length (the length-agnostic plan
-    over-decomposes), twice in a row."""
-    w = synth.WORKLOADS["gqa_32x8_d128_s131072"]
-    plan = ta.plan_decode(1, 32, 8, w.S, 128, varlen=True)
-    assert plan.n_split > 64 and plan.workspace_bytes <= SCRATCH_BYTES
+def test_noalloc_separate_merge_path_over_128_chunks():
+    """A plan with more than 128 chunks (so separate merge launches read the
+    partials from, and write their intermediates into, the fixed scratch): one
+    sequence with one KV head and 131072 keys passed with its length (the
+    length-agnostic plan over-decomposes to about four items per SM), twice in
+    a row."""
+    w = synth.Workload("one_kv_head", 2, "decode", 1, 4, 1, 131072, 128, "bf16")
+    plan = ta.plan_decode(1, 4, 1, w.S, 128, varlen=True)
+    assert plan.n_split > 128 and plan.levels == 2 and plan.workspace_bytes <= SCRATCH_BYTES
     for seed in (None, 78):
         x = synth.make_inputs(w, seed=seed)
         x["seqlens"] = torch.tensor([w.S], dtype=torch.int32)
