@@ -41,9 +41,11 @@ DECODE_WORKLOAD = "gqa_32x8_d128_s131072"
 WORKLOAD_DESC = (f"{DECODE_WORKLOAD}: B=1, Hq=32, Hkv=8, D=128, S=131072, bf16 q/K/V N(0,1), "
                  f"scale=1/sqrt(128)")
 PREFILL_WORKLOAD = "causal_prefill_32x8_d128_s16384"
-PROFILES = {  # committed ncu summaries: (file, kernel source they were taken on)
-    "decode": ("decode_tc_kernel_gqa_32x8_d128_s131072.md", "decode_tc.cu"),
-    "prefill": ("prefill_causal_kernel_causal_prefill_32x8_d128_s16384.md", "prefill.cu"),
+PROFILES = {  # committed ncu summaries: (file, kernel sources they were taken on)
+    "decode": ("decode_tc_kernel_gqa_32x8_d128_s131072.md",
+               ("decode_tc.cu", "decode_tc_common.cuh", "common.cuh", "tcgen05.cuh")),
+    "prefill": ("prefill_causal_kernel_causal_prefill_32x8_d128_s16384.md",
+                ("prefill.cu", "common.cuh", "tcgen05.cuh")),
 }
 
 
@@ -123,7 +125,7 @@ def source_hash(path):
 def profiled_traffic(which):
     """DRAM bytes per launch of a kernel from its committed ncu summary, if the
     kernel source is unchanged since that capture; else None."""
-    name, src_name = PROFILES[which]
+    name, src_names = PROFILES[which]
     try:
         text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
@@ -133,9 +135,10 @@ def profiled_traffic(which):
         if ":" in line and line.startswith("- "):
             key, _, val = line[2:].partition(":")
             kv[key.strip()] = val.strip().strip("`")
-    src = os.path.join(ROOT, "long_context_decode_04_b300", "csrc", src_name)
-    if kv.get(f"{src_name} sha256") != source_hash(src):
-        return None
+    for src_name in src_names:
+        src = os.path.join(ROOT, "long_context_decode_04_b300", "csrc", src_name)
+        if kv.get(f"{src_name} sha256") != source_hash(src):
+            return None
     try:
         return int(kv["dram bytes per launch"])
     except (KeyError, ValueError):
@@ -420,6 +423,45 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_launches(which, n):
+    """A few plain launches of one workload and nothing else (no timing, no
+    JSON): the command the ncu captures in profiles/ run.  `which` is one of
+    decode (the 128K-token GQA decode), fp8 (the same over an E4M3 cache),
+    paged (the 16-sequence variable-length decode in 64-key pages), prefill
+    (the 16K-token causal prefill)."""
+    import torch
+    from long_context_decode_04_b300 import synth, ta
+    dev = torch.device("cuda", 0)
+    if which == "prefill":
+        pw = synth.WORKLOADS[PREFILL_WORKLOAD]
+        y = synth.make_inputs(pw)
+        pq, pk, pv = (y[n].to(dev) for n in ("q", "k", "v"))
+        fn = lambda: ta.prefill_causal(pq, pk, pv, scale=pw.scale)
+    elif which == "paged":
+        w = synth.WORKLOADS["varlen_b16_32x8_d128_s1k_32k"]
+        x = synth.make_inputs(w)
+        lens = [int(v) for v in x["seqlens"]]
+        kp, vp, bt = synth.to_pages(x["k"], x["v"], lens, 64, seed=11)
+        q, kp, vp, bt = x["q"].to(dev), kp.to(dev), vp.to(dev), bt.to(dev)
+        sl = x["seqlens"].to(dev)
+        fn = lambda: ta.decode_paged(q, kp, vp, bt, sl, scale=w.scale)
+    else:
+        w = synth.WORKLOADS[DECODE_WORKLOAD]
+        x = synth.make_inputs(w)
+        q = x["q"].to(dev)
+        if which == "fp8":
+            k8, ks = synth.to_e4m3(x["k"])
+            v8, vs = synth.to_e4m3(x["v"])
+            k8, ks, v8, vs = k8.to(dev), ks.to(dev), v8.to(dev), vs.to(dev)
+            fn = lambda: ta.decode_fp8(q, k8, v8, k_scale=ks, v_scale=vs, scale=w.scale)
+        else:
+            k, v = x["k"].to(dev), x["v"].to(dev)
+            fn = lambda: ta.decode(q, k, v, scale=w.scale)
+    for _ in range(n):
+        fn()
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -430,9 +472,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-extra", action="store_true", help="skip the variable-length / paged decode figures")
+    ap.add_argument("--launches", choices=["decode", "fp8", "paged", "prefill"],
+                    help="only make --steps plain launches of one workload (for profilers); prints nothing")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_env()
+
+    if args.launches:
+        run_launches(args.launches, args.steps)
+        return
 
     if args.impl == "reference":
         run_reference(args, rank, world)
