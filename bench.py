@@ -318,6 +318,42 @@ def measure_fp8(ta, synth, accounting, peaks, dev, w, x, reps=20):
             "kv_bytes": kv_bytes, "us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
 
 
+def measure_nvfp4(ta, synth, accounting, peaks, dev, w, x, reps=20):
+    """Decode of the 128K-token workload with its K/V quantised to NVFP4 (E2M1
+    codes, one E4M3 scale per 16 elements, one factor per KV head): median of
+    `reps` graph replays; bytes read: 0.5 per element plus 1/16 for the block
+    scales."""
+    import torch
+    k4, kbs, kf = synth.to_nvfp4(x["k"])
+    v4, vbs, vf = synth.to_nvfp4(x["v"])
+    q = x["q"].to(dev)
+    k4, kbs, kf, v4, vbs, vf = (t.to(dev) for t in (k4, kbs, kf, v4, vbs, vf))
+    kv_bytes = 2 * w.B * w.Hkv * w.S * (w.D // 2 + w.D // 16)
+    ws = ta.decode_workspace(w.B, w.Hq, w.Hkv, w.S, w.D, device=dev)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    fn = lambda: ta.decode_nvfp4(q, k4, v4, kbs, vbs, k_factor=kf, v_factor=vf, scale=w.scale, workspace=ws,
+                                 out=out, lse=lse)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = sorted(1e3 * a.elapsed_time(b) for a, b in ev)[reps // 2]
+    gbs = kv_bytes / (us / 1e6) / 1e9
+    return {"workload": "B=1, Hq=32, Hkv=8, D=128, S=131072, K/V NVFP4 (E2M1 + E4M3 per 16 elements + fp32 per KV "
+                        "head), bf16 q",
+            "kv_bytes": kv_bytes, "us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
+
+
 def measure_prefill_varlen(ta, synth, peaks, dev, reps=5):
     """Causal prefill of 8 packed sequences with lengths uniform in [1024, 16384]
     (seeded), 32 heads / 8 KV heads: median of `reps` graph replays."""
@@ -626,6 +662,7 @@ def main():
     extra = None if args.no_extra else measure_varlen(ta, synth, accounting, peaks, dev)
     pi_fig = None if args.no_extra else measure_pi(ta, accounting, peaks, dev, w, q, k, v)
     fp8_fig = None if args.no_extra else measure_fp8(ta, synth, accounting, peaks, dev, w, x)
+    nvfp4_fig = None if args.no_extra else measure_nvfp4(ta, synth, accounting, peaks, dev, w, x)
     others_fig = None if args.no_extra else measure_other_configs(ta, synth, accounting, peaks, dev)
     pvar_fig = None if (args.no_extra or not do_prefill) else measure_prefill_varlen(ta, synth, peaks, dev)
 
@@ -710,6 +747,7 @@ def main():
         "varlen_b16": extra,
         "pi_attention": pi_fig,
         "fp8_kv": fp8_fig,
+        "nvfp4_kv": nvfp4_fig,
         "other_decode_configs": others_fig,
         "prefill_varlen": pvar_fig,
         "gpu_launches": launches_per_step * args.steps,

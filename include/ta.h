@@ -220,6 +220,28 @@ ta_status ta_decode_ex(const ta_decode_params *p);
 ta_status ta_decode_fp8(const ta_decode_params *p, const float *k_scale, const float *v_scale);
 
 /*
+ * Split-KV decode over an NVFP4 KV cache: about a quarter of the bytes of a
+ * bf16 cache (the ThriftAttention page, hyperion-consulting.io, "the rise of
+ * FP4": NVFP4 KV-cache compression; the COMPUTE layer: low-precision storage
+ * inside a kernel that computes in higher precision).
+ *   k, v [B, Hkv, S, D/2] bytes: FP4 E2M1 codes (sign, 2 exponent bits with
+ *   bias 1, 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), element
+ *   2i of a row in the low nibble of byte i, element 2i + 1 in the high one;
+ *   k_block_scales, v_block_scales [B, Hkv, S, D/16] bytes: one E4M3 scale per
+ *   16 consecutive elements of a row; k_factor, v_factor [B * Hkv] fp32 on
+ *   the device, or NULL (1).  The value of element d of key j of (b, kv head)
+ *   is e2m1 * e4m3(block d / 16) * factor[b * Hkv + kv head].
+ *   q bf16 (p->in_dtype = TA_BF16), output bf16 or fp32, fp32 accumulation;
+ *   every element is widened exactly to fp16 on chip.  Everything else as
+ *   ta_decode_ex.
+ *   Supported: D = 128, G in {2, 4}, S a multiple of 16, chunks of whole
+ *   128-key tiles (the default plan; chunk overrides that are multiples of
+ *   128).  k, v, k_block_scales, v_block_scales 16-byte aligned.
+ */
+ta_status ta_decode_nvfp4(const ta_decode_params *p, const void *k_block_scales, const void *v_block_scales,
+                          const float *k_factor, const float *v_factor);
+
+/*
  * Split-KV decode over the key set of pi-Attention (pi-Attention explainer,
  * gist.science/ja/paper/2511.10696, technical summary section 2A): the
  * query of each sequence, the newest token i = L_b - 1, attends

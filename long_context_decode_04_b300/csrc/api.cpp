@@ -223,7 +223,8 @@ namespace {
 // given (block_table != nullptr; p->k, p->v are then the page pools).
 ta_status decode_impl(const ta_decode_params *p, const int32_t *block_table, int page_size, int pages_per_seq,
                       int num_pages, int pi_window = 0, int pi_period = 0, bool kv_fp8 = false,
-                      const float *k_scale = nullptr, const float *v_scale = nullptr)
+                      const float *k_scale = nullptr, const float *v_scale = nullptr, bool kv_nvfp4 = false,
+                      const void *k_bs = nullptr, const void *v_bs = nullptr)
 {
     ta_status s;
     ta_decode_plan plan;
@@ -257,6 +258,9 @@ ta_status decode_impl(const ta_decode_params *p, const int32_t *block_table, int
     a.kv_fp8 = kv_fp8;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    a.kv_nvfp4 = kv_nvfp4;
+    a.k_bs = k_bs;
+    a.v_bs = v_bs;
     a.wait_ns = ta::wait_limit_or_default(p->wait_limit_ns);
     a.test_stall = ta::injected_stall();
     a.q = p->q;
@@ -328,6 +332,35 @@ ta_status ta_decode_fp8(const ta_decode_params *p, const float *k_scale, const f
     if ((k_scale && !aligned(k_scale, 4)) || (v_scale && !aligned(v_scale, 4)))
         return fail(TA_ERR_INVALID_ARG, "k_scale and v_scale must be 4-byte aligned");
     return decode_impl(p, nullptr, 0, 0, 0, 0, 0, true, k_scale, v_scale);
+}
+
+ta_status ta_decode_nvfp4(const ta_decode_params *p, const void *k_block_scales, const void *v_block_scales,
+                          const float *k_factor, const float *v_factor)
+{
+    ta_status s = validate_decode(p);
+    if (s != TA_OK)
+        return s;
+    if (p->in_dtype != TA_BF16)
+        return fail(TA_ERR_INVALID_ARG, "NVFP4 decode takes bf16 queries (in_dtype = TA_BF16)");
+    if (!k_block_scales || !v_block_scales)
+        return fail(TA_ERR_INVALID_ARG, "k_block_scales and v_block_scales must be non-NULL");
+    if (!aligned(k_block_scales, 16) || !aligned(v_block_scales, 16))
+        return fail(TA_ERR_INVALID_ARG, "k_block_scales and v_block_scales must be 16-byte aligned");
+    if ((k_factor && !aligned(k_factor, 4)) || (v_factor && !aligned(v_factor, 4)))
+        return fail(TA_ERR_INVALID_ARG, "k_factor and v_factor must be 4-byte aligned");
+    const int G = p->Hq / p->Hkv;
+    if (p->D != 128 || (G != 2 && G != 4))
+        return fail(TA_ERR_UNSUPPORTED, "NVFP4 decode supports D = 128 with 2 or 4 query heads per KV head");
+    if (p->S % 16 != 0)
+        return fail(TA_ERR_UNSUPPORTED, "NVFP4 decode needs S (the cache's keys per sequence) a multiple of 16");
+    ta_decode_plan plan;
+    s = ta_decode_plan_for(p->B, p->Hq, p->Hkv, p->S, p->D, p->chunk, p->n_split, p->seqlens != nullptr, 0, &plan);
+    if (s != TA_OK)
+        return s;
+    if (plan.n_split > 1 && plan.chunk % ta::kDecodeTileKeysTC != 0)
+        return fail(TA_ERR_UNSUPPORTED, "NVFP4 decode needs chunks of whole 128-key tiles (chunk override a "
+                                        "multiple of 128, or an n_split that gives such chunks)");
+    return decode_impl(p, nullptr, 0, 0, 0, 0, 0, false, k_factor, v_factor, true, k_block_scales, v_block_scales);
 }
 
 ta_status ta_decode_pi(const ta_decode_params *p, int window, int period)
@@ -441,6 +474,8 @@ ta_status ta_decode_partials(const ta_decode_params *p, float *m, float *l, floa
     a.pi_window = a.pi_period = 0;
     a.kv_fp8 = false;
     a.k_scale = a.v_scale = nullptr;
+    a.kv_nvfp4 = false;
+    a.k_bs = a.v_bs = nullptr;
     a.wait_ns = ta::wait_limit_or_default(p->wait_limit_ns);
     a.test_stall = ta::injected_stall();
     a.stream = static_cast<cudaStream_t>(p->stream);

@@ -981,6 +981,8 @@ cudaError_t launch_decode(const DecodeLaunch &a)
         return launch_decode_tc(a);
     if (decode_fp8_tc_eligible(a))
         return launch_decode_fp8_tc(a);
+    if (a.kv_nvfp4)
+        return cudaErrorNotSupported;  // NVFP4 caches run on the tensor-core kernel only
     DecodeParams p;
     p.q = a.q;
     p.k = a.k;

@@ -58,10 +58,29 @@ constexpr int kTile = kDecodeTileKeysTC;  // 128 keys a tile
 constexpr int kRows = 128;                // MMA rows: one key a row
 constexpr int kN = 16;                  // score-product N: the group's heads, zero-padded
 constexpr int kON = 2 * kN;             // value-product N: (warp, head) columns, hi then lo
-constexpr int kRawStages = 3;
 constexpr int kConvBufs = 3;                      // widened tiles (K in TMEM, V in shared memory)
-constexpr int kRawTile = kTile * kD;              // 128 rows of 128 one-byte codes
-constexpr int kRawStage = 2 * kRawTile;           // K then V
+// The raw ring holds tiles as they arrive by TMA, in the cache's format:
+//   E4M3:  K then V, each 128 rows of 128 one-byte codes (128-byte swizzle);
+//   NVFP4: K codes, V codes (each 128 keys x 64 bytes seen as 64 rows of 128
+//          bytes, two keys a row, 128-byte swizzle), then K and V block
+//          scales (each 128 keys x 8 bytes seen as 8 rows of 128 bytes).
+template <bool NV4>
+struct Raw;
+template <>
+struct Raw<false> {
+    static constexpr int kKBytes = kTile * kD;     // 16 KiB
+    static constexpr int kStage = 2 * kKBytes;     // 32 KiB
+    static constexpr int kStages = 3;
+};
+template <>
+struct Raw<true> {
+    static constexpr int kCodes = kTile * kD / 2;  // 8 KiB
+    static constexpr int kScales = kTile * kD / 16;  // 1 KiB
+    static constexpr int kStage = 2 * kCodes + 2 * kScales;  // 18 KiB
+    static constexpr int kStages = 5;
+};
+constexpr int kMaxRawStages = 5;
+constexpr int kRawRegion = 98304;                 // room for either ring
 constexpr int kHalf = kRows * 128;                // one 64-dim half of an fp16 V tile
 constexpr int kVBytes = 2 * kHalf;                // 32 KiB
 constexpr int kQHalf = kN * 128;
@@ -72,8 +91,7 @@ constexpr int kVOff = 0;                          // kConvBufs fp16 V tiles
 constexpr int kQOff = kVOff + kConvBufs * kVBytes;  // two fp16 Q operands
 constexpr int kPOff = kQOff + 2 * kQBytes;        // two P operands
 constexpr int kRawOff = kPOff + 2 * kPBytes;      // the raw ring
-constexpr int kMiscOff = kRawOff + kRawStages * kRawStage;
-constexpr uint32_t kRawTx = (uint32_t)kRawStage;  // bytes of one raw stage
+constexpr int kMiscOff = kRawOff + kRawRegion;
 constexpr int kDescRing = 8;
 constexpr int kSoftWarp0 = 4;
 constexpr int kConvWarp0 = 8;
@@ -96,8 +114,8 @@ struct TileDesc {
 };
 
 struct Misc {
-    uint64_t raw_full[kRawStages];   // raw codes landed (TMA bytes), descriptor written
-    uint64_t raw_empty[kRawStages];  // raw codes widened (128 converting threads)
+    uint64_t raw_full[kMaxRawStages];   // raw codes landed (TMA bytes), descriptor written
+    uint64_t raw_empty[kMaxRawStages];  // raw codes widened (128 converting threads)
     uint64_t conv_full[kConvBufs];   // K in TMEM and V as fp16 (128 converting threads)
     uint64_t conv_empty[kConvBufs];  // the value product of the tile read them (MMA commit)
     uint64_t s_full[2];              // S in TMEM (MMA commit) and its descriptor (score issuer)
@@ -118,11 +136,17 @@ struct Misc {
 
 constexpr size_t kSmem = (size_t)kMiscOff + sizeof(Misc) + 1024;  // + alignment slack
 static_assert(kSmem <= 232448, "shared memory per CTA");
-static_assert(kRawTile % 1024 == 0 && kRawOff % 1024 == 0, "raw tiles on 1024-byte boundaries (swizzle atoms)");
+static_assert(Raw<false>::kStages * Raw<false>::kStage <= kRawRegion && Raw<true>::kStages * Raw<true>::kStage <= kRawRegion,
+              "raw rings");
+static_assert(Raw<false>::kKBytes % 1024 == 0 && Raw<true>::kCodes % 1024 == 0 && Raw<true>::kStage % 1024 == 0 &&
+                  kRawOff % 1024 == 0, "raw tiles on 1024-byte boundaries (swizzle atoms)");
 static_assert(kTile * 16 % kSoftThreads == 0, "V widening tasks per thread");
 
 struct Fp8Params {
-    CUtensorMap kmap, vmap;  // raw codes (D, S, B*Hkv), box 128 x 128
+    // E4M3: codes (D, S, B*Hkv), box 128 x 128; NVFP4: codes (128 bytes,
+    // S/2, B*Hkv), box 128 x 64, and block scales (128 bytes, S/16, B*Hkv),
+    // box 128 x 8
+    CUtensorMap kmap, vmap, ksmap, vsmap;
     const __nv_bfloat16 *q;
     void *out;
     float *lse;
@@ -156,7 +180,35 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t
     hi = e4m3x2_to_f16x2(w >> 16);
 }
 
-template <int G, typename OUT>
+// Eight E2M1 codes of a word (element 2i in the low nibble of byte i) to
+// four fp16 pairs, each multiplied by the fp16 pair s2: an E2M1 value (2
+// significant bits) times an E4M3 scale (4) is exact in fp16 (11), and in
+// its range (at most 6 * 448 in magnitude, at least 2^-10 when not 0).
+__device__ __forceinline__ void e2m1x8_scaled(uint32_t w, uint32_t s2, uint32_t (&d)[4])
+{
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        ".reg .b32 c0, c1, c2, c3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 c0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 c1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 c2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 c3, b3;\n\t"
+        "mul.rn.f16x2 %0, c0, %5;\n\t"
+        "mul.rn.f16x2 %1, c1, %5;\n\t"
+        "mul.rn.f16x2 %2, c2, %5;\n\t"
+        "mul.rn.f16x2 %3, c3, %5;\n\t}"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(w), "r"(s2));
+}
+
+// An E4M3 block scale (one byte) as an fp16 pair (the value twice).
+__device__ __forceinline__ uint32_t e4m3_scale2(uint32_t byte)
+{
+    const uint32_t h = e4m3x2_to_f16x2(byte & 0xffu) & 0xffffu;
+    return h | (h << 16);
+}
+
+template <int G, typename OUT, bool NV4>
 __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid_constant__ Fp8Params p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -174,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
         *reinterpret_cast<uint4 *>(smem + kQOff + i * 16) = z4;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 
+    using RC = Raw<NV4>;
+    constexpr int kRawStages = RC::kStages;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRawStages; ++s) {
             mbar_init(&ms->raw_full[s], 1);
@@ -217,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
         }
         const uint64_t policy = l2_policy_evict_first();
         int stage = 0, ti = 0, ic = 0;
-        uint32_t uses[kRawStages] = {};
+        uint32_t uses[kMaxRawStages] = {};
         uint32_t q_uses[2] = {0u, 0u};
         // The item's G query rows as fp16 into Q buffer ic % 2: 16-byte chunk c
         // of head h (8 dims) to row h of the operand, 128-byte swizzle.
@@ -315,10 +369,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                         if (n > 0) {
                             // rows past S read as zero; V rows in [n, 128) are
                             // written as zero by the converting threads
-                            unsigned char *rd = smem + kRawOff + stage * kRawStage;
-                            mbar_arrive_expect_tx(fb, kRawTx);
-                            tc::tma_load_3d_hint(rd, &p.kmap, 0, j0, unit, fb, policy);
-                            tc::tma_load_3d_hint(rd + kRawTile, &p.vmap, 0, j0, unit, fb, policy);
+                            unsigned char *rd = smem + kRawOff + stage * RC::kStage;
+                            mbar_arrive_expect_tx(fb, (uint32_t)RC::kStage);
+                            if constexpr (!NV4) {
+                                tc::tma_load_3d_hint(rd, &p.kmap, 0, j0, unit, fb, policy);
+                                tc::tma_load_3d_hint(rd + RC::kKBytes, &p.vmap, 0, j0, unit, fb, policy);
+                            } else {
+                                // tiles start on multiples of 128 keys: whole
+                                // code rows (2 keys) and scale rows (16 keys)
+                                tc::tma_load_3d_hint(rd, &p.kmap, 0, j0 / 2, unit, fb, policy);
+                                tc::tma_load_3d_hint(rd + RC::kCodes, &p.vmap, 0, j0 / 2, unit, fb, policy);
+                                tc::tma_load_3d_hint(rd + 2 * RC::kCodes, &p.ksmap, 0, j0 / 16, unit, fb, policy);
+                                tc::tma_load_3d_hint(rd + 2 * RC::kCodes + RC::kScales, &p.vsmap, 0, j0 / 16, unit, fb,
+                                                     policy);
+                            }
                         } else {
                             mbar_arrive(fb);
                         }
@@ -455,28 +519,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                 mbar_arrive(&ms->conv_full[cv]);  // the issuers read the end from the descriptor
                 break;
             }
-            const unsigned char *rk = smem + kRawOff + stage * kRawStage;
-            const unsigned char *rv = rk + kRawTile;
-            // K row ct into TMEM lane ct: 128 codes -> 64 fp16 pairs (the raw
-            // rows are swizzled, so the 32 lanes' chunks fall in 8 bank groups)
-            {
+            const unsigned char *rk = smem + kRawOff + stage * RC::kStage;
+            const uint32_t k_tm = tmem + lane_base + kKCol + cv * (kD / 2);
+            unsigned char *vd = smem + kVOff + cv * kVBytes;
+            constexpr int kVTasks = kTile * 16 / kSoftThreads;  // 16 a thread
+            if constexpr (!NV4) {
+                const unsigned char *rv = rk + RC::kKBytes;
+                // K row ct into TMEM lane ct: 128 codes -> 64 fp16 pairs (the raw
+                // rows are swizzled, so the 32 lanes' chunks fall in 8 bank groups)
                 uint32_t kr[32];
                 uint32_t kh[32];
-                if (ct < kTile) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 x = *reinterpret_cast<const uint4 *>(rk + ct * kD + ((c ^ (ct & 7)) << 4));
-                        kr[4 * c + 0] = x.x;
-                        kr[4 * c + 1] = x.y;
-                        kr[4 * c + 2] = x.z;
-                        kr[4 * c + 3] = x.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        kr[i] = 0u;
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 x = *reinterpret_cast<const uint4 *>(rk + ct * kD + ((c ^ (ct & 7)) << 4));
+                    kr[4 * c + 0] = x.x;
+                    kr[4 * c + 1] = x.y;
+                    kr[4 * c + 2] = x.z;
+                    kr[4 * c + 3] = x.w;
                 }
-                const uint32_t k_tm = tmem + lane_base + kKCol + cv * (kD / 2);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -484,30 +544,92 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                         e4m3x4_to_f16(kr[16 * half + i], kh[2 * i], kh[2 * i + 1]);
                     tc::tmem_st32(k_tm + 32 * half, kh);
                 }
-            }
-            // V: task i = (row r, half h, fp16 chunk fc) -> the 8 codes of dims
-            // 64h + 8fc .. + 7 as one 16-byte fp16 chunk (zero past the
-            // tile's end); 8 lanes cover a 128-byte half-row.  All loads first.
-            unsigned char *vd = smem + kVOff + cv * kVBytes;
-            constexpr int kVTasks = kTile * 16 / kSoftThreads;  // 15 a thread
-            uint2 vx[kVTasks];
+                // V: task i = (row r, half h, fp16 chunk fc) -> the 8 codes of dims
+                // 64h + 8fc .. + 7 as one 16-byte fp16 chunk (zero past the
+                // tile's end); 8 lanes cover a 128-byte half-row.  All loads first.
+                uint2 vx[kVTasks];
 #pragma unroll
-            for (int k = 0; k < kVTasks; ++k) {
-                const int i = ct + k * kSoftThreads;
-                const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
-                const int c16 = h * 4 + (fc >> 1);  // raw 16-byte chunk, swizzled
-                vx[k] = r < d.n ? *reinterpret_cast<const uint2 *>(rv + r * kD + ((c16 ^ (r & 7)) << 4) + (fc & 1) * 8)
-                                : make_uint2(0u, 0u);
-            }
+                for (int k = 0; k < kVTasks; ++k) {
+                    const int i = ct + k * kSoftThreads;
+                    const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
+                    const int c16 = h * 4 + (fc >> 1);  // raw 16-byte chunk, swizzled
+                    vx[k] = r < d.n ? *reinterpret_cast<const uint2 *>(rv + r * kD + ((c16 ^ (r & 7)) << 4) + (fc & 1) * 8)
+                                    : make_uint2(0u, 0u);
+                }
 #pragma unroll
-            for (int k = 0; k < kVTasks; ++k) {
-                const int i = ct + k * kSoftThreads;
-                const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
-                uint32_t f[4];
-                e4m3x4_to_f16(vx[k].x, f[0], f[1]);
-                e4m3x4_to_f16(vx[k].y, f[2], f[3]);
-                *reinterpret_cast<uint4 *>(vd + h * kHalf + r * 128 + ((fc ^ (r & 7)) << 4)) =
-                    make_uint4(f[0], f[1], f[2], f[3]);
+                for (int k = 0; k < kVTasks; ++k) {
+                    const int i = ct + k * kSoftThreads;
+                    const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
+                    uint32_t f[4];
+                    e4m3x4_to_f16(vx[k].x, f[0], f[1]);
+                    e4m3x4_to_f16(vx[k].y, f[2], f[3]);
+                    *reinterpret_cast<uint4 *>(vd + h * kHalf + r * 128 + ((fc ^ (r & 7)) << 4)) =
+                        make_uint4(f[0], f[1], f[2], f[3]);
+                }
+            } else {
+                const unsigned char *rv = rk + RC::kCodes;
+                const unsigned char *rks = rk + 2 * RC::kCodes;
+                const unsigned char *rvs = rks + RC::kScales;
+                // K row ct into TMEM lane ct: 64 code bytes (half of swizzled
+                // raw row ct / 2) and 8 block scales -> 64 fp16 pairs
+                {
+                    const int y = ct >> 1, hf = ct & 1;
+                    uint32_t kr[16];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(rk + y * 128 + (((4 * hf + c) ^ (y & 7)) << 4));
+                        kr[4 * c + 0] = x.x;
+                        kr[4 * c + 1] = x.y;
+                        kr[4 * c + 2] = x.z;
+                        kr[4 * c + 3] = x.w;
+                    }
+                    const uint2 sc = *reinterpret_cast<const uint2 *>(rks + (ct >> 4) * 128 + (ct & 15) * 8);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t kh[32];
+#pragma unroll
+                        for (int b4 = 0; b4 < 4; ++b4) {
+                            // block b = 4 * half + b4: 16 elements = words 2b, 2b + 1
+                            const int blk = 4 * half + b4;
+                            const uint32_t s2 = e4m3_scale2(((blk < 4 ? sc.x : sc.y) >> (8 * (blk & 3))) & 0xffu);
+                            uint32_t d0[4], d1[4];
+                            e2m1x8_scaled(kr[2 * blk], s2, d0);
+                            e2m1x8_scaled(kr[2 * blk + 1], s2, d1);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                kh[8 * b4 + i] = d0[i];
+                                kh[8 * b4 + 4 + i] = d1[i];
+                            }
+                        }
+                        tc::tmem_st32(k_tm + 32 * half, kh);
+                    }
+                }
+                // V: task i = (row r, half h, fp16 chunk fc) -> the 8 elements of
+                // dims 64h + 8fc .. + 7 (4 code bytes, block 4h + fc / 2) as one
+                // 16-byte fp16 chunk (zero past the tile's end).  All loads first.
+                uint32_t vx[kVTasks], vs[kVTasks];
+#pragma unroll
+                for (int k = 0; k < kVTasks; ++k) {
+                    const int i = ct + k * kSoftThreads;
+                    const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
+                    const int y = r >> 1;
+                    const int lb = 64 * (r & 1) + 32 * h + 4 * fc;  // byte in the 128-byte raw row
+                    vx[k] = r < d.n ? *reinterpret_cast<const uint32_t *>(rv + y * 128 + (((lb >> 4) ^ (y & 7)) << 4) +
+                                                                          (lb & 15))
+                                    : 0u;
+                    // (a row past the tile's end is written as zero: its block
+                    // scale may be anything, NaN included)
+                    vs[k] = r < d.n ? rvs[(r >> 4) * 128 + (r & 15) * 8 + 4 * h + (fc >> 1)] : 0u;
+                }
+#pragma unroll
+                for (int k = 0; k < kVTasks; ++k) {
+                    const int i = ct + k * kSoftThreads;
+                    const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
+                    uint32_t f[4];
+                    e2m1x8_scaled(vx[k], e4m3_scale2(vs[k]), f);
+                    *reinterpret_cast<uint4 *>(vd + h * kHalf + r * 128 + ((fc ^ (r & 7)) << 4)) =
+                        make_uint4(f[0], f[1], f[2], f[3]);
+                }
             }
             tc::tmem_wait_st();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -677,10 +799,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
     }
 }
 
-template <int G, typename OUT>
+template <int G, typename OUT, bool NV4>
 cudaError_t launch_typed(const DecodeLaunch &a, const Fp8Params &p)
 {
-    auto kern = decode_fp8_tc_kernel<G, OUT>;
+    auto kern = decode_fp8_tc_kernel<G, OUT, NV4>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess)
         return e;
@@ -693,7 +815,7 @@ cudaError_t launch_typed(const DecodeLaunch &a, const Fp8Params &p)
 bool decode_fp8_tc_eligible(const DecodeLaunch &a)
 {
     const int G = a.Hq / a.Hkv;
-    return a.kv_fp8 && a.D == kD && (G == 2 || G == 4) && !a.block_table && a.pi_period == 0;
+    return (a.kv_fp8 || a.kv_nvfp4) && a.D == kD && (G == 2 || G == 4) && !a.block_table && a.pi_period == 0;
 }
 
 cudaError_t launch_decode_fp8_tc(const DecodeLaunch &a)
@@ -728,19 +850,43 @@ cudaError_t launch_decode_fp8_tc(const DecodeLaunch &a)
     p.part_o = a.part_o;
     p.k_scale = a.k_scale;
     p.v_scale = a.v_scale;
-    // K, V codes [B, Hkv, S, D] as (D, S, B*Hkv), one byte each, box 128 x 128,
-    // 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r % 8))
     const uint64_t units = (uint64_t)a.B * a.Hkv;
-    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.S, units};
-    const uint64_t strides[2] = {(uint64_t)kD, (uint64_t)a.S * kD};
-    const uint32_t box[3] = {(uint32_t)kD, (uint32_t)kTile, 1};
-    if (!encode_tmap_3d_u8(&p.kmap, a.k, dims, strides, box, true) ||
-        !encode_tmap_3d_u8(&p.vmap, a.v, dims, strides, box, true))
-        return cudaErrorInvalidValue;
+    if (!a.kv_nvfp4) {
+        // K, V codes [B, Hkv, S, D] as (D, S, B*Hkv), one byte each, box 128 x
+        // 128, 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r % 8))
+        const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.S, units};
+        const uint64_t strides[2] = {(uint64_t)kD, (uint64_t)a.S * kD};
+        const uint32_t box[3] = {(uint32_t)kD, (uint32_t)kTile, 1};
+        if (!encode_tmap_3d_u8(&p.kmap, a.k, dims, strides, box, true) ||
+            !encode_tmap_3d_u8(&p.vmap, a.v, dims, strides, box, true))
+            return cudaErrorInvalidValue;
+        p.ksmap = p.vsmap = p.kmap;  // unused
+    } else {
+        // NVFP4 codes [B, Hkv, S, D/2] as (128 bytes, S/2, B*Hkv): two keys a
+        // row, box 64 rows (128 keys), 128-byte swizzle; block scales [B, Hkv,
+        // S, D/16] as (128 bytes, S/16, B*Hkv), box 8 rows (128 keys).  S is a
+        // multiple of 16 (checked by the entry point).
+        const uint64_t cdims[3] = {128, (uint64_t)a.S / 2, units};
+        const uint64_t cstr[2] = {128, (uint64_t)a.S * (kD / 2)};
+        const uint32_t cbox[3] = {128, (uint32_t)kTile / 2, 1};
+        const uint64_t sdims[3] = {128, (uint64_t)a.S / 16, units};
+        const uint64_t sstr[2] = {128, (uint64_t)a.S * (kD / 16)};
+        const uint32_t sbox[3] = {128, (uint32_t)kTile / 16, 1};
+        if (!encode_tmap_3d_u8(&p.kmap, a.k, cdims, cstr, cbox, true) ||
+            !encode_tmap_3d_u8(&p.vmap, a.v, cdims, cstr, cbox, true) ||
+            !encode_tmap_3d_u8(&p.ksmap, a.k_bs, sdims, sstr, sbox, false) ||
+            !encode_tmap_3d_u8(&p.vsmap, a.v_bs, sdims, sstr, sbox, false))
+            return cudaErrorInvalidValue;
+    }
     const bool bf16_out = a.out_dtype == TA_BF16;
+    if (a.kv_nvfp4) {
+        if (G == 2)
+            return bf16_out ? launch_typed<2, __nv_bfloat16, true>(a, p) : launch_typed<2, float, true>(a, p);
+        return bf16_out ? launch_typed<4, __nv_bfloat16, true>(a, p) : launch_typed<4, float, true>(a, p);
+    }
     if (G == 2)
-        return bf16_out ? launch_typed<2, __nv_bfloat16>(a, p) : launch_typed<2, float>(a, p);
-    return bf16_out ? launch_typed<4, __nv_bfloat16>(a, p) : launch_typed<4, float>(a, p);
+        return bf16_out ? launch_typed<2, __nv_bfloat16, false>(a, p) : launch_typed<2, float, false>(a, p);
+    return bf16_out ? launch_typed<4, __nv_bfloat16, false>(a, p) : launch_typed<4, float, false>(a, p);
 }
 
 }  // namespace ta

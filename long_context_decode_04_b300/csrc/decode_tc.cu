@@ -752,7 +752,7 @@ bool decode_tc_eligible(const DecodeLaunch &a)
     const bool tiles_aligned = a.plan.n_split == 1 || a.plan.chunk % kTile == 0;
     const bool pages_ok = !a.block_table || (tiles_aligned && ((a.page_size % 128 == 0) ||
                           (a.page_size >= 8 && a.page_size <= 64 && 128 % a.page_size == 0)));
-    return a.D == kD && (G == 2 || G == 4) && a.in_dtype == TA_BF16 && !a.kv_fp8 && pages_ok;
+    return a.D == kD && (G == 2 || G == 4) && a.in_dtype == TA_BF16 && !a.kv_fp8 && !a.kv_nvfp4 && pages_ok;
 }
 
 cudaError_t launch_decode_tc(const DecodeLaunch &a)

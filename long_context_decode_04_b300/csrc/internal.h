@@ -51,6 +51,8 @@ struct DecodeLaunch {
     int pi_window, pi_period;          // pi-Attention key set (period 0: every key)
     bool kv_fp8;                       // K/V are e4m3 bytes (q bf16), dequantised by
     const float *k_scale, *v_scale;    //   per (sequence, KV head) factors
+    bool kv_nvfp4;                     // K/V are NVFP4 codes [.., D/2] with E4M3 block
+    const void *k_bs, *v_bs;           //   scales [.., D/16] (factors as for E4M3)
     uint64_t wait_ns;                  // time limit of a pipeline wait (ns)
     int test_stall;                    // test hook (ta_test_stall_next_launches)
     cudaStream_t stream;

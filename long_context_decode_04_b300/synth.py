@@ -212,3 +212,41 @@ def to_e4m3(x: torch.Tensor):
     sc = (amax / 448.0).to(torch.float32)
     bits = (xf / sc.view(B, Hkv, 1, 1)).to(torch.float8_e4m3fn).view(torch.uint8)
     return bits.contiguous(), sc.reshape(-1).contiguous()
+
+
+_E2M1_MAGS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _e2m1_codes(y: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 code of each value (ties to the even code, magnitudes above
+    6 saturate to 6): sign in bit 3, magnitude index in bits 0-2."""
+    a = np.minimum(np.abs(y), 6.0)
+    idx = np.searchsorted(_E2M1_MAGS, a)            # first magnitude >= a
+    idx = np.clip(idx, 1, 7)
+    lo, hi = _E2M1_MAGS[idx - 1], _E2M1_MAGS[idx]
+    pick_hi = (a - lo > hi - a) | ((a - lo == hi - a) & (idx % 2 == 0))
+    code = np.where(pick_hi, idx, idx - 1)
+    code = np.where(a == 0, 0, code)
+    return (code | np.where(y < 0, 8, 0)).astype(np.uint8)
+
+
+def to_nvfp4(x: torch.Tensor):
+    """Quantise K or V [B, Hkv, S, D] to NVFP4: one fp32 factor per (sequence,
+    KV head) = max|x| / (6 * 448), one E4M3 scale per 16 consecutive elements
+    of a row = RNE of (block max|x| / 6) / factor (torch's float8_e4m3fn
+    cast), elements = nearest E2M1 of x / (scale * factor).  Returns (codes
+    [B, Hkv, S, D/2] uint8 with element 2i in the low nibble, scales [B, Hkv,
+    S, D/16] uint8, factors [B*Hkv] float32).  Input generation only."""
+    B, Hkv, S, D = x.shape
+    xf = x.float()
+    amax = xf.abs().amax(dim=(2, 3)).clamp_min(1e-30)
+    fac = (amax / (6.0 * 448.0)).to(torch.float32)
+    blocks = xf.reshape(B, Hkv, S, D // 16, 16)
+    bmax = blocks.abs().amax(dim=-1)
+    sc = (bmax / 6.0 / fac.view(B, Hkv, 1, 1)).to(torch.float8_e4m3fn)
+    sc_val = sc.float().clamp_min(2.0 ** -9)  # a zero scale only occurs for an all-zero block
+    y = (blocks / (sc_val.unsqueeze(-1) * fac.view(B, Hkv, 1, 1, 1))).reshape(B, Hkv, S, D).numpy()
+    codes = _e2m1_codes(y)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    return (torch.from_numpy(np.ascontiguousarray(packed)), sc.view(torch.uint8).contiguous(),
+            fac.reshape(-1).contiguous())

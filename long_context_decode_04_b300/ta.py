@@ -85,6 +85,7 @@ def lib() -> ctypes.CDLL:
         L.ta_decode_paged.argtypes = [ctypes.POINTER(PagedDecodeParams)]
         L.ta_decode_pi.argtypes = [ctypes.POINTER(DecodeParams), i, i]
         L.ta_decode_fp8.argtypes = [ctypes.POINTER(DecodeParams), vp, vp]
+        L.ta_decode_nvfp4.argtypes = [ctypes.POINTER(DecodeParams), vp, vp, vp, vp]
         L.ta_decode_pi_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i, i]
         L.ta_decode_pi_workspace_bytes.restype = st
         L.ta_decode_partials.argtypes = [ctypes.POINTER(DecodeParams), vp, vp, vp]
@@ -108,7 +109,8 @@ def lib() -> ctypes.CDLL:
         L.ta_last_error.restype = ctypes.c_char_p
         for fn in ("ta_decode", "ta_decode_noalloc", "ta_decode_ex", "ta_decode_paged", "ta_decode_pi", "ta_decode_fp8",
                    "ta_prefill_causal_varlen", "ta_decode_partials", "ta_decode_plan_for", "ta_decode_status", "ta_combine",
-                   "ta_prefill_causal", "ta_prefill_causal_ex", "ta_decode_noalloc_setup", "ta_decode_noalloc_status"):
+                   "ta_prefill_causal", "ta_prefill_causal_ex", "ta_decode_noalloc_setup", "ta_decode_noalloc_status",
+                   "ta_decode_nvfp4"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -218,6 +220,25 @@ def decode_fp8(q, k8, v8, *, k_scale=None, v_scale=None, seqlens=None, scale=Non
     p = _params(q, k8, v8, seqlens, scale, chunk, n_split, workspace, out=out, lse=lse, out_dtype=out.dtype,
                 wait_limit_ns=wait_limit_ns)
     _check(lib().ta_decode_fp8(ctypes.byref(p), _ptr(k_scale), _ptr(v_scale)))
+    return out, lse
+
+
+def decode_nvfp4(q, k4, v4, k_bs, v_bs, *, k_factor=None, v_factor=None, seqlens=None, scale=None, out_dtype=None,
+                 chunk=0, n_split=0, workspace=None, out=None, lse=None, wait_limit_ns=0):
+    """Decode over an NVFP4 KV cache.  q [B,Hq,D] bf16; k4/v4 [B,Hkv,S,D/2] uint8
+    (E2M1 codes, even element in the low nibble); k_bs/v_bs [B,Hkv,S,D/16] uint8
+    (E4M3 block scales); k_factor/v_factor [B*Hkv] fp32 or None.  Returns (out,
+    lse)."""
+    B, Hq, D = q.shape
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    p = _params(q, k4, v4, seqlens, scale, chunk, n_split, workspace, out=out, lse=lse, out_dtype=out.dtype,
+                wait_limit_ns=wait_limit_ns)
+    p.D = D  # the code tensors' last dimension is D/2
+    _check(lib().ta_decode_nvfp4(ctypes.byref(p), _ptr(k_bs), _ptr(v_bs), _ptr(k_factor), _ptr(v_factor)))
     return out, lse
 
 

@@ -261,3 +261,46 @@ def decode_fp8(q, k8, v8, k_scale, v_scale, scale, seqlens=None, rows=None, thre
     vd = e4m3_to_float(vb) * vs.reshape(B, Hkv, 1, 1)
     return decode(q, np.ascontiguousarray(kd), np.ascontiguousarray(vd), scale, seqlens=seqlens, rows=rows,
                   threads=threads)
+
+
+def e2m1_to_float(codes):
+    """Values of FP4 E2M1 codes (the low 4 bits of each entry): sign, 2
+    exponent bits with bias 1, 1 mantissa bit; exponent 0 is subnormal
+    (m/2); no infinity or NaN (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6).
+    Written from the format definition."""
+    c = np.asarray(codes).astype(np.int64) & 15
+    s = (c >> 3) & 1
+    e = (c >> 1) & 3
+    m = c & 1
+    mag = np.where(e == 0, m / 2.0, (1.0 + m / 2.0) * np.exp2(e - 1.0))
+    return np.where(s == 1, -mag, mag)
+
+
+def nvfp4_dequantize(codes, block_scales, factor):
+    """NVFP4 values in float64: codes [..., D/2] uint8 holding element 2i in
+    the low nibble and element 2i + 1 in the high nibble (E2M1), block_scales
+    [..., D/16] uint8 E4M3, one per 16 consecutive elements, and `factor` an
+    fp32 array broadcastable to the leading dimensions.  value = e2m1 *
+    e4m3(block scale) * factor (exact in float64)."""
+    c = np.asarray(codes.cpu().numpy() if hasattr(codes, "cpu") else codes, dtype=np.uint8)
+    bs = np.asarray(block_scales.cpu().numpy() if hasattr(block_scales, "cpu") else block_scales, dtype=np.uint8)
+    lo = e2m1_to_float(c & 15)
+    hi = e2m1_to_float(c >> 4)
+    vals = np.stack([lo, hi], axis=-1).reshape(*c.shape[:-1], 2 * c.shape[-1])
+    vals = vals * np.repeat(e4m3_to_float(bs), 16, axis=-1)
+    return vals * np.asarray(factor, dtype=np.float64)
+
+
+def decode_nvfp4(q, k4, k_bs, v4, v_bs, k_factor, v_factor, scale, seqlens=None, rows=None, threads=None):
+    """Decode over an NVFP4 KV cache: K and V are dequantised first
+    (``nvfp4_dequantize`` with the (sequence, KV head) factors; None = 1) and
+    ``decode`` does the rest.  k4/v4 [B,Hkv,S,D/2] uint8, k_bs/v_bs
+    [B,Hkv,S,D/16] uint8, k_factor/v_factor [B*Hkv]."""
+    kb = np.asarray(k4.cpu().numpy() if hasattr(k4, "cpu") else k4, dtype=np.uint8)
+    B, Hkv = kb.shape[:2]
+    kf = np.ones(B * Hkv) if k_factor is None else np.asarray(k_factor, dtype=np.float64).reshape(-1)
+    vf = np.ones(B * Hkv) if v_factor is None else np.asarray(v_factor, dtype=np.float64).reshape(-1)
+    kd = nvfp4_dequantize(kb, k_bs, kf.reshape(B, Hkv, 1, 1))
+    vd = nvfp4_dequantize(v4, v_bs, vf.reshape(B, Hkv, 1, 1))
+    return decode(q, np.ascontiguousarray(kd), np.ascontiguousarray(vd), scale, seqlens=seqlens, rows=rows,
+                  threads=threads)

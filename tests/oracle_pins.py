@@ -594,4 +594,72 @@ def pin_fp8_scales_are_linear():
     assert np.max(np.abs(3.0 * a[0] - b_[0])) < 1e-12 and np.max(np.abs(a[1] - b_[1])) < 1e-12
 
 
+# ------------------------------------------------------------ NVFP4 KV cache
+
+def pin_e2m1_values_match_the_format_table():
+    """The 16 E2M1 codes: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 for codes 0-7
+    (the FP4 E2M1 element table of the microscaling formats), the same with
+    the sign bit (code + 8) negative."""
+    table = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    mine = oracle.e2m1_to_float(np.arange(16))
+    assert np.array_equal(mine[:8], table) and np.array_equal(mine[8:], -table)
+    assert np.array_equal(oracle.e2m1_to_float(np.arange(16) + 16 * 5), mine)  # only the low 4 bits count
+
+
+def pin_nvfp4_block_scale_covers_16_elements():
+    """A block scale multiplies exactly its 16 consecutive elements, and the
+    low nibble of a byte is the even element: codes 0x42 (elements 1.0, 2.0)
+    everywhere, block scales 1.0 (0x38) except block 5 (2.0, 0x40)."""
+    codes = np.full((1, 1, 3, 64), 0x42, dtype=np.uint8)
+    bs = np.full((1, 1, 3, 8), 0x38, dtype=np.uint8)
+    bs[0, 0, 1, 5] = 0x40
+    vals = oracle.nvfp4_dequantize(codes, bs, np.full((1, 1, 1, 1), 0.5))
+    expect = np.tile(np.array([0.5, 1.0]), 64).reshape(1, 1, 1, 128).repeat(3, axis=2)
+    expect[0, 0, 1, 80:96] *= 2.0
+    assert np.array_equal(vals, expect)
+
+
+def pin_nvfp4_brute_force():
+    """NVFP4 decode against 50-digit attention over keys and values dequantised
+    element by element: element d of a key is the E2M1 value of nibble d % 2 of
+    byte d // 2 (sign * 2^(e-1) * (1 + m/2), or m/2 when e = 0), times the E4M3
+    scale of block d // 16, times the (sequence, KV head) factor."""
+    rng = _rng(73)
+    B, Hkv, G, S, D = 2, 2, 2, 7, 32
+    k4 = rng.integers(0, 256, size=(B, Hkv, S, D // 2)).astype(np.uint8)
+    v4 = rng.integers(0, 256, size=(B, Hkv, S, D // 2)).astype(np.uint8)
+    kbs = rng.integers(0x20, 0x40, size=(B, Hkv, S, D // 16)).astype(np.uint8)   # scales 2^-3 .. 2^0
+    vbs = rng.integers(0x30, 0x50, size=(B, Hkv, S, D // 16)).astype(np.uint8)
+    kf = rng.uniform(0.05, 0.2, B * Hkv)
+    vf = rng.uniform(0.5, 2.0, B * Hkv)
+    q = _f32(rng, B, Hkv * G, D)
+
+    def e2m1(n):
+        sgn = -1 if n & 8 else 1
+        e, m = (n >> 1) & 3, n & 1
+        return sgn * (mpmath.mpf(m) / 2 if e == 0 else (1 + mpmath.mpf(m) / 2) * mpmath.mpf(2) ** (e - 1))
+
+    def e4m3(bt):
+        e, m = (int(bt) >> 3) & 15, int(bt) & 7
+        return mpmath.mpf(m) / 8 * mpmath.mpf(2) ** -6 if e == 0 else (1 + mpmath.mpf(m) / 8) * mpmath.mpf(2) ** (e - 7)
+
+    def row(codes, scales, fac):
+        out = []
+        for d in range(D):
+            byte = int(codes[d // 2])
+            nib = byte & 15 if d % 2 == 0 else byte >> 4
+            out.append(float(e2m1(nib) * e4m3(scales[d // 16]) * mpmath.mpf(float(fac))))
+        return out
+
+    out, lse = oracle.decode_nvfp4(q, k4, kbs, v4, vbs, kf, vf, 0.9)
+    for b in range(B):
+        for h in range(Hkv * G):
+            u = b * Hkv + h // G
+            kk = np.array([row(k4[b, h // G, j], kbs[b, h // G, j], kf[u]) for j in range(S)])
+            vv = np.array([row(v4[b, h // G, j], vbs[b, h // G, j], vf[u]) for j in range(S)])
+            ref, ref_lse = _mp_attend(q[b, h], kk, vv, 0.9)
+            assert np.max(np.abs(out[b * Hkv * G + h] - np.array(ref))) < 1e-12 * max(1.0, float(np.max(np.abs(vv))))
+            assert abs(lse[b * Hkv * G + h] - ref_lse) < 1e-12
+
+
 ALL_PINS = [f for name, f in sorted(globals().items()) if name.startswith("pin_") and callable(f)]

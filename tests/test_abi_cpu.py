@@ -263,3 +263,20 @@ def test_launch_failure_hook_refuses_launches_after_validation():
     assert b"ta_test_fail_next_launches" not in L.ta_last_error()
     assert L.ta_test_fail_next_launches(5) == 0
     assert L.ta_test_fail_next_launches(0) == 5  # cancelled with 5 pending
+
+
+def test_nvfp4_decode_rejects_bad_arguments():
+    base = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, B=1, Hq=8, Hkv=2, S=64, D=128,
+                scale=0.1, in_dtype=ta.TA_BF16, out_dtype=ta.TA_BF16)
+    L = ta.lib()
+    vp = ctypes.c_void_p
+    p = ta.DecodeParams(**base)
+    assert L.ta_decode_nvfp4(ctypes.byref(p), None, vp(0x6000), None, None) == ta.TA_ERR_INVALID_ARG
+    assert L.ta_decode_nvfp4(ctypes.byref(p), vp(0x6008), vp(0x6000), None, None) == ta.TA_ERR_INVALID_ARG
+    assert L.ta_decode_nvfp4(ctypes.byref(p), vp(0x6000), vp(0x7000), vp(0x8002), None) == ta.TA_ERR_INVALID_ARG
+    p = ta.DecodeParams(**dict(base, Hq=2))  # one query head per KV head
+    assert L.ta_decode_nvfp4(ctypes.byref(p), vp(0x6000), vp(0x7000), None, None) == ta.TA_ERR_UNSUPPORTED
+    p = ta.DecodeParams(**dict(base, S=70))  # S not a multiple of 16
+    assert L.ta_decode_nvfp4(ctypes.byref(p), vp(0x6000), vp(0x7000), None, None) == ta.TA_ERR_UNSUPPORTED
+    p = ta.DecodeParams(**dict(base, in_dtype=ta.TA_F32, out_dtype=ta.TA_F32))
+    assert L.ta_decode_nvfp4(ctypes.byref(p), vp(0x6000), vp(0x7000), None, None) == ta.TA_ERR_INVALID_ARG

@@ -175,6 +175,14 @@ def test_varlen_prefill_mutation_is_caught(monkeypatch, name):
 
 
 FP8_MUTATIONS = {
+    ("e2m1_to_float", "bias_2"): ("np.exp2(e - 1.0)", "np.exp2(e - 2.0)"),
+    ("e2m1_to_float", "subnormal_as_normal"): ("np.where(e == 0, m / 2.0,", "np.where(e == 0, (1.0 + m / 2.0) * 0.5,"),
+    ("nvfp4_dequantize", "nibbles_swapped"): ("np.stack([lo, hi], axis=-1)", "np.stack([hi, lo], axis=-1)"),
+    ("nvfp4_dequantize", "block_of_32"): ("np.repeat(e4m3_to_float(bs), 16, axis=-1)",
+                                          "np.repeat(e4m3_to_float(bs[..., ::2]), 32, axis=-1)"),
+    ("nvfp4_dequantize", "block_scale_dropped"): ("vals = vals * np.repeat(e4m3_to_float(bs), 16, axis=-1)", "pass"),
+    ("decode_nvfp4", "v_factor_dropped"): ("vd = nvfp4_dequantize(v4, v_bs, vf.reshape(B, Hkv, 1, 1))",
+                                           "vd = nvfp4_dequantize(v4, v_bs, 1.0)"),
     ("e4m3_to_float", "bias_8"): ("np.exp2(e - 7.0)", "np.exp2(e - 8.0)"),
     ("e4m3_to_float", "subnormal_as_normal"): ("m / 8.0 * 2.0 ** -6", "(1.0 + m / 8.0) * 2.0 ** -7"),
     ("e4m3_to_float", "sign_ignored"): ("return np.where(s == 1, -mag, mag)", "return mag"),
