@@ -463,6 +463,7 @@ def run_launches(which, n):
     """A few plain launches of one workload and nothing else (no timing, no
     JSON): the command the ncu captures in profiles/ run.  `which` is one of
     decode (the 128K-token GQA decode), fp8 (the same over an E4M3 cache),
+    nvfp4 (the same over an NVFP4 cache),
     paged (the 16-sequence variable-length decode in 64-key pages), prefill
     (the 16K-token causal prefill)."""
     import torch
@@ -490,6 +491,10 @@ def run_launches(which, n):
             v8, vs = synth.to_e4m3(x["v"])
             k8, ks, v8, vs = k8.to(dev), ks.to(dev), v8.to(dev), vs.to(dev)
             fn = lambda: ta.decode_fp8(q, k8, v8, k_scale=ks, v_scale=vs, scale=w.scale)
+        elif which == "nvfp4":
+            k4, kbs, kf = (t.to(dev) for t in synth.to_nvfp4(x["k"]))
+            v4, vbs, vf = (t.to(dev) for t in synth.to_nvfp4(x["v"]))
+            fn = lambda: ta.decode_nvfp4(q, k4, v4, kbs, vbs, k_factor=kf, v_factor=vf, scale=w.scale)
         else:
             k, v = x["k"].to(dev), x["v"].to(dev)
             fn = lambda: ta.decode(q, k, v, scale=w.scale)
@@ -508,7 +513,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-extra", action="store_true", help="skip the variable-length / paged decode figures")
-    ap.add_argument("--launches", choices=["decode", "fp8", "paged", "prefill"],
+    ap.add_argument("--launches", choices=["decode", "fp8", "nvfp4", "paged", "prefill"],
                     help="only make --steps plain launches of one workload (for profilers); prints nothing")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

@@ -68,7 +68,8 @@ enum {
                                (its first 16 KiB, or all of a smaller workspace) before it is
                                used again; ta_decode_status does this for the library's own
                                workspace. */
-    TA_DEVERR_RANGE = 4,    /* prefill: some |V| > 65280 (outside fp16); output undefined */
+    TA_DEVERR_RANGE = 4,    /* prefill: some |V| > 65280; FP8 / NVFP4 decode: some |q| > 65280
+                               (outside fp16); output undefined */
     TA_DEVERR_PAGE = 8      /* paged decode: a block-table entry outside [0, num_pages); output undefined */
 };
 
@@ -215,7 +216,9 @@ ta_status ta_decode_ex(const ta_decode_params *p);
  *   1 when the pointer is NULL.  q bf16 (p->in_dtype = TA_BF16), output
  *   bf16 or fp32, fp32 accumulation.  Everything else as ta_decode_ex.
  *   Supported: D = 128, G in {1, 2, 4}.  Queries are used as f16 values
- *   (exact for bf16 values of magnitude in [2^-14, 65504]).
+ *   (exact for bf16 values of magnitude in [2^-17, 65280] and zero; below
+ *   2^-17 they lose low bits, above 65280 they do not fit, and such a query
+ *   records TA_DEVERR_RANGE in the status word, output undefined).
  */
 ta_status ta_decode_fp8(const ta_decode_params *p, const float *k_scale, const float *v_scale);
 
@@ -232,8 +235,9 @@ ta_status ta_decode_fp8(const ta_decode_params *p, const float *k_scale, const f
  *   the device, or NULL (1).  The value of element d of key j of (b, kv head)
  *   is e2m1 * e4m3(block d / 16) * factor[b * Hkv + kv head].
  *   q bf16 (p->in_dtype = TA_BF16), output bf16 or fp32, fp32 accumulation;
- *   every element is widened exactly to fp16 on chip.  Everything else as
- *   ta_decode_ex.
+ *   every element is widened exactly to fp16 on chip, and so is q (as for
+ *   ta_decode_fp8, a query element of magnitude above 65280 records
+ *   TA_DEVERR_RANGE).  Everything else as ta_decode_ex.
  *   Supported: D = 128, G in {2, 4}, S a multiple of 16, chunks of whole
  *   128-key tiles (the default plan; chunk overrides that are multiples of
  *   128).  k, v, k_block_scales, v_block_scales 16-byte aligned.

@@ -185,6 +185,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// True when either bf16 of the pair is finite and of magnitude at least 2^16
+// (biased exponent 143 .. 254), which fp16 cannot hold (its largest finite
+// value is 65504; the bf16 value below 2^16 is 65280).
+__device__ __forceinline__ bool bf16x2_beyond_f16(uint32_t w)
+{
+    const uint32_t elo = (w >> 7) & 0xffu, ehi = (w >> 23) & 0xffu;
+    return (elo >= 143u && elo != 255u) || (ehi >= 143u && ehi != 255u);
+}
+
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 

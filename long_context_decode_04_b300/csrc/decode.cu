@@ -611,6 +611,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
                                 uint32_t hv;
                                 asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hv) : "f"(bf16_hi(wv[w])), "f"(bf16_lo(wv[w])));
                                 qw[h][8 * i + 4 * u + w] = hv;
+                                // a query outside the fp16 range: its scores are not the exact ones
+                                if (bf16x2_beyond_f16(wv[w]))
+                                    atomicOr(&p.status[0], TA_DEVERR_RANGE);
                             }
                         }
                     }

@@ -23,8 +23,9 @@
 //                                            (MN-major, 128-byte swizzle),
 //                                            B = P, one row per (softmax
 //                                            warp, head), hi then lo parts
-// Queries are used as fp16 values (exact for bf16 values of magnitude in
-// [2^-14, 65504]).
+// Queries are used as fp16 values: exact for bf16 values of magnitude in
+// [2^-17, 65280] (and zero); one of magnitude 2^16 or more does not fit,
+// and the producer records TA_DEVERR_RANGE.
 //
 // Kernel layout (one persistent CTA per SM, 12 warps):
 //   * warp 0: producer.  Work items (sequence, KV head, chunk) from the
@@ -32,7 +33,8 @@
 //     two Q buffers; raw K and V tiles (128 rows of 128 codes) by TMA into a
 //     3-stage ring.
 //   * warp 1: TMEM (512 columns: S and O double buffers, three K buffers)
-//     and the score products; warp 2: the value products.
+//     and the score products; warp 2: the value products; warp 3 (fused
+//     mode): the ticket thread of the merge.
 //   * warps 4-7: softmax and accumulation, as in decode_tc.cu (each warp its
 //     own online softmax over its 32 keys, per-warp references raised
 //     lazily, the four warps merged at the item end).
@@ -140,7 +142,7 @@ static_assert(Raw<false>::kStages * Raw<false>::kStage <= kRawRegion && Raw<true
               "raw rings");
 static_assert(Raw<false>::kKBytes % 1024 == 0 && Raw<true>::kCodes % 1024 == 0 && Raw<true>::kStage % 1024 == 0 &&
                   kRawOff % 1024 == 0, "raw tiles on 1024-byte boundaries (swizzle atoms)");
-static_assert(kTile * 16 % kSoftThreads == 0, "V widening tasks per thread");
+static_assert(kTile * 4 % kSoftThreads == 0, "V widening tasks per thread");
 
 struct Fp8Params {
     // E4M3: codes (D, S, B*Hkv), box 128 x 128; NVFP4: codes (128 bytes,
@@ -201,11 +203,13 @@ __device__ __forceinline__ void e2m1x8_scaled(uint32_t w, uint32_t s2, uint32_t 
         : "r"(w), "r"(s2));
 }
 
-// An E4M3 block scale (one byte) as an fp16 pair (the value twice).
-__device__ __forceinline__ uint32_t e4m3_scale2(uint32_t byte)
+// Two E4M3 block scales (the low two bytes of `two`) as two fp16 pairs,
+// each holding its value twice.
+__device__ __forceinline__ void e4m3_scales2(uint32_t two, uint32_t &s0, uint32_t &s1)
 {
-    const uint32_t h = e4m3x2_to_f16x2(byte & 0xffu) & 0xffffu;
-    return h | (h << 16);
+    const uint32_t h = e4m3x2_to_f16x2(two & 0xffffu);
+    s0 = __byte_perm(h, 0u, 0x1010);
+    s1 = __byte_perm(h, 0u, 0x3232);
 }
 
 template <int G, typename OUT, bool NV4>
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
         mbar_init(&ms->grp_bar, 4);
         mbar_init(&ms->mma_done, 2);  // both MMA issuers commit
         ms->abort = 0;
-        ms->isum.merge_unit = -1;
+        tcd::init_item_smem(&ms->isum);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -285,17 +289,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                 return false;
             unsigned char *qd = smem + kQOff + qb * kQBytes;
             const __nv_bfloat16 *qsrc = p.q + (size_t)unit * G * kD;
+            bool big = false;
             for (int i = lane; i < G * 16; i += 32) {
                 const int h = i >> 4, c = i & 15;
                 const uint4 x = *reinterpret_cast<const uint4 *>(qsrc + h * kD + c * 8);
                 const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
                 uint32_t hv[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
+                for (int k = 0; k < 4; ++k) {
                     hv[k] = tc::pack_f16x2(bf16_lo(wv[k]), bf16_hi(wv[k]));
+                    big |= bf16x2_beyond_f16(wv[k]);
+                }
                 *reinterpret_cast<uint4 *>(qd + (c >> 3) * kQHalf + h * 128 + ((((c & 7) ^ h) & 7) << 4)) =
                     make_uint4(hv[0], hv[1], hv[2], hv[3]);
             }
+            if (big)  // a query outside the fp16 range: its scores are not the exact ones
+                atomicOr(&p.status[0], TA_DEVERR_RANGE);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (leader)
@@ -522,7 +531,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
             const unsigned char *rk = smem + kRawOff + stage * RC::kStage;
             const uint32_t k_tm = tmem + lane_base + kKCol + cv * (kD / 2);
             unsigned char *vd = smem + kVOff + cv * kVBytes;
-            constexpr int kVTasks = kTile * 16 / kSoftThreads;  // 16 a thread
             if constexpr (!NV4) {
                 const unsigned char *rv = rk + RC::kKBytes;
                 // K row ct into TMEM lane ct: 128 codes -> 64 fp16 pairs (the raw
@@ -544,27 +552,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                         e4m3x4_to_f16(kr[16 * half + i], kh[2 * i], kh[2 * i + 1]);
                     tc::tmem_st32(k_tm + 32 * half, kh);
                 }
-                // V: task i = (row r, half h, fp16 chunk fc) -> the 8 codes of dims
-                // 64h + 8fc .. + 7 as one 16-byte fp16 chunk (zero past the
-                // tile's end); 8 lanes cover a 128-byte half-row.  All loads first.
-                uint2 vx[kVTasks];
+                // V: task i = (row r, quarter qq) -> the 32 codes of dims 32qq ..
+                // + 31 (raw 16-byte chunks 2qq, 2qq + 1, swizzled) as four
+                // 16-byte fp16 chunks 4 (qq & 1) .. + 3 of half qq / 2 (zero
+                // past the tile's end).  All loads first.
+                constexpr int kV4Tasks = kTile * 4 / kSoftThreads;  // 4 a thread
+                uint4 vx[kV4Tasks][2];
 #pragma unroll
-                for (int k = 0; k < kVTasks; ++k) {
+                for (int k = 0; k < kV4Tasks; ++k) {
                     const int i = ct + k * kSoftThreads;
-                    const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
-                    const int c16 = h * 4 + (fc >> 1);  // raw 16-byte chunk, swizzled
-                    vx[k] = r < d.n ? *reinterpret_cast<const uint2 *>(rv + r * kD + ((c16 ^ (r & 7)) << 4) + (fc & 1) * 8)
-                                    : make_uint2(0u, 0u);
+                    const int r = i >> 2, qq = i & 3;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        vx[k][j] = r < d.n ? *reinterpret_cast<const uint4 *>(rv + r * kD + (((2 * qq + j) ^ (r & 7)) << 4))
+                                           : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
-                for (int k = 0; k < kVTasks; ++k) {
+                for (int k = 0; k < kV4Tasks; ++k) {
                     const int i = ct + k * kSoftThreads;
-                    const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
-                    uint32_t f[4];
-                    e4m3x4_to_f16(vx[k].x, f[0], f[1]);
-                    e4m3x4_to_f16(vx[k].y, f[2], f[3]);
-                    *reinterpret_cast<uint4 *>(vd + h * kHalf + r * 128 + ((fc ^ (r & 7)) << 4)) =
-                        make_uint4(f[0], f[1], f[2], f[3]);
+                    const int r = i >> 2, qq = i & 3;
+                    unsigned char *dst = vd + (qq >> 1) * kHalf + r * 128;
+                    const int fc0 = 4 * (qq & 1);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 x = vx[k][c >> 1];
+                        const uint32_t lo = (c & 1) ? x.z : x.x, hi = (c & 1) ? x.w : x.y;
+                        uint32_t f[4];
+                        e4m3x4_to_f16(lo, f[0], f[1]);
+                        e4m3x4_to_f16(hi, f[2], f[3]);
+                        *reinterpret_cast<uint4 *>(dst + (((fc0 + c) ^ (r & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                    }
                 }
             } else {
                 const unsigned char *rv = rk + RC::kCodes;
@@ -587,14 +604,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t kh[32];
+                        uint32_t s2[4];  // blocks 4 * half .. + 3, each as an fp16 pair
+                        const uint32_t sw = half ? sc.y : sc.x;
+                        e4m3_scales2(sw, s2[0], s2[1]);
+                        e4m3_scales2(sw >> 16, s2[2], s2[3]);
 #pragma unroll
                         for (int b4 = 0; b4 < 4; ++b4) {
                             // block b = 4 * half + b4: 16 elements = words 2b, 2b + 1
                             const int blk = 4 * half + b4;
-                            const uint32_t s2 = e4m3_scale2(((blk < 4 ? sc.x : sc.y) >> (8 * (blk & 3))) & 0xffu);
                             uint32_t d0[4], d1[4];
-                            e2m1x8_scaled(kr[2 * blk], s2, d0);
-                            e2m1x8_scaled(kr[2 * blk + 1], s2, d1);
+                            e2m1x8_scaled(kr[2 * blk], s2[b4], d0);
+                            e2m1x8_scaled(kr[2 * blk + 1], s2[b4], d1);
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 kh[8 * b4 + i] = d0[i];
@@ -604,31 +624,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                         tc::tmem_st32(k_tm + 32 * half, kh);
                     }
                 }
-                // V: task i = (row r, half h, fp16 chunk fc) -> the 8 elements of
-                // dims 64h + 8fc .. + 7 (4 code bytes, block 4h + fc / 2) as one
-                // 16-byte fp16 chunk (zero past the tile's end).  All loads first.
-                uint32_t vx[kVTasks], vs[kVTasks];
+                // V: task i = (row r, quarter qq) -> the 32 elements of dims
+                // 32qq .. + 31 (16 code bytes, blocks 2qq and 2qq + 1) as four
+                // 16-byte fp16 chunks 4 (qq & 1) .. + 3 of half qq / 2 (zero
+                // past the tile's end).  All loads first.
+                constexpr int kV4Tasks = kTile * 4 / kSoftThreads;  // 4 a thread
+                uint4 vx[kV4Tasks];
+                uint32_t vs[kV4Tasks];
 #pragma unroll
-                for (int k = 0; k < kVTasks; ++k) {
+                for (int k = 0; k < kV4Tasks; ++k) {
                     const int i = ct + k * kSoftThreads;
-                    const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
+                    const int r = i >> 2, qq = i & 3;
                     const int y = r >> 1;
-                    const int lb = 64 * (r & 1) + 32 * h + 4 * fc;  // byte in the 128-byte raw row
-                    vx[k] = r < d.n ? *reinterpret_cast<const uint32_t *>(rv + y * 128 + (((lb >> 4) ^ (y & 7)) << 4) +
-                                                                          (lb & 15))
-                                    : 0u;
+                    const int c16 = 4 * (r & 1) + qq;  // 16-byte chunk of the 128-byte raw row
                     // (a row past the tile's end is written as zero: its block
-                    // scale may be anything, NaN included)
-                    vs[k] = r < d.n ? rvs[(r >> 4) * 128 + (r & 15) * 8 + 4 * h + (fc >> 1)] : 0u;
+                    // scales may be anything, NaN included)
+                    vx[k] = r < d.n ? *reinterpret_cast<const uint4 *>(rv + y * 128 + ((c16 ^ (y & 7)) << 4))
+                                    : make_uint4(0u, 0u, 0u, 0u);
+                    vs[k] = r < d.n ? *reinterpret_cast<const uint16_t *>(rvs + (r >> 4) * 128 + (r & 15) * 8 + 2 * qq)
+                                    : 0u;
                 }
 #pragma unroll
-                for (int k = 0; k < kVTasks; ++k) {
+                for (int k = 0; k < kV4Tasks; ++k) {
                     const int i = ct + k * kSoftThreads;
-                    const int r = i >> 4, h = (i >> 3) & 1, fc = i & 7;
-                    uint32_t f[4];
-                    e2m1x8_scaled(vx[k], e4m3_scale2(vs[k]), f);
-                    *reinterpret_cast<uint4 *>(vd + h * kHalf + r * 128 + ((fc ^ (r & 7)) << 4)) =
-                        make_uint4(f[0], f[1], f[2], f[3]);
+                    const int r = i >> 2, qq = i & 3;
+                    unsigned char *dst = vd + (qq >> 1) * kHalf + r * 128;
+                    const int fc0 = 4 * (qq & 1);
+                    uint32_t s0, s1;
+                    e4m3_scales2(vs[k], s0, s1);
+                    const uint32_t w[4] = {vx[k].x, vx[k].y, vx[k].z, vx[k].w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t f[4];
+                        e2m1x8_scaled(w[c], c < 2 ? s0 : s1, f);
+                        *reinterpret_cast<uint4 *>(dst + (((fc0 + c) ^ (r & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                    }
                 }
             }
             tc::tmem_wait_st();
@@ -652,7 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
         float mw[G], l_run[G], o[4][G];
         int unit = 0, split = 0, b = 0, kvh = 0;
         float qs = p.qscale;
-        const tcd::ItemOut io{p.out, p.lse, p.Hq, p.mode, p.n_split, p.part_m, p.part_l, p.part_o, p.counters};
+        const tcd::ItemOut io{p.out,     p.lse,    p.Hq,       p.mode,     p.n_split, p.part_m,
+                              p.part_l,  p.part_o, p.counters, abort_flag, p.wait_ns};
         float *const stage_area = ms->isum.stage;
         tcd::PendingTicket pt;
         bool ended = false;
@@ -787,6 +818,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
         }
         if (ended)
             tcd::finish_pending<G, OUT>(io, &ms->isum, stage_area, q4, lane, pt, group_sync);
+        if (p.mode == kModeFused)
+            tcd::end_tickets(&ms->isum, row);
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ ticket thread
+        if (lane == 0 && p.mode == kModeFused) {
+            const tcd::ItemOut io{p.out,     p.lse,    p.Hq,       p.mode,     p.n_split, p.part_m,
+                                  p.part_l,  p.part_o, p.counters, abort_flag, p.wait_ns};
+            tcd::ticket_loop(io, &ms->isum);
+        }
+        __syncwarp();
     }
 
     tc::fence_before_sync();

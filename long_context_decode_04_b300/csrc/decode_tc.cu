@@ -42,6 +42,8 @@
 //     buffer) and issues the score products; warp 2 issues the value
 //     products.  Each blocks on the one barrier it needs next, so a tile's
 //     value product never waits for the next tile's copy.
+//   * warp 3 (fused mode): the ticket thread, which takes the merge tickets
+//     the softmax warps ask for at their item ends.
 //   * warps 4-7 (one warpgroup, TMEM lane quadrants 0-3): thread r owns key
 //     row r of every tile for the softmax and output dimension r for the
 //     accumulation.  Each warp runs its own online softmax over its 32 key
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         mbar_init(&ms->grp_bar, 4);
         mbar_init(&ms->mma_done, 2);  // both MMA issuers commit
         ms->abort = 0;
-        ms->isum.merge_unit = -1;
+        tcd::init_item_smem(&ms->isum);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -565,7 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         int t = 0;
         float mw[G], l_run[G], o[4][G];
         int unit = 0, split = 0, b = 0, kvh = 0;
-        const tcd::ItemOut io{p.out, p.lse, p.Hq, p.mode, p.n_split, p.part_m, p.part_l, p.part_o, p.counters};
+        const tcd::ItemOut io{p.out,     p.lse,    p.Hq,       p.mode,     p.n_split, p.part_m,
+                              p.part_l,  p.part_o, p.counters, abort_flag, p.wait_ns};
         float *const stage_area = ms->isum.stage;
         tcd::PendingTicket pt;
         bool ended = false;
@@ -717,6 +720,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         if (ended)
             tcd::finish_pending<G, OUT>(io, &ms->isum, stage_area, q4, lane, pt, group_sync);
+        if (p.mode == kModeFused)
+            tcd::end_tickets(&ms->isum, row);
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ ticket thread
+        if (lane == 0 && p.mode == kModeFused) {
+            const tcd::ItemOut io{p.out,     p.lse,    p.Hq,       p.mode,     p.n_split, p.part_m,
+                                  p.part_l,  p.part_o, p.counters, abort_flag, p.wait_ns};
+            tcd::ticket_loop(io, &ms->isum);
+        }
+        __syncwarp();
     }
 
     tc::fence_before_sync();

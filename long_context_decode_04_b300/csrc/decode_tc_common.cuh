@@ -12,6 +12,9 @@
 // is either the result (one chunk), or written to the partials, and in
 // fused mode the CTA that writes a unit's last partial merges all of them
 // (learning that it is the last one item later, so no item waits for it).
+// Which CTA that is comes from a GPU-scope acquire-release increment of
+// the unit's counter, which stalls its thread for about a microsecond: a
+// warp of its own (the ticket thread) takes it, off the softmax warps' path.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -40,32 +43,68 @@ struct ItemOut {
     int n_split;
     float *part_m, *part_l, *part_o;  // [R, n_split], [R, n_split], [R, n_split, D]
     int32_t *counters;                // [B*Hkv] finished chunks per unit (fused mode)
+    volatile int *abort;              // the launch's give-up flag
+    uint64_t wait_ns;                 // time limit of a pipeline wait
 };
 
 template <int G>
 constexpr int stage_floats() { return 2 * G * kFusedMergeMaxSplits + 2 * G; }
 
 // Shared memory of the item end: the four warps' sums and references, the
-// decision of a deferred ticket (below), and the merge's staging area.  (The
-// staging area is its own: the weight buffers of the value product are not
-// free for it, since the entries of a warp's rows outside its own 32 keys
-// must stay zero.)
+// ticket channel to the ticket thread, the decision of a deferred ticket
+// (below), and the merge's staging area.  (The staging area is its own: the
+// weight buffers of the value product are not free for it, since the
+// entries of a warp's rows outside its own 32 keys must stay zero.)
 struct ItemSmem {
+    uint64_t tk_req;   // a ticket asked for: the 128 softmax threads, each after its partial stores
+    uint64_t tk_done;  // the ticket is taken and its result is in tk_old (the ticket thread)
     float lred[4][4];  // [warp][head] weight sums
     float mred[4][4];  // [warp][head] references
     int merge_unit;    // unit whose partials are all written (-1: none)
+    int tk_unit;       // the unit of the ticket asked for; -1: no more tickets
+    int tk_old;        // the unit counter's value before the ticket's increment
     float stage[stage_floats<4>()];
 };
 
-// A ticket taken and not yet looked at.  In fused mode the CTA that writes
-// a unit's last partial merges that unit; which CTA that is comes back from
-// a GPU-scope atomic on the unit's counter.  Thread 0 of the warpgroup
-// issues that atomic and only reads its result at the next item's end (or
-// after the last item), so no item waits for the round trip.
+// Called by one thread before the kernel's first __syncthreads.
+__device__ __forceinline__ void init_item_smem(ItemSmem *sm)
+{
+    mbar_init(&sm->tk_req, kSoftThreads);
+    mbar_init(&sm->tk_done, 1);
+    sm->merge_unit = -1;
+    sm->tk_unit = -1;
+}
+
+// A ticket asked for and not yet looked at (kept by softmax thread 0).  In
+// fused mode the CTA that writes a unit's last partial merges that unit;
+// the ticket says whether this CTA's was the last.  Its result is read at
+// the next item's end (or after the last item), so no item waits for it.
 struct PendingTicket {
-    int unit = -1;   // -1: none
-    int old = 0;     // the counter's value before this CTA's increment
+    int unit = -1;   // -1: none pending
+    uint32_t n = 0;  // tickets asked for so far (the phase of tk_done)
 };
+
+// The ticket thread (one thread of an otherwise idle warp, fused mode
+// only): for each ticket asked for, the acquire-release increment of the
+// unit's counter.  The 128 arrivals on tk_req order every softmax thread's
+// partial stores before the increment (whose release publishes them to the
+// merging CTA); its acquire, passed on through tk_done, orders the other
+// CTAs' partials before this CTA's merge reads them.  Its waits last as long
+// as an item, so they are bounded by the larger of the launch's limit and
+// the default, and end early when the launch gives up.
+__device__ __forceinline__ void ticket_loop(const ItemOut &io, ItemSmem *sm)
+{
+    const uint64_t limit = io.wait_ns > kWaitLimitNs ? io.wait_ns : kWaitLimitNs;
+    for (uint32_t n = 0;; ++n) {
+        if (!mbar_wait_bounded(&sm->tk_req, n & 1, io.abort, limit))
+            return;
+        const int u = *reinterpret_cast<volatile int *>(&sm->tk_unit);
+        if (u < 0)
+            return;
+        sm->tk_old = atomic_add_acq_rel_gpu(&io.counters[u], 1);
+        mbar_arrive(&sm->tk_done);
+    }
+}
 
 // The merge of a unit whose partials are all written: out = sum_n e^(m_n -
 // max) o_n / sum_n e^(m_n - max) l_n, lse = max + ln(that sum), over the
@@ -122,14 +161,21 @@ __device__ __forceinline__ bool merge_unit(const ItemOut &io, float *stage, int 
         const float *wh = sw + h * ns;
         const float4 *po = reinterpret_cast<const float4 *>(io.part_o + (row0 + h) * ns * kD + d4);
         float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int n = 0; n < ns; ++n) {
-            const float4 x = __ldcg(po + (size_t)n * (kD / 4));
-            const float a = wh[n];
-            os.x = fmaf(a, x.x, os.x);
-            os.y = fmaf(a, x.y, os.y);
-            os.z = fmaf(a, x.z, os.z);
-            os.w = fmaf(a, x.w, os.w);
+        // sixteen loads in flight per round (the partials come from L2)
+        constexpr int kBatch = 16;
+        for (int n0 = 0; n0 < ns; n0 += kBatch) {
+            float4 x[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                x[i] = n0 + i < ns ? __ldcg(po + (size_t)(n0 + i) * (kD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const float a = n0 + i < ns ? wh[n0 + i] : 0.f;
+                os.x = fmaf(a, x[i].x, os.x);
+                os.y = fmaf(a, x[i].y, os.y);
+                os.z = fmaf(a, x[i].z, os.z);
+                os.w = fmaf(a, x[i].w, os.w);
+            }
         }
         const float mx = shd[2 * h], lsum = shd[2 * h + 1];
         const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
@@ -147,17 +193,33 @@ __device__ __forceinline__ bool merge_unit(const ItemOut &io, float *stage, int 
 }
 
 // Thread 0 publishes the decision of its pending ticket (called before a
-// rendezvous, after which every thread reads sm->merge_unit).
+// rendezvous, after which every thread reads sm->merge_unit).  If the wait
+// for the ticket gives up, the launch's give-up flag is set and no merge is
+// made.
 __device__ __forceinline__ void publish_ticket(const ItemOut &io, ItemSmem *sm, int row, PendingTicket &pt)
 {
     if (row != 0)
         return;
     int u = -1;
-    if (pt.unit >= 0 && pt.old == io.n_split - 1) {
-        u = pt.unit;
-        io.counters[u] = 0;  // ready for the next launch
+    if (pt.unit >= 0) {
+        if (mbar_wait_bounded(&sm->tk_done, (pt.n - 1) & 1, io.abort, io.wait_ns) &&
+            *reinterpret_cast<volatile int *>(&sm->tk_old) == io.n_split - 1) {
+            u = pt.unit;
+            io.counters[u] = 0;  // ready for the next launch
+        }
+        pt.unit = -1;
     }
     sm->merge_unit = u;
+}
+
+// After the softmax warpgroup's last item (every thread, fused mode): tells
+// the ticket thread that no ticket follows.  The last ticket has been read
+// by then (finish_pending), so tk_unit is free.
+__device__ __forceinline__ void end_tickets(ItemSmem *sm, int row)
+{
+    if (row == 0)
+        *reinterpret_cast<volatile int *>(&sm->tk_unit) = -1;
+    mbar_arrive(&sm->tk_req);
 }
 
 // The end of an item for softmax thread `row` (warp q4 of the warpgroup):
@@ -234,16 +296,15 @@ __device__ __forceinline__ bool finish_item(const ItemOut &io, ItemSmem *sm, flo
     // (unit u = b * Hkv + kvh has output rows u * G .. u * G + G - 1)
     if (mu >= 0 && !merge_unit<G, OUT>(io, stage, q4, lane, (size_t)mu * G, group_sync))
         return false;
-    // This item's ticket.  The rendezvous orders the warpgroup's partial
-    // stores before thread 0's GPU-scope acquire-release increment, which
-    // publishes them to the merging CTA (and, for that CTA, acquires the
-    // others').  Its result is read at the next item's end.
-    if (!group_sync())
-        return false;
+    // This item's ticket: thread 0 names the unit and every thread arrives
+    // after its own partial stores; the ticket thread takes it.  Its result
+    // is read at the next item's end.
     if (row == 0) {
+        *reinterpret_cast<volatile int *>(&sm->tk_unit) = unit;
         pt.unit = unit;
-        pt.old = atomic_add_acq_rel_gpu(&io.counters[unit], 1);
+        ++pt.n;
     }
+    mbar_arrive(&sm->tk_req);
     return true;
 }
 

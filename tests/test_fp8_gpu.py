@@ -66,3 +66,52 @@ def test_fp8_varlen_nan_padding_and_unit_scales():
     # no scales: the bytes are the values
     out, lse = _run(x, k8, v8, None, None, seqlens=lens, out_dtype=torch.float32)
     _check(x, k8, v8, None, None, out, lse, bf16=False, seqlens=lens)
+
+
+# every E4M3 byte but the two NaN patterns: signed zeros, the subnormals
+# (k * 2^-9, k = 1..7) and +-448 included
+_FINITE_E4M3 = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+
+
+@pytest.mark.parametrize("G,out_dtype", [(1, torch.float32), (2, torch.bfloat16), (4, torch.float32)])
+def test_fp8_uniform_random_codes(G, out_dtype):
+    """K and V bytes drawn uniformly over the 254 finite E4M3 patterns, with
+    +-448 and the smallest subnormal also planted at fixed strides so that
+    every tile holds them; factors 2^-6 (K) and 2^-8 (V) keep the scores of
+    order one."""
+    w = synth.Workload("fp8", 2, "decode", 2, 2 * G, 2, 3001, 128, "bf16")
+    x = synth.make_inputs(w, seed=1600 + G)
+    rng = np.random.Generator(np.random.PCG64(93 + G))
+    shape = (2, 2, 3001, 128)
+    k8 = _FINITE_E4M3[rng.integers(0, _FINITE_E4M3.size, size=shape)]
+    v8 = _FINITE_E4M3[rng.integers(0, _FINITE_E4M3.size, size=shape)]
+    k8[:, :, ::97, 5] = 0x7E   # +448
+    k8[:, :, 1::89, 6] = 0xFE  # -448
+    v8[:, :, ::83, 7] = 0xFE
+    v8[:, :, 2::79, 8] = 0x7E
+    k8[:, :, 3::101, 9] = 0x01  # 2^-9
+    v8[:, :, 4::103, 10] = 0x81  # -2^-9
+    k8, v8 = torch.from_numpy(k8), torch.from_numpy(v8)
+    ks = torch.full((4,), 2.0 ** -6, dtype=torch.float32)
+    vs = torch.full((4,), 2.0 ** -8, dtype=torch.float32)
+    out, lse = _run(x, k8, v8, ks, vs, out_dtype=out_dtype)
+    _check(x, k8, v8, ks, vs, out, lse, bf16=out_dtype == torch.bfloat16)
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_fp8_flags_a_query_outside_fp16(G):
+    """Queries are used as fp16 values: 65280, the largest bf16 value below
+    2^16, fits; 2^16 and beyond do not, and record TA_DEVERR_RANGE."""
+    w = synth.Workload("fp8", 2, "decode", 2, 2 * G, 2, 1024, 128, "bf16")
+    x = synth.make_inputs(w, seed=1700 + G)
+    k8, ks = synth.to_e4m3(x["k"])
+    v8, vs = synth.to_e4m3(x["v"])
+    ta.decode_status()
+    for value, flagged in ((65280.0, False), (-65280.0, False), (65536.0, True), (-3.0e38, True)):
+        q = x["q"].clone()
+        q[1, 2 * G - 1, 77] = value
+        ta.decode_fp8(q.to(DEV), k8.to(DEV), v8.to(DEV), k_scale=ks.to(DEV), v_scale=vs.to(DEV), scale=x["scale"])
+        torch.cuda.synchronize()
+        st = ta.decode_status()
+        assert bool(st & ta.TA_DEVERR_RANGE) == flagged, (value, st)
+        assert st & ~ta.TA_DEVERR_RANGE == 0, st

@@ -131,6 +131,21 @@ def test_nvfp4_attends_exactly_the_keys_up_to_each_length():
         assert np.all(out[b, :, 2:] == 0.0)
 
 
+def test_nvfp4_flags_a_query_outside_fp16():
+    """As for the E4M3 cache: a query element of magnitude 2^16 or more (not an
+    fp16 value) records TA_DEVERR_RANGE; 65280 does not."""
+    w = synth.Workload("t", 9, "decode", 2, 8, 2, 2048, 128, "bf16")
+    x, c = _quantised_from(w)
+    ta.decode_status()
+    for value, flagged in ((65280.0, False), (65536.0, True)):
+        q = x["q"].clone()
+        q[0, 5, 100] = value
+        _run(dict(x, q=q), c)
+        st = ta.decode_status()
+        assert bool(st & ta.TA_DEVERR_RANGE) == flagged, (value, st)
+        assert st & ~ta.TA_DEVERR_RANGE == 0, st
+
+
 def test_nvfp4_rejects_unsupported_shapes():
     q = torch.zeros(1, 8, 128, dtype=torch.bfloat16, device=DEV)
     k4 = torch.zeros(1, 8, 1000, 64, dtype=torch.uint8, device=DEV)  # S not a multiple of 16
