@@ -90,6 +90,9 @@ constexpr uint32_t kOCol = 2 * kN;   // S at TMEM columns 0 and 16, O at 32 and 
 constexpr uint32_t kTmemCols = 128;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kRescaleLog2 = 8.0f;
+// partial outputs in flight per round of the fused merge (the register
+// budget of 256 threads allows sixteen float4, that of 384 threads eight)
+constexpr int kMergeBatch = 16;
 
 enum : int { kFirst = 1, kLast = 2, kEnd = 4 };
 constexpr int kModeFinal = tcd::kModeFinal, kModePartials = tcd::kModePartials, kModeFused = tcd::kModeFused;
@@ -714,12 +717,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 break;
 
             // ---- end of item: the partial, the result, and in fused mode the merge
-            if (!tcd::finish_item<G, OUT>(io, &ms->isum, stage_area, q4, lane, unit, split, b, kvh, 1.f, mw, l_run,
+            if (!tcd::finish_item<G, OUT, kMergeBatch>(io, &ms->isum, stage_area, q4, lane, unit, split, b, kvh, 1.f, mw, l_run,
                                           o, pt, group_sync))
                 break;
         }
         if (ended)
-            tcd::finish_pending<G, OUT>(io, &ms->isum, stage_area, q4, lane, pt, group_sync);
+            tcd::finish_pending<G, OUT, kMergeBatch>(io, &ms->isum, stage_area, q4, lane, pt, group_sync);
         if (p.mode == kModeFused)
             tcd::end_tickets(&ms->isum, row);
     } else if (warp == 3) {

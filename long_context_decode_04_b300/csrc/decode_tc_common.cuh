@@ -48,7 +48,7 @@ struct ItemOut {
 };
 
 template <int G>
-constexpr int stage_floats() { return 2 * G * kFusedMergeMaxSplits + 2 * G; }
+constexpr int stage_floats() { return G * kFusedMergeMaxSplits + 2 * G; }
 
 // Shared memory of the item end: the four warps' sums and references, the
 // ticket channel to the ticket thread, the decision of a deferred ticket
@@ -108,42 +108,59 @@ __device__ __forceinline__ void ticket_loop(const ItemOut &io, ItemSmem *sm)
 
 // The merge of a unit whose partials are all written: out = sum_n e^(m_n -
 // max) o_n / sum_n e^(m_n - max) l_n, lse = max + ln(that sum), over the
-// unit's ns partials of each of its G heads.  The G x ns references (natural
-// log) and sums are staged in shared memory in one round of loads; warp h
-// turns head h's references into weights and sums them; every thread then
-// adds its 4 output dimensions of all ns partials with independent loads.
-template <int G, typename OUT, typename Sync>
+// unit's ns partials of each of its G heads.  Warp h loads head h's
+// references (natural log) and sums and turns them into weights (kept in
+// shared memory) and the weighted sum; every thread adds its 4 output
+// dimensions of all ns partials, kBatch independent loads a round (as many
+// as the kernel's register budget allows), the first round issued before
+// the weights are known.
+template <int G, typename OUT, int kBatch, typename Sync>
 __device__ __forceinline__ bool merge_unit(const ItemOut &io, float *stage, int q4, int lane, size_t row0,
                                            Sync &&group_sync)
 {
     const int row = q4 * 32 + lane;
     const int ns = io.n_split;
+    constexpr int kCols = G * kD / 4;  // output columns of 4 dimensions
+    static_assert(kCols <= kSoftThreads && kFusedMergeMaxSplits <= 128, "one column a thread, 4 partials a lane");
 
-    float *sw = stage;               // [G][ns] references, then weights
-    float *sl = stage + G * ns;      // [G][ns] sums
-    float *shd = stage + 2 * G * ns; // [G][2] maximum, weighted sum
-    for (int i = row; i < G * ns; i += kSoftThreads) {
-        const size_t pi = row0 * ns + i;  // head i / ns, partial i % ns
-        sw[i] = __ldcg(io.part_m + pi);
-        sl[i] = __ldcg(io.part_l + pi);
+    float *sw = stage;          // [G][ns] weights
+    float *shd = stage + G * ns; // [G][2] maximum, weighted sum
+    // Thread `row` owns column `row` (head h, dimensions d4 .. d4 + 3).  Its
+    // first kBatch partial outputs are loaded before the weights are known,
+    // so that round trip overlaps the one of the references.
+    const bool has_col = row < kCols;
+    const int h = row / (kD / 4);
+    const int d4 = (row - h * (kD / 4)) * 4;
+    const float4 *po = reinterpret_cast<const float4 *>(io.part_o + (row0 + h) * ns * kD + d4);
+    float4 x[kBatch];
+    if (has_col) {
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+            x[i] = i < ns ? __ldcg(po + (size_t)i * (kD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (!group_sync())
-        return false;
+    // warp q4 < G: head q4's references and sums (at most four a lane) ->
+    // its maximum, the weights e^(m_n - max) and the weighted sum of l_n
     if (q4 < G) {
-        float *wh = sw + q4 * ns;
-        const float *lh = sl + q4 * ns;
-        float mx = -INFINITY;
-        for (int n = lane; n < ns; n += 32)
-            mx = fmaxf(mx, wh[n]);
+        const size_t base = (row0 + q4) * ns;
+        float mv[4], lv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int n = lane + 32 * k;
+            mv[k] = n < ns ? __ldcg(io.part_m + base + n) : -INFINITY;
+            lv[k] = n < ns ? __ldcg(io.part_l + base + n) : 0.f;
+        }
+        float mx = fmax3(mv[0], mv[1], fmaxf(mv[2], mv[3]));
 #pragma unroll
         for (int mask = 16; mask >= 1; mask >>= 1)
             mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, mask));
         float lsum = 0.f;
-        for (int n = lane; n < ns; n += 32) {
-            const float m = wh[n];
-            const float a = m == -INFINITY ? 0.f : fast_exp2((m - mx) * kLog2e);
-            wh[n] = a;
-            lsum = fmaf(a, lh[n], lsum);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int n = lane + 32 * k;
+            const float a = mv[k] == -INFINITY ? 0.f : fast_exp2((mv[k] - mx) * kLog2e);
+            if (n < ns)
+                sw[q4 * ns + n] = a;
+            lsum = fmaf(a, lv[k], lsum);
         }
 #pragma unroll
         for (int mask = 16; mask >= 1; mask >>= 1)
@@ -155,19 +172,10 @@ __device__ __forceinline__ bool merge_unit(const ItemOut &io, float *stage, int 
     }
     if (!group_sync())
         return false;
-    for (int idx = row; idx < G * kD / 4; idx += kSoftThreads) {
-        const int h = idx / (kD / 4);
-        const int d4 = (idx - h * (kD / 4)) * 4;
+    if (has_col) {
         const float *wh = sw + h * ns;
-        const float4 *po = reinterpret_cast<const float4 *>(io.part_o + (row0 + h) * ns * kD + d4);
         float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
-        // sixteen loads in flight per round (the partials come from L2)
-        constexpr int kBatch = 16;
-        for (int n0 = 0; n0 < ns; n0 += kBatch) {
-            float4 x[kBatch];
-#pragma unroll
-            for (int i = 0; i < kBatch; ++i)
-                x[i] = n0 + i < ns ? __ldcg(po + (size_t)(n0 + i) * (kD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int n0 = 0;;) {
 #pragma unroll
             for (int i = 0; i < kBatch; ++i) {
                 const float a = n0 + i < ns ? wh[n0 + i] : 0.f;
@@ -176,6 +184,12 @@ __device__ __forceinline__ bool merge_unit(const ItemOut &io, float *stage, int 
                 os.z = fmaf(a, x[i].z, os.z);
                 os.w = fmaf(a, x[i].w, os.w);
             }
+            n0 += kBatch;
+            if (n0 >= ns)
+                break;
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                x[i] = n0 + i < ns ? __ldcg(po + (size_t)(n0 + i) * (kD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         const float mx = shd[2 * h], lsum = shd[2 * h + 1];
         const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
@@ -230,7 +244,7 @@ __device__ __forceinline__ void end_tickets(ItemSmem *sm, int row)
 // output (a value dequantisation factor, 1 for bf16 caches).  group_sync()
 // is a rendezvous of the four warps that returns false when the launch gave
 // up.  Returns false on give-up.
-template <int G, typename OUT, typename Sync>
+template <int G, typename OUT, int kBatch, typename Sync>
 __device__ __forceinline__ bool finish_item(const ItemOut &io, ItemSmem *sm, float *stage, int q4, int lane, int unit,
                                             int split, int b, int kvh, float vscale, const float (&mw)[G],
                                             const float (&l_run)[G], const float (&o)[4][G], PendingTicket &pt,
@@ -294,7 +308,7 @@ __device__ __forceinline__ bool finish_item(const ItemOut &io, ItemSmem *sm, flo
     // the unit an earlier ticket found complete (read after the rendezvous)
     const int mu = *reinterpret_cast<volatile int *>(&sm->merge_unit);
     // (unit u = b * Hkv + kvh has output rows u * G .. u * G + G - 1)
-    if (mu >= 0 && !merge_unit<G, OUT>(io, stage, q4, lane, (size_t)mu * G, group_sync))
+    if (mu >= 0 && !merge_unit<G, OUT, kBatch>(io, stage, q4, lane, (size_t)mu * G, group_sync))
         return false;
     // This item's ticket: thread 0 names the unit and every thread arrives
     // after its own partial stores; the ticket thread takes it.  Its result
@@ -309,7 +323,7 @@ __device__ __forceinline__ bool finish_item(const ItemOut &io, ItemSmem *sm, flo
 }
 
 // After the last item: the decision of the last pending ticket, and its merge.
-template <int G, typename OUT, typename Sync>
+template <int G, typename OUT, int kBatch, typename Sync>
 __device__ __forceinline__ bool finish_pending(const ItemOut &io, ItemSmem *sm, float *stage, int q4, int lane,
                                                PendingTicket &pt, Sync &&group_sync)
 {
@@ -320,7 +334,7 @@ __device__ __forceinline__ bool finish_pending(const ItemOut &io, ItemSmem *sm, 
         return false;
     const int mu = *reinterpret_cast<volatile int *>(&sm->merge_unit);
     if (mu >= 0)
-        return merge_unit<G, OUT>(io, stage, q4, lane, (size_t)mu * G, group_sync);
+        return merge_unit<G, OUT, kBatch>(io, stage, q4, lane, (size_t)mu * G, group_sync);
     return true;
 }
 

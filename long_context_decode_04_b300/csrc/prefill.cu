@@ -14,7 +14,8 @@
 // (b, h) and walks the 128-key K/V tiles up to the causal diagonal:
 //   warp 8   TMA producer: loads both Q tiles once, then K tiles into a
 //            3-stage and V tiles into a 2-stage shared-memory ring (128-byte
-//            swizzle, two 64-column boxes per tile), K one tile ahead of V.
+//            swizzle, two 64-column boxes per tile), each ring refilled as
+//            soon as it has a free stage (a V tile never before its K tile).
 //            It also allocates and frees the TMEM.
 //   warp 9   MMA issuer (one thread): per K tile j and query tile t,
 //              PV_t(j-1): O_t += P_t(j-1) V_{j-1}  (P from TMEM, V MN-major)
@@ -244,35 +245,63 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                     tc::tma_load_3d(dst + kHalfBytes, &p.qmap, 64, y0 + q0 + t * kBM, zq, &bars->q_full);
                 }
             }
-            // Issue order K0, K1, V0, K2, V1, ...: K runs one tile ahead of
-            // V, since S of a tile needs K while its PV comes a softmax later.
+            // K and V tiles each go as soon as their own ring has a free
+            // stage (V tile j never before K tile j): a K tile is needed by
+            // the score product of its step, while the V ring frees only
+            // after the value product of two steps back, so a K copy must
+            // not queue behind a V stage.  The thread polls both rings and
+            // naps briefly when neither moved; it gives up when nothing moved
+            // for the launch's time limit or another role gave up.
             int k_armed[kKStages] = {0, 0, 0}, v_armed[kVStages] = {0, 0};
             bool ok = go;
-            for (int i = 0; ok && i <= nk; ++i) {
-                if (i < nk) {  // K tile i
-                    const int st = i % kKStages, use = i / kKStages;
-                    if (use > 0 && !mbar_wait_bounded(&bars->k_empty[st], (use - 1) & 1, abort_flag, p.wait_ns)) {
-                        ok = false;
-                        break;
+            int kn = 0, vn = 0;  // next K tile, next V tile
+            uint64_t idle_since = 0;
+            uint32_t spins = 0;
+            while (ok && vn < nk) {
+                bool moved = false;
+                if (kn < nk) {
+                    const int st = kn % kKStages, use = kn / kKStages;
+                    if (use == 0 || mbar_test_wait(&bars->k_empty[st], (use - 1) & 1)) {
+                        unsigned char *kd = smem + kKOff + st * kTileBytes;
+                        mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
+                        tc::tma_load_3d(kd, &p.kmap, 0, y0 + kn * kBN, zkv, &bars->k_full[st]);
+                        tc::tma_load_3d(kd + kHalfBytes, &p.kmap, 64, y0 + kn * kBN, zkv, &bars->k_full[st]);
+                        ++k_armed[st];
+                        ++kn;
+                        moved = true;
                     }
-                    unsigned char *kd = smem + kKOff + st * kTileBytes;
-                    mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-                    tc::tma_load_3d(kd, &p.kmap, 0, y0 + i * kBN, zkv, &bars->k_full[st]);
-                    tc::tma_load_3d(kd + kHalfBytes, &p.kmap, 64, y0 + i * kBN, zkv, &bars->k_full[st]);
-                    ++k_armed[st];
                 }
-                if (i > 0) {  // V tile i - 1
-                    const int j = i - 1;
-                    const int st = j % kVStages, use = j / kVStages;
-                    if (use > 0 && !mbar_wait_bounded(&bars->v_empty[st], (use - 1) & 1, abort_flag, p.wait_ns)) {
+                if (vn < kn) {
+                    const int st = vn % kVStages, use = vn / kVStages;
+                    if (use == 0 || mbar_test_wait(&bars->v_empty[st], (use - 1) & 1)) {
+                        unsigned char *vd = smem + kVOff + st * kTileBytes;
+                        mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
+                        tc::tma_load_3d(vd, &p.vmap, 0, y0 + vn * kBN, zkv, &bars->v_full[st]);
+                        tc::tma_load_3d(vd + kHalfBytes, &p.vmap, 64, y0 + vn * kBN, zkv, &bars->v_full[st]);
+                        ++v_armed[st];
+                        ++vn;
+                        moved = true;
+                    }
+                }
+                if (moved) {
+                    idle_since = 0;
+                    spins = 0;
+                    continue;
+                }
+                __nanosleep(64);
+                if ((++spins & 15) == 0) {
+                    if (*abort_flag) {
                         ok = false;
                         break;
                     }
-                    unsigned char *vd = smem + kVOff + st * kTileBytes;
-                    mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-                    tc::tma_load_3d(vd, &p.vmap, 0, y0 + j * kBN, zkv, &bars->v_full[st]);
-                    tc::tma_load_3d(vd + kHalfBytes, &p.vmap, 64, y0 + j * kBN, zkv, &bars->v_full[st]);
-                    ++v_armed[st];
+                    const uint64_t now = globaltimer_ns();
+                    if (idle_since == 0) {
+                        idle_since = now;
+                    } else if (now - idle_since > p.wait_ns) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
                 }
             }
             {
