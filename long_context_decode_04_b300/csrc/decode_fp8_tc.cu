@@ -820,7 +820,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                 break;
         }
         if (ended)
-            tcd::finish_pending<G, OUT, kMergeBatch>(io, &ms->isum, stage_area, q4, lane, pt, group_sync);
+            tcd::finish_pending<G, OUT, kMergeBatch>(io, &ms->isum, stage_area, q4, lane, pt, group_sync, smem + kRawOff,
+                                                     (size_t)kRawRegion);
         if (p.mode == kModeFused)
             tcd::end_tickets(&ms->isum, row);
     } else if (warp == 3) {

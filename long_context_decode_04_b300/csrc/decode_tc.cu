@@ -722,7 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 break;
         }
         if (ended)
-            tcd::finish_pending<G, OUT, kMergeBatch>(io, &ms->isum, stage_area, q4, lane, pt, group_sync);
+            tcd::finish_pending<G, OUT, kMergeBatch>(io, &ms->isum, stage_area, q4, lane, pt, group_sync, smem,
+                                                     (size_t)kStages * kStageBytes);
         if (p.mode == kModeFused)
             tcd::end_tickets(&ms->isum, row);
     } else if (warp == 3) {

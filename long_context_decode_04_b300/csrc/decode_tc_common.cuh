@@ -58,6 +58,7 @@ constexpr int stage_floats() { return G * kFusedMergeMaxSplits + 2 * G; }
 struct ItemSmem {
     uint64_t tk_req;   // a ticket asked for: the 128 softmax threads, each after its partial stores
     uint64_t tk_done;  // the ticket is taken and its result is in tk_old (the ticket thread)
+    uint64_t mg_bar;   // the last merge's partial outputs landed (one bulk copy, phase 0 only)
     float lred[4][4];  // [warp][head] weight sums
     float mred[4][4];  // [warp][head] references
     int merge_unit;    // unit whose partials are all written (-1: none)
@@ -71,6 +72,7 @@ __device__ __forceinline__ void init_item_smem(ItemSmem *sm)
 {
     mbar_init(&sm->tk_req, kSoftThreads);
     mbar_init(&sm->tk_done, 1);
+    mbar_init(&sm->mg_bar, 1);
     sm->merge_unit = -1;
     sm->tk_unit = -1;
 }
@@ -114,9 +116,14 @@ __device__ __forceinline__ void ticket_loop(const ItemOut &io, ItemSmem *sm)
 // dimensions of all ns partials, kBatch independent loads a round (as many
 // as the kernel's register budget allows), the first round issued before
 // the weights are known.
+//
+// After the CTA's last item its copy ring is idle: there (bulk != nullptr,
+// room for the G x ns partial outputs) the outputs come by one bulk copy
+// into shared memory, issued before the weights are computed, instead of
+// rounds of loads.
 template <int G, typename OUT, int kBatch, typename Sync>
-__device__ __forceinline__ bool merge_unit(const ItemOut &io, float *stage, int q4, int lane, size_t row0,
-                                           Sync &&group_sync)
+__device__ __forceinline__ bool merge_unit(const ItemOut &io, ItemSmem *sm, float *stage, int q4, int lane,
+                                           size_t row0, Sync &&group_sync, unsigned char *bulk = nullptr)
 {
     const int row = q4 * 32 + lane;
     const int ns = io.n_split;
@@ -133,7 +140,17 @@ __device__ __forceinline__ bool merge_unit(const ItemOut &io, float *stage, int 
     const int d4 = (row - h * (kD / 4)) * 4;
     const float4 *po = reinterpret_cast<const float4 *>(io.part_o + (row0 + h) * ns * kD + d4);
     float4 x[kBatch];
-    if (has_col) {
+    if (bulk) {
+        if (row == 0) {
+            // The copy runs in the async proxy: this fence orders before it the
+            // ring's last generic-proxy accesses and the other CTAs' partial
+            // stores, which the ticket's acquire made visible to this thread.
+            asm volatile("fence.proxy.async;" ::: "memory");
+            const uint32_t bytes = (uint32_t)(G * ns * kD * sizeof(float));
+            mbar_arrive_expect_tx(&sm->mg_bar, bytes);
+            bulk_copy_g2s(bulk, io.part_o + row0 * ns * kD, bytes, &sm->mg_bar);
+        }
+    } else if (has_col) {
 #pragma unroll
         for (int i = 0; i < kBatch; ++i)
             x[i] = i < ns ? __ldcg(po + (size_t)i * (kD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -172,7 +189,31 @@ __device__ __forceinline__ bool merge_unit(const ItemOut &io, float *stage, int 
     }
     if (!group_sync())
         return false;
-    if (has_col) {
+    if (bulk && !mbar_wait_bounded(&sm->mg_bar, 0, io.abort, io.wait_ns))
+        return false;
+    if (has_col && bulk) {
+        const float *wh = sw + h * ns;
+        const float4 *so = reinterpret_cast<const float4 *>(bulk) + h * ns * (kD / 4) + d4 / 4;
+        float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int n = 0; n < ns; ++n) {
+            const float4 y = so[n * (kD / 4)];
+            const float a = wh[n];
+            os.x = fmaf(a, y.x, os.x);
+            os.y = fmaf(a, y.y, os.y);
+            os.z = fmaf(a, y.z, os.z);
+            os.w = fmaf(a, y.w, os.w);
+        }
+        const float mx = shd[2 * h], lsum = shd[2 * h + 1];
+        const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+        OUT *dst = static_cast<OUT *>(io.out) + (row0 + h) * kD + d4;
+        store_out(dst + 0, os.x * inv);
+        store_out(dst + 1, os.y * inv);
+        store_out(dst + 2, os.z * inv);
+        store_out(dst + 3, os.w * inv);
+        if (d4 == 0 && io.lse)
+            io.lse[row0 + h] = lsum > 0.f ? mx + fast_log2(lsum) * kLn2 : -INFINITY;
+    } else if (has_col) {
         const float *wh = sw + h * ns;
         float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int n0 = 0;;) {
@@ -308,7 +349,7 @@ __device__ __forceinline__ bool finish_item(const ItemOut &io, ItemSmem *sm, flo
     // the unit an earlier ticket found complete (read after the rendezvous)
     const int mu = *reinterpret_cast<volatile int *>(&sm->merge_unit);
     // (unit u = b * Hkv + kvh has output rows u * G .. u * G + G - 1)
-    if (mu >= 0 && !merge_unit<G, OUT, kBatch>(io, stage, q4, lane, (size_t)mu * G, group_sync))
+    if (mu >= 0 && !merge_unit<G, OUT, kBatch>(io, sm, stage, q4, lane, (size_t)mu * G, group_sync))
         return false;
     // This item's ticket: thread 0 names the unit and every thread arrives
     // after its own partial stores; the ticket thread takes it.  Its result
@@ -322,10 +363,13 @@ __device__ __forceinline__ bool finish_item(const ItemOut &io, ItemSmem *sm, flo
     return true;
 }
 
-// After the last item: the decision of the last pending ticket, and its merge.
+// After the last item: the decision of the last pending ticket, and its
+// merge (through `ring`, the idle copy ring of ring_bytes, when the unit's
+// partial outputs fit there).
 template <int G, typename OUT, int kBatch, typename Sync>
 __device__ __forceinline__ bool finish_pending(const ItemOut &io, ItemSmem *sm, float *stage, int q4, int lane,
-                                               PendingTicket &pt, Sync &&group_sync)
+                                               PendingTicket &pt, Sync &&group_sync, unsigned char *ring,
+                                               size_t ring_bytes)
 {
     if (io.mode != kModeFused)
         return true;
@@ -333,8 +377,17 @@ __device__ __forceinline__ bool finish_pending(const ItemOut &io, ItemSmem *sm, 
     if (!group_sync())
         return false;
     const int mu = *reinterpret_cast<volatile int *>(&sm->merge_unit);
-    if (mu >= 0)
-        return merge_unit<G, OUT, kBatch>(io, stage, q4, lane, (size_t)mu * G, group_sync);
+    if (mu >= 0) {
+        const bool fits = (size_t)G * io.n_split * kD * sizeof(float) <= ring_bytes;
+        const bool ok = merge_unit<G, OUT, kBatch>(io, sm, stage, q4, lane, (size_t)mu * G, group_sync,
+                                                   fits ? ring : nullptr);
+        if (fits) {
+            // the copy lands before the CTA leaves, even when the merge gave up
+            int drain_abort = 0;
+            mbar_wait_bounded(&sm->mg_bar, 0, &drain_abort);
+        }
+        return ok;
+    }
     return true;
 }
 
