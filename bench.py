@@ -238,11 +238,14 @@ def measure_pi(ta, accounting, peaks, dev, w, q, k, v, window=4096, period=64, r
             "frac": round(gbs / peaks["hbm_gbs"], 4)}
 
 
-def measure_other_configs(ta, synth, accounting, peaks, dev, reps=20):
+def measure_other_configs(ta, synth, accounting, peaks, dev, reps=7, inner=10):
     """Decode of the single-head fp32 workload (4096 keys, D = 64) and of the
     1M-key GQA workload with its forced 256-key chunks (4096 splits, merged in
-    two levels by the merge kernel): median of `reps` graph replays each, all
-    KV bytes."""
+    two levels by the merge kernel): the median over `reps` groups of the mean
+    of `inner` back-to-back graph replays (a group between two events, so the
+    events' resolution does not bound a short launch), all KV bytes; the
+    first-level partials (m, l, o written by the split phase and read back by
+    the merge) are reported beside them."""
     import torch
     res = {}
     for name in ("single_head_d64_s4096_f32", "gqa_32x8_d128_s1048576_c256"):
@@ -270,16 +273,20 @@ def measure_other_configs(ta, synth, accounting, peaks, dev, reps=20):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         for a, b in ev:
             a.record(stream)
-            g.replay()
+            for _ in range(inner):
+                g.replay()
             b.record(stream)
         torch.cuda.synchronize()
-        us = sorted(1e3 * a.elapsed_time(b) for a, b in ev)[reps // 2]
+        us = sorted(1e3 * a.elapsed_time(b) / inner for a, b in ev)[reps // 2]
         gbs = kv_bytes / (us / 1e6) / 1e9
+        pbytes = accounting.partial_bytes(w.B, w.Hq, plan.n_split, w.D) if plan.n_split > 1 else 0
         res[name] = {"workload": f"B={w.B}, Hq={w.Hq}, Hkv={w.Hkv}, D={w.D}, S={w.S}, {w.dtype}",
                      "n_split": plan.n_split, "chunk": plan.chunk,
                      "launches": 1 + plan.levels,
                      "kv_bytes": kv_bytes, "us": round(us, 2), "gbs": round(gbs, 1),
-                     "frac": round(gbs / peaks["hbm_gbs"], 4)}
+                     "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "partial_bytes": pbytes,
+                     "frac_with_partials": round((kv_bytes + pbytes) / (us / 1e6) / 1e9 / peaks["hbm_gbs"], 4)}
         del q, k, v, ws, out, lse, g
         torch.cuda.empty_cache()
     return res
