@@ -328,6 +328,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
             constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kBM, kBN, false);
             constexpr uint32_t kIdescPV = tc::idesc_f16_f32(kBM, kHD, true);
             const uint32_t sbase = smem_u32(smem);
+            // Matrix descriptors of the tiles' first K steps; a later step or
+            // stage adds its byte offset / 16 to the start-address field (the
+            // addresses stay below 256 KiB, so the field never carries).  The
+            // tensor pipe takes only a few operations ahead of this thread, so
+            // every instruction it spends between two MMAs can leave the pipe
+            // idle: nothing is recomputed per MMA.
+            const uint64_t qdesc0 = tc::sw128_desc(sbase + kQOff, 16, 1024);
+            const uint64_t kdesc0 = tc::sw128_desc(sbase + kKOff, 16, 1024);
+            const uint64_t vdesc0 = tc::sw128_desc(sbase + kVOff, kHalfBytes, 1024);
             bool ok = mbar_wait_bounded(&bars->q_full, 0, abort_flag, p.wait_ns);
             tc::fence_after_sync();
             for (int j = 0; ok && j <= nk; ++j) {
@@ -355,27 +364,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                         if (!ok)
                             break;
                         tc::fence_after_sync();
-                        const uint32_t vb = sbase + kVOff + ((j - 1) % kVStages) * kTileBytes;
+                        const uint64_t vdesc = vdesc0 + (uint64_t)(((j - 1) % kVStages) * (kTileBytes >> 4));
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk) {
                             // B = V rows [16kk, 16kk+16): MN-major, the two
                             // 64-column halves are 16 KiB apart (LBO), 8-key
                             // groups 1 KiB apart (SBO).
-                            const uint64_t bdesc = tc::sw128_desc(vb + kk * 2048, kHalfBytes, 1024);
-                            tc::mma_ts(o_tmem, s_tmem + kk * 8, bdesc, kIdescPV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+                            tc::mma_ts(o_tmem, s_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), kIdescPV,
+                                       (j - 1 > 0 || kk > 0) ? 1u : 0u);
                         }
                         if (j > diag)
                             tc::commit(&bars->o_full[t]);  // last PV of this tile
                     }
                     if (j < nk && t_active && j <= diag) {
                         // S_t = Q_t K_j^T
-                        const uint32_t qb = sbase + kQOff + t * kTileBytes;
-                        const uint32_t kb = sbase + kKOff + st * kTileBytes;
+                        const uint64_t qdesc = qdesc0 + (uint64_t)(t * (kTileBytes >> 4));
+                        const uint64_t kdesc = kdesc0 + (uint64_t)(st * (kTileBytes >> 4));
 #pragma unroll
                         for (int kk = 0; kk < kHD / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                            tc::mma_ss(s_tmem, tc::sw128_desc(qb + off, 16, 1024), tc::sw128_desc(kb + off, 16, 1024),
-                                       kIdescS, kk > 0 ? 1u : 0u);
+                            const uint64_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                            tc::mma_ss(s_tmem, qdesc + off, kdesc + off, kIdescS, kk > 0 ? 1u : 0u);
                         }
                         tc::commit(&bars->s_full[t]);
                     }
