@@ -458,10 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                     const uint32_t s_tm = tmem + (t & 1) * kN;
                     const uint32_t k_tm = tmem + kKCol + (t % kConvBufs) * (kD / 2);
                     const uint32_t qa = sbase + kQOff + qb * kQBytes;
+                    // descriptor of the first K step; a later step adds its
+                    // offset / 16 to the start-address field (no carry below
+                    // 256 KiB), so no MMA rebuilds one
+                    const uint64_t qdesc = tc::sw128_desc(qa, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk) {
                         const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
-                        tc::mma_ts(s_tm, k_tm + kk * 8, tc::sw128_desc(qa + qo, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                        tc::mma_ts(s_tm, k_tm + kk * 8, qdesc + (qo >> 4), kIdS, kk > 0 ? 1u : 0u);
                     }
                     // the commit arrives when S is in TMEM; the plain arrive
                     // releases the descriptor this thread acquired
@@ -487,6 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
                     const uint32_t vb = sbase + kVOff + (t % kConvBufs) * kVBytes;
                     const uint32_t pb = sbase + kPOff + (t & 1) * kPBytes;
                     bool ok = true;
+                    const uint64_t vdesc = tc::sw128_desc(vb, kHalf, 1024), pdesc = tc::sw128_desc(pb, 16, 1024);
 #pragma unroll
                     for (int w = 0; w < 4 && ok; ++w) {
                         ok = mbar_wait_bounded(&ms->p_full[t & 1][w], (t >> 1) & 1, abort_flag, p.wait_ns);
@@ -496,9 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_tc_kernel(const __grid
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
                             const int kk = 2 * w + i;
-                            const uint64_t a = tc::sw128_desc(vb + kk * 2048, kHalf, 1024);
                             const uint32_t po = (kk >> 2) * kPHalf + (kk & 3) * 32;
-                            tc::mma_ss(o_tm, a, tc::sw128_desc(pb + po, 16, 1024), kIdPV, kk > 0 ? 1u : 0u);
+                            tc::mma_ss(o_tm, vdesc + (uint64_t)(kk * (2048 >> 4)), pdesc + (po >> 4), kIdPV,
+                                       kk > 0 ? 1u : 0u);
                         }
                     }
                     if (!ok)

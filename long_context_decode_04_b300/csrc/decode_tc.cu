@@ -487,12 +487,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     const uint32_t s_tm = tmem + (t & 1) * kN;
                     const uint32_t kb = sbase + stage * kStageBytes;
                     const uint32_t qa = sbase + kQOff + qb * kQBytes;
+                    // descriptors of the first K step; a later step adds its
+                    // offset / 16 to the start-address field (no carry below
+                    // 256 KiB), so no MMA rebuilds one
+                    const uint64_t kdesc = tc::sw128_desc(kb, 16, 1024), qdesc = tc::sw128_desc(qa, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk) {
                         const uint32_t ko = (kk >> 2) * kHalf + (kk & 3) * 32;
                         const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
-                        tc::mma_ss(s_tm, tc::sw128_desc(kb + ko, 16, 1024), tc::sw128_desc(qa + qo, 16, 1024), kIdS,
-                                   kk > 0 ? 1u : 0u);
+                        tc::mma_ss(s_tm, kdesc + (ko >> 4), qdesc + (qo >> 4), kIdS, kk > 0 ? 1u : 0u);
                     }
                     tc::commit(&ms->s_full[t & 1]);
                     if (d.flags & kLast) {
@@ -522,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     const uint32_t vb = sbase + stage * kStageBytes + kTileBytes;
                     const uint32_t pb = sbase + kPOff + (t & 1) * kPBytes;
                     bool ok = true;
+                    const uint64_t vdesc = tc::sw128_desc(vb, kHalf, 1024), pdesc = tc::sw128_desc(pb, 16, 1024);
 #pragma unroll
                     for (int w = 0; w < 4 && ok; ++w) {
                         ok = mbar_wait_bounded(&ms->p_full[t & 1][w], (t >> 1) & 1, abort_flag, p.wait_ns);
@@ -531,9 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
                             const int kk = 2 * w + i;
-                            const uint64_t a = tc::sw128_desc(vb + kk * 2048, kHalf, 1024);
                             const uint32_t po = (kk >> 2) * kPHalf + (kk & 3) * 32;
-                            tc::mma_ss(o_tm, a, tc::sw128_desc(pb + po, 16, 1024), kIdPV, kk > 0 ? 1u : 0u);
+                            tc::mma_ss(o_tm, vdesc + (uint64_t)(kk * (2048 >> 4)), pdesc + (po >> 4), kIdPV,
+                                       kk > 0 ? 1u : 0u);
                         }
                     }
                     if (!ok)
