@@ -1,6 +1,6 @@
 // decode_tc_common.cuh -- the end of a work item, shared by the two
 // tensor-core decodes (decode_tc.cu: bf16 cache; decode_fp8_tc.cu: E4M3
-// cache).
+// and NVFP4 caches).
 //
 // Both kernels run a warpgroup of four softmax warps; warp w keeps, for
 // each of the G query heads of the item's KV head, its own running
@@ -52,9 +52,10 @@ constexpr int stage_floats() { return G * kFusedMergeMaxSplits + 2 * G; }
 
 // Shared memory of the item end: the four warps' sums and references, the
 // ticket channel to the ticket thread, the decision of a deferred ticket
-// (below), and the merge's staging area.  (The staging area is its own: the
-// weight buffers of the value product are not free for it, since the
-// entries of a warp's rows outside its own 32 keys must stay zero.)
+// (below), and the merge's area for the weights of the partials.  (The area
+// is its own: the weight buffers of the value product are not free for it,
+// since the entries of a warp's rows outside its own 32 keys must stay
+// zero.)
 struct ItemSmem {
     uint64_t tk_req;   // a ticket asked for: the 128 softmax threads, each after its partial stores
     uint64_t tk_done;  // the ticket is taken and its result is in tk_old (the ticket thread)

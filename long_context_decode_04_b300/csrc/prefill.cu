@@ -161,6 +161,62 @@ __device__ __forceinline__ uint4 out_pack4(const float *x, __nv_bfloat16 *)
                       tc::pack_bf16x2(x[6], x[7]));
 }
 
+// Eight score-product MMAs (K steps of 16) in one asm block: the predicate
+// of the accumulate flag is set once, and steps 1-7 add their offsets (in
+// 16-byte units of the start-address field) to the first step's
+// descriptors.  Steps: (kk >> 2) * 16 KiB + (kk & 3) * 32 bytes.
+__device__ __forceinline__ void mma_ss_x8(uint32_t d, uint64_t a0, uint64_t b0, uint32_t idesc, uint32_t acc0)
+{
+    asm volatile(
+        "{\n\t.reg .pred p0, p1;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.ne.b32 p1, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+        "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, 1024;\n\tadd.s64 b, %2, 1024;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, 1026;\n\tadd.s64 b, %2, 1026;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, 1028;\n\tadd.s64 b, %2, 1028;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, 1030;\n\tadd.s64 b, %2, 1030;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t}"
+        ::"r"(d), "l"(a0), "l"(b0), "r"(idesc), "r"(acc0), "r"(1u)
+        : "memory");
+}
+
+// Eight value-product MMAs: A (P) from TMEM columns a + 8 kk, B (V) steps of
+// 2 KiB (128 in 16-byte units).
+__device__ __forceinline__ void mma_ts_x8(uint32_t d, uint32_t a0, uint64_t b0, uint32_t idesc, uint32_t acc0)
+{
+    asm volatile(
+        "{\n\t.reg .pred p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.ne.b32 p1, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 32;\n\tadd.s64 b, %2, 512;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 40;\n\tadd.s64 b, %2, 640;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 48;\n\tadd.s64 b, %2, 768;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 56;\n\tadd.s64 b, %2, 896;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t}"
+        ::"r"(d), "r"(a0), "l"(b0), "r"(idesc), "r"(acc0), "r"(1u)
+        : "memory");
+}
+
 template <typename OUT>
 __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __grid_constant__ PrefillParams p)
 {
@@ -365,14 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                             break;
                         tc::fence_after_sync();
                         const uint64_t vdesc = vdesc0 + (uint64_t)(((j - 1) % kVStages) * (kTileBytes >> 4));
-#pragma unroll
-                        for (int kk = 0; kk < kBN / 16; ++kk) {
-                            // B = V rows [16kk, 16kk+16): MN-major, the two
-                            // 64-column halves are 16 KiB apart (LBO), 8-key
-                            // groups 1 KiB apart (SBO).
-                            tc::mma_ts(o_tmem, s_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), kIdescPV,
-                                       (j - 1 > 0 || kk > 0) ? 1u : 0u);
-                        }
+                        // B = V rows [16kk, 16kk+16): MN-major, the two
+                        // 64-column halves are 16 KiB apart (LBO), 8-key
+                        // groups 1 KiB apart (SBO).
+                        mma_ts_x8(o_tmem, s_tmem, vdesc, kIdescPV, j - 1 > 0 ? 1u : 0u);
                         if (j > diag)
                             tc::commit(&bars->o_full[t]);  // last PV of this tile
                     }
@@ -380,11 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_causal_kernel(const __gri
                         // S_t = Q_t K_j^T
                         const uint64_t qdesc = qdesc0 + (uint64_t)(t * (kTileBytes >> 4));
                         const uint64_t kdesc = kdesc0 + (uint64_t)(st * (kTileBytes >> 4));
-#pragma unroll
-                        for (int kk = 0; kk < kHD / 16; ++kk) {
-                            const uint64_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-                            tc::mma_ss(s_tmem, qdesc + off, kdesc + off, kIdescS, kk > 0 ? 1u : 0u);
-                        }
+                        mma_ss_x8(s_tmem, qdesc, kdesc, kIdescS, 0u);
                         tc::commit(&bars->s_full[t]);
                     }
                 }
