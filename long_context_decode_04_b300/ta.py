@@ -210,7 +210,8 @@ def decode_fp8(q, k8, v8, *, k_scale=None, v_scale=None, seqlens=None, scale=Non
                n_split=0, workspace=None, out=None, lse=None, wait_limit_ns=0):
     """Decode over an E4M3 KV cache.  q [B,Hq,D] bf16; k8/v8 [B,Hkv,S,D] uint8
     (E4M3 bit patterns); k_scale/v_scale [B*Hkv] fp32 or None.  Returns
-    (out, lse)."""
+    (out, lse).  The queries are used as fp16 values: an element of magnitude
+    2^16 or more sets TA_DEVERR_RANGE (read with decode_status)."""
     B, Hq, D = q.shape
     out_dtype = q.dtype if out_dtype is None else out_dtype
     if out is None:
@@ -228,7 +229,8 @@ def decode_nvfp4(q, k4, v4, k_bs, v_bs, *, k_factor=None, v_factor=None, seqlens
     """Decode over an NVFP4 KV cache.  q [B,Hq,D] bf16; k4/v4 [B,Hkv,S,D/2] uint8
     (E2M1 codes, even element in the low nibble); k_bs/v_bs [B,Hkv,S,D/16] uint8
     (E4M3 block scales); k_factor/v_factor [B*Hkv] fp32 or None.  Returns (out,
-    lse)."""
+    lse).  As for decode_fp8, a query element of magnitude 2^16 or more sets
+    TA_DEVERR_RANGE."""
     B, Hq, D = q.shape
     out_dtype = q.dtype if out_dtype is None else out_dtype
     if out is None:
